@@ -1,0 +1,443 @@
+"""Pins of the CPU oracle to facts that do not come from the oracle itself.
+
+Each test ties one oracle function to something independent of it: values
+written out by hand from the format definitions (tests/golden/), closed-form
+invariants, special cases that reduce to a library routine, or brute force on
+tiny inputs.  The cases are chosen so that a plausible slip anywhere in the
+oracle (a swapped nibble, a wrong scale offset, an off-by-one in the causal
+bound, a dropped sign, K used for V, a transposed block table) fails one.
+"""
+import math
+import os
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from mxfp4_sparse_paged_gb300 import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _lines(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        for ln in f:
+            ln = ln.split("#", 1)[0].strip()
+            if ln:
+                yield ln
+
+
+# ---------------------------------------------------------------- formats
+
+def test_e2m1_table_all_codes():
+    seen = 0
+    for ln in _lines("e2m1_values.txt"):
+        code, val = ln.split()
+        got = oracle.e2m1_value(int(code))
+        want = float(val)
+        assert got == want and math.copysign(1, got) == math.copysign(1, want), code
+        seen += 1
+    assert seen == 16
+
+
+def test_e8m0_values():
+    for ln in _lines("e8m0_values.txt"):
+        b, val = ln.split()
+        got = oracle.e8m0_value(int(b))
+        if val == "nan":
+            assert math.isnan(got)
+        else:
+            assert got == float(val), b
+
+
+def test_e2m1_rounding_midpoints():
+    n = 0
+    for ln in _lines("e2m1_rounding.txt"):
+        y, code = ln.split()
+        assert oracle.round_magnitude(float(y)) == int(code), y
+        n += 1
+    assert n >= 28
+
+
+def test_block_exponent_special_cases():
+    # power-of-two amax: floor(log2) exact
+    assert oracle.block_exponent(1.0) == -2
+    assert oracle.block_exponent(2.0) == -1
+    assert oracle.block_exponent(4.0) == 0
+    # just below a power of two
+    assert oracle.block_exponent(float(np.nextafter(np.float32(2.0), np.float32(0)))) == -2
+    assert oracle.block_exponent(6.0) == 0
+    assert oracle.block_exponent(7.99) == 0
+    assert oracle.block_exponent(8.0) == 1
+    assert oracle.block_exponent(0.0) == -127
+    # smallest fp32 normal / subnormal clamp to -127
+    assert oracle.block_exponent(2.0 ** -126) == -127
+    assert oracle.block_exponent(2.0 ** -140) == -127
+    assert oracle.block_exponent(2.0 ** -125) == -127   # -125 - 2 = -127: at the bound
+    assert oracle.block_exponent(2.0 ** -124) == -126   # inside the range
+    # largest finite fp32: floor(log2) = 127 -> 125
+    assert oracle.block_exponent(float(np.finfo(np.float32).max)) == 125
+
+
+def test_block_exponent_generic_range():
+    # E = floor(log2 a) - 2 for random normal magnitudes, checked with exact ints
+    rng = np.random.default_rng(7)
+    for e in range(-120, 127, 7):
+        for f in rng.uniform(1.0, 2.0, 5):
+            a = float(np.float32(f * 2.0 ** e))
+            if a >= 2.0 ** (e + 1):
+                continue
+            assert oracle.block_exponent(a) == max(-127, e - 2)
+
+
+def _parse_blocks():
+    cases, cur = [], None
+    for ln in _lines("quantize_blocks.txt"):
+        key, rest = ln.split(None, 1)
+        if key == "case":
+            cur = {"name": rest, "x": np.zeros(128, np.float32)}
+            cases.append(cur)
+        elif key == "x":
+            for item in rest.split():
+                i, v = item.split("=")
+                cur["x"][int(i)] = np.float32(float(v))
+        elif key == "scale":
+            cur["scale"] = [int(h, 16) for h in rest.split()]
+        elif key == "data":
+            d = [int(h, 16) for h in rest.split()]
+            cur["data"] = d + [0] * (64 - len(d))
+    return cases
+
+
+@pytest.mark.parametrize("case", _parse_blocks(), ids=lambda c: c["name"])
+def test_hand_worked_rows(case):
+    data, scale = oracle.quantize_row(case["x"])
+    assert list(scale) == case["scale"]
+    assert list(data) == case["data"]
+
+
+def test_error_bound_closed_form():
+    # |y - q(y)| <= half the local grid spacing: 0.25 on [0,2], 0.5 on (2,4],
+    # 1 on (4,6], < 2 in saturation (6,8); y = x / 2^E.
+    rng = np.random.default_rng(11)
+    for trial in range(300):
+        sc = float(2.0 ** rng.integers(-30, 30))
+        x = (rng.standard_normal(32) * sc).astype(np.float32)
+        if trial % 3 == 0:
+            x[rng.integers(32)] *= 20
+        codes, sb = oracle.quantize_block(x)
+        E = sb - 127
+        for xi, c in zip(x, codes):
+            y = abs(float(xi)) / 2.0 ** E
+            qv = abs(oracle.e2m1_value(int(c)))
+            bound = 0.25 if y <= 2 else 0.5 if y <= 4 else 1.0 if y <= 6 else 2.0
+            assert abs(y - qv) <= bound
+            assert y < 8
+            if qv != 0:
+                assert (int(c) >> 3) == (1 if xi < 0 else 0)
+
+
+def test_representable_values_roundtrip_exactly():
+    # A block whose values are grid values times 2^E, with the largest magnitude in
+    # [4, 6] so floor(log2 amax) = E + 2, quantises to exactly those codes.
+    rng = np.random.default_rng(5)
+    grid = np.array([oracle.e2m1_value(c) for c in range(16)])
+    for trial in range(200):
+        E = int(rng.integers(-100, 100))
+        codes = rng.integers(0, 16, 32)
+        codes[rng.integers(32)] = rng.choice([6, 7, 14, 15])
+        x = (grid[codes] * 2.0 ** E).astype(np.float32)
+        got, sb = oracle.quantize_block(x)
+        assert sb == E + 127
+        # zero may come back with either sign only if the input zero had that sign
+        assert np.array_equal(got, codes.astype(np.uint8))
+
+
+def test_nonfinite_rejected():
+    x = np.zeros(32, np.float32)
+    x[3] = np.inf
+    with pytest.raises(ValueError):
+        oracle.quantize_block(x)
+    x[3] = np.nan
+    with pytest.raises(ValueError):
+        oracle.quantize_block(x)
+
+
+# ---------------------------------------------------------------- page layout
+
+def test_page_geometry_constants():
+    # [128 tokens x 64 B data][128 tokens x 4 B scale] = 8704 B = 128 x 68 B
+    assert oracle.PAGE_BYTES == 8704 == 128 * 68 == W.PAGE_BYTES
+    assert oracle._load().orc_page_bytes() == 8704
+
+
+def test_insert_writes_exactly_the_row_bytes():
+    # Insert one token into page 2, row 37 of a 4-page, 2-head cache and check that
+    # only bytes row*64..row*64+63 (data view) and 8192+row*4..+3 (scale view) of
+    # that page and head changed.
+    P, H = 4, 2
+    rng = np.random.default_rng(3)
+    kp = np.full((P, H, 8704), 0xAA, np.uint8)
+    vp = np.full((P, H, 8704), 0xAA, np.uint8)
+    ip = np.full((P, 8704), 0xAA, np.uint8)
+    k = rng.standard_normal((1, H, 128)).astype(np.float32)
+    v = rng.standard_normal((1, H, 128)).astype(np.float32)
+    ik = rng.standard_normal((1, 128)).astype(np.float32)
+    slot = np.array([2 * 128 + 37], np.int64)
+    oracle.mx4_insert(k, v, ik, slot, kp, vp, ip)
+    for arr, src, heads in ((kp, k, H), (vp, v, H), (ip, ik, 0)):
+        for h in range(max(heads, 1)):
+            page = arr[2, h] if heads else arr[2]
+            x = src[0, h] if heads else src[0]
+            data, scale = oracle.quantize_row(x)
+            assert np.array_equal(page[37 * 64:38 * 64], data)
+            assert np.array_equal(page[8192 + 37 * 4:8192 + 38 * 4], scale)
+            mask = np.ones(8704, bool)
+            mask[37 * 64:38 * 64] = False
+            mask[8192 + 37 * 4:8192 + 38 * 4] = False
+            assert np.all(page[mask] == 0xAA)
+        others = [p for p in range(P) if p != 2]
+        assert np.all(arr[others] == 0xAA)
+
+
+def test_negative_slot_skips_and_out_of_pool_is_rejected():
+    kp = np.zeros((2, 1, 8704), np.uint8)
+    vp = np.zeros((2, 1, 8704), np.uint8)
+    ip = np.zeros((2, 8704), np.uint8)
+    x = np.ones((1, 1, 128), np.float32)
+    oracle.mx4_insert(x, x, x[:, 0], np.array([-1], np.int64), kp, vp, ip)
+    assert not kp.any() and not vp.any() and not ip.any()
+    with pytest.raises(ValueError):
+        oracle.mx4_insert(x, x, x[:, 0], np.array([2 * 128], np.int64), kp, vp, ip)
+
+
+def test_nibble_order_and_dequant():
+    page = np.zeros(8704, np.uint8)
+    page[5 * 64 + 0] = 0x92        # elements 0,1 of row 5: codes 2 (1.0), 9 (-0.5)
+    page[5 * 64 + 63] = 0x7F       # elements 126,127: codes 15 (-6), 7 (6)
+    page[8192 + 5 * 4 + 0] = 128   # block 0 scale 2
+    page[8192 + 5 * 4 + 3] = 125   # block 3 scale 0.25
+    d = oracle.dequant_row(page, 5)
+    assert d[0] == 2.0 and d[1] == -1.0
+    assert d[126] == -1.5 and d[127] == 1.5
+    assert np.all(d[2:126] == 0)
+    page[8192 + 5 * 4 + 1] = 255   # NaN scale poisons exactly block 1
+    d = oracle.dequant_row(page, 5)
+    assert np.all(np.isnan(d[32:64])) and not np.isnan(d[:32]).any()
+
+
+# ---------------------------------------------------------------- scoring
+
+def _grid_rows(rng, n, E_range=(-4, 3)):
+    """Rows of exactly representable values (so dequant(quant(x)) == x)."""
+    grid = np.array([oracle.e2m1_value(c) for c in range(16)])
+    rows = np.zeros((n, 128), np.float32)
+    for i in range(n):
+        for b in range(4):
+            E = int(rng.integers(*E_range))
+            codes = rng.integers(0, 16, 32)
+            codes[rng.integers(32)] = rng.choice([6, 7, 14, 15])
+            rows[i, 32 * b:32 * b + 32] = grid[codes] * 2.0 ** E
+    return rows
+
+
+def _fill(pages_shape_P, bt, lens, rows):
+    ip = np.full((pages_shape_P, 8704), 0xFF, np.uint8)
+    for s, L in enumerate(lens):
+        pos = np.arange(L)
+        slots = bt[s, pos // 128].astype(np.int64) * 128 + pos % 128
+        oracle.mx4_insert(None, None, rows[s], slots, None, None, ip)
+    return ip
+
+
+def test_representable_rows_roundtrip_through_pages():
+    rng = np.random.default_rng(9)
+    rows = _grid_rows(rng, 300)
+    bt = np.array([[2, 0, 1]], np.int32)
+    ip = _fill(3, bt, [300], [rows])
+    back = oracle.dequant_tokens(ip, bt[0], 300)
+    assert np.array_equal(back, rows.astype(np.float64))
+
+
+def test_index_score_exact_small_case_and_causal_bound():
+    # Two sequences, q = 2 decode tokens each, physical pages permuted.  Values are
+    # exactly representable and the queries are small integers, so the exact
+    # score is a rational number computed here with Fractions.
+    rng = np.random.default_rng(21)
+    lens = [130, 7]
+    bt = np.array([[3, 1], [0, -1]], np.int32)
+    rows = [_grid_rows(rng, L) for L in lens]
+    ip = _fill(4, bt, lens, rows)
+    q = 2
+    iqf = rng.integers(-3, 4, (4, 128)).astype(np.float32)
+    iq = W.to_bf16_bits(iqf)
+    ld = 140
+    sc = oracle.index_score(iq, q, ip, bt, np.array(lens, np.int32), ld)
+    for s in range(2):
+        for j in range(q):
+            t = s * q + j
+            p = lens[s] - q + j
+            for i in range(ld):
+                if i > p:
+                    assert sc[t, i] == -np.inf
+                    continue
+                exact = sum(Fraction(int(iqf[t, d])) * Fraction(float(rows[s][i, d]))
+                            for d in range(128))
+                assert sc[t, i] == float(exact)
+
+
+def test_index_score_unit_query_reads_one_element():
+    rng = np.random.default_rng(2)
+    rows = _grid_rows(rng, 256)
+    bt = np.array([[1, 0]], np.int32)
+    ip = _fill(2, bt, [256], [rows])
+    for d in (0, 1, 31, 32, 77, 127):
+        iqf = np.zeros((1, 128), np.float32)
+        iqf[0, d] = 1.0
+        sc = oracle.index_score(W.to_bf16_bits(iqf), 1, ip, bt, np.array([256], np.int32), 256)
+        assert np.array_equal(sc[0], rows[:, d].astype(np.float64))
+
+
+def test_index_score_invariant_to_physical_page_permutation():
+    rng = np.random.default_rng(4)
+    L = 500
+    x = rng.standard_normal((L, 128)).astype(np.float32)
+    iq = W.to_bf16_bits(rng.standard_normal((1, 128)).astype(np.float32))
+    bt1 = np.array([[0, 1, 2, 3]], np.int32)
+    bt2 = np.array([[3, 0, 2, 1]], np.int32)
+    s1 = oracle.index_score(iq, 1, _fill(4, bt1, [L], [x]), bt1, np.array([L], np.int32), L)
+    s2 = oracle.index_score(iq, 1, _fill(4, bt2, [L], [x]), bt2, np.array([L], np.int32), L)
+    assert np.array_equal(s1, s2)
+
+
+# ---------------------------------------------------------------- top-k
+
+def test_topk_hand_cases():
+    for ln in _lines("topk_cases.txt"):
+        sc, k, want = [p.split() for p in ln.split(";")]
+        scores = np.array([[float(v) for v in sc]])
+        got = oracle.topk_select(scores, np.array([len(sc)], np.int32), 1, int(k[0]))
+        assert list(got[0]) == [int(v) for v in want], ln
+
+
+def test_topk_brute_force_small_rows():
+    # Brute force: the chosen set must be the lexicographically-best k-subset under
+    # (score desc, index asc), i.e. every chosen element ranks before every
+    # unchosen one.  Ties are forced by drawing scores from a few values.
+    rng = np.random.default_rng(13)
+    for trial in range(300):
+        n = int(rng.integers(1, 40))
+        k = int(rng.integers(1, 45))
+        scores = rng.integers(-3, 4, n).astype(np.float64) * 0.5
+        got = oracle.topk_select(scores[None], np.array([n], np.int32), 1, k)[0]
+        chosen = [int(i) for i in got if i >= 0]
+        assert chosen == sorted(chosen) and len(chosen) == min(n, k)
+        assert all(i == -1 for i in got[len(chosen):])
+        rest = [i for i in range(n) if i not in chosen]
+        for a in chosen:
+            for b in rest:
+                assert scores[a] > scores[b] or (scores[a] == scores[b] and a < b)
+
+
+def test_topk_multi_token_causal_lengths():
+    # q = 3 decode tokens of one sequence of length 5: token j sees 5 - 3 + j + 1.
+    scores = np.array([[9, 8, 7, -np.inf, -np.inf],
+                       [1, 2, 3, 4, -np.inf],
+                       [5, 5, 5, 5, 6]], np.float64)
+    got = oracle.topk_select(scores, np.array([5], np.int32), 3, 4)
+    assert list(got[0]) == [0, 1, 2, -1]
+    assert list(got[1]) == [0, 1, 2, 3]
+    assert list(got[2]) == [0, 1, 2, 4]
+
+
+# ---------------------------------------------------------------- attention
+
+def _kv_setup(rng, L, bt, outlier=False):
+    k = rng.standard_normal((L, 1, 128)).astype(np.float32)
+    v = rng.standard_normal((L, 1, 128)).astype(np.float32)
+    if outlier:
+        v[:, 0, 5] *= 20
+    P = int(bt.max()) + 1
+    kp = np.full((P, 1, 8704), 0xFF, np.uint8)
+    vp = np.full((P, 1, 8704), 0xFF, np.uint8)
+    pos = np.arange(L)
+    slots = bt[0, pos // 128].astype(np.int64) * 128 + pos % 128
+    oracle.mx4_insert(k, v, None, slots, kp, vp, None)
+    return kp, vp
+
+
+def test_decode_full_selection_equals_dense_sdpa():
+    # top-k = context -> dense softmax attention; compared with torch's float64
+    # scaled_dot_product_attention over the oracle-dequantised K and V.
+    rng = np.random.default_rng(17)
+    L = 300
+    bt = np.array([[2, 0, 1]], np.int32)
+    kp, vp = _kv_setup(rng, L, bt, outlier=True)
+    qb = W.to_bf16_bits(rng.standard_normal((1, 16, 128)).astype(np.float32))
+    sel = np.arange(512, dtype=np.int32)[None]
+    sel[0, L:] = -1
+    scale = 1 / math.sqrt(128)
+    out = oracle.sparse_paged_decode(qb, 1, kp, vp, bt, np.array([L], np.int32), sel, scale)
+    K = torch.from_numpy(oracle.dequant_tokens(kp, bt[0], L, head=0))
+    V = torch.from_numpy(oracle.dequant_tokens(vp, bt[0], L, head=0))
+    qf = torch.from_numpy(qb.astype(np.uint32) << 16).view(torch.float32).double()
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        qf.view(1, 16, 1, 128), K.expand(1, 16, L, 128), V.expand(1, 16, L, 128), scale=scale)
+    assert np.allclose(out[0], ref.view(16, 128).numpy(), rtol=1e-12, atol=1e-12)
+
+
+def test_decode_single_token_returns_its_value_row():
+    rng = np.random.default_rng(19)
+    L = 200
+    bt = np.array([[1, 0]], np.int32)
+    kp, vp = _kv_setup(rng, L, bt)
+    qb = W.to_bf16_bits(rng.standard_normal((1, 16, 128)).astype(np.float32))
+    for i in (0, 127, 128, 199):
+        sel = np.full((1, 8), -1, np.int32)
+        sel[0, 0] = i
+        out = oracle.sparse_paged_decode(qb, 1, kp, vp, bt, np.array([L], np.int32), sel, 0.1)
+        vrow = oracle.dequant_row(vp[bt[0, i // 128], 0], i % 128)
+        assert np.array_equal(out[0], np.broadcast_to(vrow, (16, 128)))
+
+
+def test_decode_zero_query_gives_mean_of_selected_values():
+    rng = np.random.default_rng(23)
+    L = 256
+    bt = np.array([[0, 1]], np.int32)
+    kp, vp = _kv_setup(rng, L, bt)
+    qb = np.zeros((1, 16, 128), np.uint16)
+    sel = np.array([[3, 50, 129, 255, -1, -1]], np.int32)
+    out = oracle.sparse_paged_decode(qb, 1, kp, vp, bt, np.array([L], np.int32), sel, 0.3)
+    V = oracle.dequant_tokens(vp, bt[0], L, head=0)
+    want = V[[3, 50, 129, 255]].mean(axis=0)
+    assert np.allclose(out[0], np.broadcast_to(want, (16, 128)), rtol=1e-14, atol=1e-15)
+
+
+def test_decode_rejects_index_beyond_position():
+    rng = np.random.default_rng(1)
+    bt = np.array([[0]], np.int32)
+    kp, vp = _kv_setup(rng, 100, bt)
+    qb = np.zeros((1, 16, 128), np.uint16)
+    with pytest.raises(ValueError):
+        oracle.sparse_paged_decode(qb, 1, kp, vp, bt, np.array([100], np.int32),
+                                   np.array([[100]], np.int32), 1.0)
+
+
+def test_decode_gqa_uses_kv_head_group():
+    # With Hkv = 2 and H = 4, heads 0,1 read KV head 0 and heads 2,3 read KV head 1.
+    rng = np.random.default_rng(29)
+    L = 10
+    k = rng.standard_normal((L, 2, 128)).astype(np.float32)
+    v = rng.standard_normal((L, 2, 128)).astype(np.float32)
+    kp = np.zeros((1, 2, 8704), np.uint8)
+    vp = np.zeros((1, 2, 8704), np.uint8)
+    oracle.mx4_insert(k, v, None, np.arange(L, dtype=np.int64), kp, vp, None)
+    qb = np.zeros((1, 4, 128), np.uint16)
+    sel = np.arange(L, dtype=np.int32)[None]
+    out = oracle.sparse_paged_decode(qb, 1, kp, vp, np.array([[0]], np.int32),
+                                     np.array([L], np.int32), sel, 1.0)
+    for h in range(4):
+        V = np.stack([oracle.dequant_row(vp[0, h // 2], i) for i in range(L)])
+        assert np.allclose(out[0, h], V.mean(axis=0), rtol=1e-14, atol=1e-15)
