@@ -1,0 +1,352 @@
+"""Benchmark: one decode step of sparse attention over MXFP4 paged caches.
+
+A step is the whole hot path on one batch: mx4_insert of the decode tokens'
+K/V/index-K rows (when the workload inserts in the step), index_score over
+every cached index key, topk_select, sparse_paged_decode (split + merge).
+Inputs are resident in HBM when the timed region starts; the L2 is flushed
+(a 256 MiB write) between timed steps, outside the per-step CUDA events.
+
+Default workload: 256 sequences, lognormal contexts (median 8192, capped at
+131072), one decode token each inserted in the step, top-2048 -- the only
+workload whose step runs all four kernels.  `--workload 0..4` picks another.
+
+Under torchrun (N > 1) every rank runs an independent replica of the same
+workload (the path shards by sequence with no exchange step): weak scaling,
+value = tokens of all ranks / the slowest rank's time.
+
+`--impl reference` times the CPU oracle (plain C, float64) on this host's
+cores over a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from mxfp4_sparse_paged_gb300 import workloads as W  # noqa: E402
+
+METRIC = "sparse MXFP4 paged-decode tokens/s"
+UNIT = "tokens/s"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _config(wl):
+    L = wl.seq_lens
+    return {"workload": wl.spec.name, "batch": wl.B, "decode_tokens_per_seq": wl.q,
+            "decode_tokens": wl.T, "contexts": {"min": int(L.min()), "median": int(np.median(L)),
+                                                "max": int(L.max()), "sum": int(L.sum())},
+            "top_k": wl.k, "q_heads": W.Q_HEADS, "kv_heads": W.KV_HEADS, "head_dim": W.HEAD_DIM,
+            "insert_in_step": wl.spec.insert_in_step, "seed": wl.spec.seed,
+            "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+            "parallelism": "replicas (one independent batch per GPU)"}
+
+
+# --------------------------------------------------------------------------- clocks
+
+class Clocks:
+    """nvidia-smi sampled every 200 ms during the timed region."""
+
+    def __init__(self, index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except Exception:
+            self.p.kill()
+        self.f.seek(0)
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.f.read().splitlines():
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        os.unlink(self.f.name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# --------------------------------------------------------------------------- CPU oracle
+
+def cpu_oracle_sample(wl, budget_s: float = 15.0):
+    """Time the oracle's step (insert of the step tokens, score, top-k, attention)
+    on a bounded sample of sequences; returns (tokens/s, detail)."""
+    import oracle
+    from mxfp4_sparse_paged_gb300.step import step_inputs_host
+
+    oracle.build()
+    host = step_inputs_host(wl)
+    rng = np.random.default_rng(1234)
+    order = rng.permutation(wl.B)
+    done_tok, spent, seqs = 0, 0.0, []
+    P = wl.num_pages
+    kp = np.full((P, 1, 8704), 0xFF, np.uint8)
+    vp = np.full_like(kp, 0xFF)
+    ip = np.full((P, 8704), 0xFF, np.uint8)
+    scale = 1 / math.sqrt(W.HEAD_DIM)
+    for s in order:
+        s = int(s)
+        n = wl.prefilled(s)
+        for a in range(0, n, 65536):  # untimed: the cache contents before the step
+            b = min(n, a + 65536)
+            oracle.mx4_insert(wl.rows(s, 0, a, b)[:, None], wl.rows(s, 1, a, b)[:, None],
+                              wl.rows(s, 2, a, b), wl.slots(s, np.arange(a, b)), kp, vp, ip)
+        tok = np.arange(s * wl.q, (s + 1) * wl.q)
+        lens = wl.seq_lens[[s]]
+        bt = wl.block_table[[s]]
+        t0 = time.perf_counter()
+        if wl.spec.insert_in_step:
+            oracle.mx4_insert(host["k"][tok][:, None], host["v"][tok][:, None], host["idx_k"][tok],
+                              host["slots"][tok], kp, vp, ip)
+        sc = oracle.index_score(host["iq"][tok], wl.q, ip, bt, lens, int(lens[0]))
+        sel = oracle.topk_select(sc, lens, wl.q, wl.k)
+        oracle.sparse_paged_decode(host["q"][tok], wl.q, kp, vp, bt, lens, sel, scale)
+        spent += time.perf_counter() - t0
+        done_tok += wl.q
+        seqs.append(s)
+        if spent >= budget_s:
+            break
+    frac_ctx = float(wl.seq_lens[seqs].sum()) / float(wl.seq_lens.sum())
+    detail = (f"{len(seqs)} of {wl.B} sequences ({done_tok} decode tokens, "
+              f"{100 * frac_ctx:.1f}% of the step's cached tokens), single thread, "
+              f"{spent:.1f} s; value = sampled decode tokens / oracle step time")
+    return done_tok / spent, detail, spent
+
+
+# --------------------------------------------------------------------------- GPU arm
+
+def run_gpu(args):
+    import torch
+    import torch.distributed as dist
+
+    import mxfp4_sparse_paged_gb300 as m
+    from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, step_inputs_host
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    wl = W.make(args.workload)
+    caches = PagedCaches(wl.num_pages, device=dev)
+    caches.fill(wl)
+    step = DecodeStep(wl, caches, device=dev)
+    host = step_inputs_host(wl)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    ab = W.algorithmic_bytes(wl)
+
+    # The in-step insert rewrites the decode tokens' rows with the same values, so
+    # every timed step does identical work.
+    names = (["mx4_insert"] if wl.spec.insert_in_step else []) + \
+        ["index_score", "topk_select", "sparse_paged_decode"]
+    step.load_inputs(host)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step.run(stream=stream)
+    m.mx4_check_status()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names}
+    st = [(ev(), ev()) for _ in range(args.steps)]
+    clocks = Clocks(local)
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        st[i][0].record(stream)
+        step.run(stream=stream, events={n: per[n][i] for n in names})
+        st[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    ck = clocks.stop()
+    m.mx4_check_status()
+    step_ms = [a.elapsed_time(b) for a, b in st]
+    kern_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in per[n]) for n in names}
+    total_ms = sum(step_ms)
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = wl.T * world * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API: host inputs -> device -> step -> host output
+    pin = {k: torch.from_numpy(np.ascontiguousarray(
+        v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory() for k, v in host.items()}
+    h_out = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in pin.values())
+    d2h = h_out.numel() * h_out.element_size()
+    for _ in range(2):
+        step.load_inputs(pin, non_blocking=True)
+        step.run(stream=stream)
+        h_out.copy_(step.out, non_blocking=True)
+    e_st = [(ev(), ev()) for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        e_st[i][0].record(stream)
+        step.load_inputs(pin, non_blocking=True)
+        step.run(stream=stream)
+        h_out.copy_(step.out, non_blocking=True)
+        e_st[i][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e_st)
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e_value = wl.T * world * args.steps / (e2e_ms / 1e3)
+    m.mx4_check_status()
+
+    peak, peak_kind = _peaks()
+    score_s = kern_ms["index_score"] / 1e3
+    achieved = ab["index_score"] / score_s / 1e9
+    dec_s = kern_ms["sparse_paged_decode"] / 1e3
+    hot_bytes = ab["index_score"] + ab["sparse_paged_decode"]
+    hot_gbs = hot_bytes / (score_s + dec_s) / 1e9
+    traffic = _ncu_traffic(wl.spec.name)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
+        "data": "synthetic (seeded N(0,1) K/V/index-K rows quantised to MXFP4 pages; "
+                "bf16 N(0,1) queries)",
+        "config": _config(wl),
+        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": ab["index_score"],
+                     "traffic": traffic},
+        "hot_path_hbm": {"kernels": "index_score + sparse_paged_decode",
+                         "algorithmic_bytes": hot_bytes, "achieved_gbs": round(hot_gbs, 1),
+                         "frac": round(hot_gbs / peak, 4)},
+        "kernel_ms": {n: round(v, 5) for n, v in kern_ms.items()},
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "clocks": ck,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        v, detail, spent = cpu_oracle_sample(wl, args.cpu_budget)
+        line["cpu_baseline"] = {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": detail}
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _ncu_traffic(name):
+    """dram bytes per index_score launch from the committed ncu summary, if one
+    was taken on the current kernel for this workload."""
+    p = os.path.join(ROOT, "profiles", "index_score_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d.get(name)
+    except Exception:
+        return None
+
+
+def run_reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    wl = W.make(args.workload)
+    budget = max(1.0, min(60.0, args.cpu_budget))
+    vals, details, spent = [], [], 0.0
+    for i in range(args.warmup + args.steps):
+        v, d, s = cpu_oracle_sample(wl, budget / max(1, args.steps + args.warmup))
+        if i >= args.warmup:
+            vals.append(v)
+            details.append(d)
+            spent += s
+    value = statistics.mean(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * wl.T / value, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(wl),
+            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": details[-1]},
+            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", type=int, default=4, choices=range(5))
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,196 @@
+/*
+ * mx4sp.h -- C ABI of the GB300 (sm_103a) library for sparse-attention decode
+ * over an MXFP4 paged KV cache.
+ *
+ * The cache format is the one described on "vllm.models.minimax_m3.amd.ops.
+ * mxfp4_pages" (module description and mxfp4_page_views): one page holds 128
+ * token rows of one head as
+ *
+ *     [128 tokens x 64 B e2m1 data][128 tokens x 4 B e8m0 scale] = 8704 B
+ *
+ * two elements a byte (the low nibble is the even element), one e8m0 scale per
+ * 32 consecutive elements, no global scale.  A page tensor is
+ * [pages, heads, 8704] for K and V and [pages, 8704] for the index key, with
+ * arbitrary page/head strides and a contiguous byte axis.  K/V and the index
+ * key are written through one page-128 slot mapping and read through one
+ * block table ("vllm.models.minimax_m3.amd.mono.dispatch", _slots_shared,
+ * _step_refusal).
+ *
+ * Conventions shared by every entry point
+ *   - All pointers to tensors are DEVICE pointers on the current CUDA device,
+ *     except where stated.  The caller owns every buffer, workspaces included;
+ *     no call allocates, frees or synchronises (mx4_check_status excepted), so
+ *     every call can be recorded into a CUDA graph.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     All work is enqueued on it, asynchronously.
+ *   - bf16 tensors are passed as uint16_t bit patterns.
+ *   - Return value: MX4_OK, or a negative mx4_status.  On error nothing has been
+ *     enqueued and mx4_last_error() returns the reason (thread-local).  Argument
+ *     checks that need device data (block-table entries, slots, sequence lengths,
+ *     top-k indices) are done by the kernels: a bad entry is skipped, its output
+ *     is left as described per call, and a bit is set in a device status word
+ *     that mx4_check_status() reads and clears.
+ *   - Page pointers must be 16-byte aligned and page/head strides multiples of
+ *     16 bytes; fp32/bf16 row tensors must be contiguous and 16-byte aligned.
+ *   - Sequence s of a batch holds seq_lens[s] cached tokens; its q decode tokens
+ *     are t = s*q + j (j = 0..q-1) at positions seq_lens[s] - q + j, and token j
+ *     attends to cached positions 0 .. seq_lens[s] - q + j.
+ */
+#ifndef MX4SP_H
+#define MX4SP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MX4_OK = 0,
+    MX4_ERR_INVALID = -1,     /* a NULL pointer, a negative size, a misaligned buffer */
+    MX4_ERR_UNSUPPORTED = -2, /* a geometry this build does not implement */
+    MX4_ERR_WORKSPACE = -3,   /* workspace too small */
+    MX4_ERR_CUDA = -4,        /* a CUDA runtime error (launch or copy) */
+    MX4_ERR_BOUNDS = -5       /* reported by mx4_check_status: a kernel skipped bad data */
+} mx4_status;
+
+/* Bits of the device status word (mx4_check_status). */
+#define MX4_STATUS_BAD_SLOT 0x1u   /* slot >= num_pages * 128 */
+#define MX4_STATUS_BAD_PAGE 0x2u   /* block-table entry outside [0, num_pages) */
+#define MX4_STATUS_BAD_LEN 0x4u    /* seq_len < q, or beyond the block table / ld */
+#define MX4_STATUS_BAD_INDEX 0x8u  /* top-k index outside [0, position] */
+#define MX4_STATUS_BAD_VALUE 0x10u /* non-finite fp32 input to mx4_insert */
+
+#define MX4_PAGE_TOKENS 128
+#define MX4_HEAD_DIM 128
+#define MX4_PAGE_BYTES 8704
+
+/* Reason for the last non-OK return on this thread ("" if none). */
+const char *mx4_last_error(void);
+
+/* Bytes of one page of one head: 8704. */
+size_t mx4_page_bytes(void);
+
+/* ---------------------------------------------------------------------------
+ * mx4_insert -- quantise-on-insert (page description of "mxfp4_pages"; slot
+ * mapping of _slots_shared).
+ *
+ * For each new token t with slot = slot_mapping[t] >= 0, quantise its K row (per
+ * KV head), V row (per KV head) and index-K row, 128 fp32 values each, into
+ * MXFP4 and write them to row slot % 128 of page slot / 128 of k_pages, v_pages
+ * and idx_pages.  Each 32-element block gets the shared exponent
+ * E = floor(log2(amax)) - 2 clamped to [-127, 127] (-127 when amax == 0), scale
+ * byte E + 127, and every element the E2M1 code of x / 2^E rounded to nearest,
+ * ties to even, saturating at 6, with the sign of x (OCP MX v1.0 conversion).
+ *
+ *   k, v         fp32 [T, Hkv, 128], contiguous
+ *   idx_k        fp32 [T, 128], contiguous
+ *   slot_mapping int64 [T]; a negative slot skips the token
+ *   k_pages, v_pages  uint8, page p head h at base + p*kv_page_stride
+ *                     + h*kv_head_stride (bytes); written in place
+ *   idx_pages    uint8, page p at base + p*idx_page_stride; written in place
+ *   num_pages    pages in each pool (slots must be < num_pages * 128)
+ * Bad slot: the token is skipped and MX4_STATUS_BAD_SLOT is set.  Non-finite
+ * inputs are out of contract: their bytes are unspecified and
+ * MX4_STATUS_BAD_VALUE is set.  1 <= Hkv <= 8.
+ * ------------------------------------------------------------------------- */
+int mx4_insert(const float *k, const float *v, const float *idx_k, int64_t T, int Hkv,
+               const int64_t *slot_mapping, uint8_t *k_pages, uint8_t *v_pages,
+               int64_t kv_page_stride, int64_t kv_head_stride, uint8_t *idx_pages,
+               int64_t idx_page_stride, int64_t num_pages, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * index_score -- the index scorer (the scorers that read [pages, 128, 64] /
+ * [pages, 128, 4] index-key views, "mxfp4_pages" / mxfp4_page_views).
+ *
+ * For decode token t = s*q + j at position p = seq_lens[s] - q + j:
+ *     scores[t*ld_scores + i] = sum_d iq[t][d] * dequant(indexK[s, i])[d]
+ * for 0 <= i <= p, computed in fp32, and -inf for p < i < seq_lens[s]; entries
+ * at i >= seq_lens[s] are not written.  dequant = e2m1 value x 2^(scale - 127).
+ * Token i of sequence s is row i % 128 of page block_table[s*bt_width + i/128].
+ * The q decode tokens of a sequence share one pass over its pages.
+ *
+ *   iq          bf16 [T, 128] with T = B * q_per_seq, contiguous
+ *   idx_pages   uint8 [num_pages, 8704] at stride idx_page_stride
+ *   block_table int32 [B, bt_width], row-contiguous
+ *   seq_lens    int32 [B]
+ *   scores      fp32 [T, ld_scores]
+ * 1 <= q_per_seq <= 8, B <= 65535.  A sequence with seq_len < q, seq_len >
+ * bt_width*128 or seq_len > ld_scores is skipped (MX4_STATUS_BAD_LEN); a page
+ * id outside [0, num_pages) skips that page (MX4_STATUS_BAD_PAGE).
+ * ------------------------------------------------------------------------- */
+int index_score(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t *idx_pages,
+                int64_t idx_page_stride, int64_t num_pages, const int32_t *block_table,
+                int64_t B, int64_t bt_width, const int32_t *seq_lens, float *scores,
+                int64_t ld_scores, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * topk_select -- per-token top-k selection of the tokens to attend.
+ *
+ * For decode token t with n = p + 1 valid scores (p as above): the min(k, n)
+ * indices i in [0, n) with the largest scores[t*ld_scores + i], ties broken
+ * towards the lower index (the order is: larger score first, then lower index;
+ * -0.0 and +0.0 are equal), written in ascending index order to
+ * topk_idx[t*k ...]; the remaining entries up to k are -1.
+ *
+ *   scores   fp32 [T, ld_scores], T = B * q_per_seq; must be finite on [0, n)
+ *   seq_lens int32 [B]
+ *   topk_idx int32 [T, k] (output)
+ *   ws       workspace of topk_select_workspace(T, k, ld_scores) bytes (may be
+ *            NULL when that is 0)
+ * 1 <= k <= 65536, 1 <= q_per_seq <= 8.  A bad seq_len (n < 1 or n > ld_scores)
+ * writes a row of -1 and sets MX4_STATUS_BAD_LEN.
+ * ------------------------------------------------------------------------- */
+int topk_select(const float *scores, int64_t ld_scores, const int32_t *seq_lens, int64_t B,
+                int q_per_seq, int k, int32_t *topk_idx, void *ws, size_t ws_bytes,
+                void *stream);
+size_t topk_select_workspace(int64_t T, int k, int64_t ld_scores);
+
+/* ---------------------------------------------------------------------------
+ * sparse_paged_decode -- GQA decode attention over the selected tokens (the
+ * pa_decode reader of [pages, heads, 128, 64] / [pages, heads, 128, 4] K/V
+ * views, "mxfp4_pages" / mxfp4_page_views), with a split-K merge.
+ *
+ * For decode token t of sequence s and query head h (KV head h / (H / Hkv)):
+ *     l_i = scale * sum_d q[t][h][d] * dequant(K[s, i])[d],
+ *     out[t][h][:] = sum_i softmax(l)_i * dequant(V[s, i])[:]
+ * over the indices i of topk_idx[t*k ...] that are >= 0 (negative entries are
+ * skipped, so the -1 padding of topk_select is ignored).
+ * Logits and the softmax are fp32; the selected list is cut into splits, each
+ * split keeps a running max and sum (online softmax), and a merge kernel
+ * combines the splits.
+ *
+ *   q         bf16 [T, H, 128], contiguous
+ *   k_pages, v_pages  uint8 [num_pages, Hkv, 8704] at the given strides
+ *   block_table int32 [B, bt_width]; seq_lens int32 [B]
+ *   topk_idx  int32 [T, k], ascending indices then -1 padding
+ *   out       fp32 [T, H, 128] (output)
+ *   ws        workspace of sparse_paged_decode_workspace(T, k) bytes
+ * H == 16 and Hkv == 1 in this build (else MX4_ERR_UNSUPPORTED).  An index
+ * outside [0, p] or a bad page id skips that token and sets
+ * MX4_STATUS_BAD_INDEX / MX4_STATUS_BAD_PAGE.  A token with no selected index
+ * gets a zero output.
+ * ------------------------------------------------------------------------- */
+int sparse_paged_decode(const uint16_t *q, int64_t T, int q_per_seq, int H, int Hkv,
+                        const uint8_t *k_pages, const uint8_t *v_pages, int64_t kv_page_stride,
+                        int64_t kv_head_stride, int64_t num_pages, const int32_t *block_table,
+                        int64_t B, int64_t bt_width, const int32_t *seq_lens,
+                        const int32_t *topk_idx, int k, float scale, float *out, void *ws,
+                        size_t ws_bytes, void *stream);
+size_t sparse_paged_decode_workspace(int64_t T, int k);
+
+/* ---------------------------------------------------------------------------
+ * mx4_check_status -- synchronise `stream`, return MX4_OK if no kernel of this
+ * library has flagged bad data on the current device since the last check,
+ * else MX4_ERR_BOUNDS with the flagged MX4_STATUS_* bits in *bits (if bits is
+ * not NULL) and in mx4_last_error().  Clears the word.  This is the only call
+ * that synchronises.
+ * ------------------------------------------------------------------------- */
+int mx4_check_status(void *stream, uint32_t *bits);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MX4SP_H */

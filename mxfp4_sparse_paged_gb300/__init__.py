@@ -1,0 +1,206 @@
+"""Sparse-attention decode over an MXFP4 paged KV cache, native to GB300.
+
+Thin Python binding of the C ABI in include/mx4sp.h (libmx4sp.so, hand-written
+sm_103a CUDA kernels).  Every function here has the name of the C entry point
+it calls and only marshals arguments: torch tensors become device pointers,
+byte strides and the current CUDA stream.  All computation runs in the CUDA
+library; there is no fallback, and a missing library raises.
+
+Page tensors are uint8 with a contiguous 8704-byte last axis: K/V pages
+[pages, heads, 8704], index-K pages [pages, 8704] (the page of
+"vllm.models.minimax_m3.amd.ops.mxfp4_pages").
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+__all__ = ["mx4_insert", "index_score", "topk_select", "sparse_paged_decode",
+           "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
+           "mx4_last_error", "mx4_page_bytes", "library_path", "Mx4Error", "PAGE_BYTES",
+           "PAGE_TOKENS", "HEAD_DIM"]
+
+PAGE_BYTES = 8704
+PAGE_TOKENS = 128
+HEAD_DIM = 128
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "_build", "libmx4sp.so")
+_lock = threading.Lock()
+_lib = None
+
+STATUS_BITS = {0x1: "bad-slot", 0x2: "bad-page", 0x4: "bad-seq-len", 0x8: "bad-topk-index",
+               0x10: "non-finite-input"}
+
+
+class Mx4Error(RuntimeError):
+    def __init__(self, code: int, msg: str, bits: int = 0):
+        super().__init__(f"mx4 status {code}: {msg}")
+        self.code = code
+        self.bits = bits
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"{_LIB_PATH} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, i64, i32, sz = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+        lib.mx4_last_error.restype = ctypes.c_char_p
+        lib.mx4_last_error.argtypes = []
+        lib.mx4_page_bytes.restype = sz
+        lib.mx4_page_bytes.argtypes = []
+        lib.mx4_insert.restype = i32
+        lib.mx4_insert.argtypes = [P, P, P, i64, i32, P, P, P, i64, i64, P, i64, i64, P]
+        lib.index_score.restype = i32
+        lib.index_score.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, P]
+        lib.topk_select.restype = i32
+        lib.topk_select.argtypes = [P, i64, P, i64, i32, i32, P, P, sz, P]
+        lib.topk_select_workspace.restype = sz
+        lib.topk_select_workspace.argtypes = [i64, i32, i64]
+        lib.sparse_paged_decode.restype = i32
+        lib.sparse_paged_decode.argtypes = [P, i64, i32, i32, i32, P, P, i64, i64, i64, P, i64,
+                                            i64, P, P, i32, ctypes.c_float, P, P, sz, P]
+        lib.sparse_paged_decode_workspace.restype = sz
+        lib.sparse_paged_decode_workspace.argtypes = [i64, i32]
+        lib.mx4_check_status.restype = i32
+        lib.mx4_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+        _lib = lib
+        return lib
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise Mx4Error(rc, _load().mx4_last_error().decode())
+
+
+def _need(t, dtype, name, contiguous=True):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+    if contiguous and not t.is_contiguous():
+        raise ValueError(f"{name}: must be contiguous")
+
+
+def _pages(t, name, ndim):
+    _need(t, torch.uint8, name, contiguous=False)
+    if t.dim() != ndim or t.shape[-1] != PAGE_BYTES or t.stride(-1) != 1:
+        raise ValueError(f"{name}: uint8 pages need shape [...] x {PAGE_BYTES} with a "
+                         f"contiguous byte axis, got {tuple(t.shape)} strides {t.stride()}")
+
+
+def mx4_last_error() -> str:
+    return _load().mx4_last_error().decode()
+
+
+def mx4_page_bytes() -> int:
+    return int(_load().mx4_page_bytes())
+
+
+def mx4_insert(k, v, idx_k, slot_mapping, k_pages, v_pages, idx_pages, stream=None):
+    """Quantise new tokens' K [T,Hkv,128], V [T,Hkv,128] and index-K [T,128] (fp32)
+    into their page rows through slot_mapping (int64 [T]); pages are written in place."""
+    _need(k, torch.float32, "k")
+    _need(v, torch.float32, "v")
+    _need(idx_k, torch.float32, "idx_k")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _pages(k_pages, "k_pages", 3)
+    _pages(v_pages, "v_pages", 3)
+    _pages(idx_pages, "idx_pages", 2)
+    if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    T, Hkv = int(k.shape[0]), int(k.shape[1])
+    _check(_load().mx4_insert(_ptr(k), _ptr(v), _ptr(idx_k), T, Hkv, _ptr(slot_mapping),
+                              _ptr(k_pages), _ptr(v_pages), k_pages.stride(0), k_pages.stride(1),
+                              _ptr(idx_pages), idx_pages.stride(0), int(k_pages.shape[0]),
+                              _stream(stream)))
+
+
+def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=None):
+    """scores[t, i] = iq[t] . dequant(indexK[s, i]) for i <= position (fp32 [T, ld])."""
+    _need(iq, torch.bfloat16, "iq")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(scores, torch.float32, "scores", contiguous=False)
+    _pages(idx_pages, "idx_pages", 2)
+    if scores.stride(1) != 1:
+        raise ValueError("scores: rows must be contiguous")
+    B = int(seq_lens.shape[0])
+    _check(_load().index_score(_ptr(iq), int(iq.shape[0]), int(q_per_seq), _ptr(idx_pages),
+                               idx_pages.stride(0), int(idx_pages.shape[0]), _ptr(block_table), B,
+                               int(block_table.shape[1]), _ptr(seq_lens), _ptr(scores),
+                               scores.stride(0), _stream(stream)))
+
+
+def topk_select_workspace(T, k, ld_scores) -> int:
+    return int(_load().topk_select_workspace(int(T), int(k), int(ld_scores)))
+
+
+def topk_select(scores, seq_lens, q_per_seq, k, topk_idx, ws=None, stream=None):
+    """topk_idx[t] = the min(k, n) best indices (ties -> lower index), ascending, -1 padded."""
+    _need(scores, torch.float32, "scores", contiguous=False)
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(topk_idx, torch.int32, "topk_idx")
+    if scores.stride(1) != 1:
+        raise ValueError("scores: rows must be contiguous")
+    ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
+    _check(_load().topk_select(_ptr(scores), scores.stride(0), _ptr(seq_lens),
+                               int(seq_lens.shape[0]), int(q_per_seq), int(k), _ptr(topk_idx),
+                               _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def sparse_paged_decode_workspace(T, k) -> int:
+    return int(_load().sparse_paged_decode_workspace(int(T), int(k)))
+
+
+def sparse_paged_decode(q, q_per_seq, k_pages, v_pages, block_table, seq_lens, topk_idx, scale,
+                        out, ws, stream=None):
+    """out[t, h] = softmax(scale * q[t,h] . K_sel) V_sel over the selected tokens (fp32)."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(out, torch.float32, "out")
+    _pages(k_pages, "k_pages", 3)
+    _pages(v_pages, "v_pages", 3)
+    if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    T, H = int(q.shape[0]), int(q.shape[1])
+    ws_bytes = ws.numel() * ws.element_size()
+    _check(_load().sparse_paged_decode(
+        _ptr(q), T, int(q_per_seq), H, int(k_pages.shape[1]), _ptr(k_pages), _ptr(v_pages),
+        k_pages.stride(0), k_pages.stride(1), int(k_pages.shape[0]), _ptr(block_table),
+        int(seq_lens.shape[0]), int(block_table.shape[1]), _ptr(seq_lens), _ptr(topk_idx),
+        int(topk_idx.shape[1]), float(scale), _ptr(out), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def mx4_check_status(stream=None) -> int:
+    """Synchronise the stream; raise Mx4Error if a kernel flagged bad data (clears it)."""
+    bits = ctypes.c_uint32(0)
+    rc = _load().mx4_check_status(_stream(stream), ctypes.byref(bits))
+    if rc != 0:
+        raise Mx4Error(rc, _load().mx4_last_error().decode(), bits.value)
+    return 0

@@ -1,0 +1,120 @@
+// mx4_insert: quantise each new token's K, V and index-K rows into MXFP4 page
+// rows through the shared page-128 slot mapping.
+//
+// Format: "vllm.models.minimax_m3.amd.ops.mxfp4_pages" (module description):
+// 64 B of e2m1 codes per 128-element row, element 2n in the low nibble of byte
+// n, then one e8m0 scale per 32 elements in the page's scale rows.  Rule: OCP
+// MX v1.0 conversion -- shared exponent floor(log2(amax)) - 2 per 32-element
+// block, elements rounded to the nearest E2M1 value, ties to even, saturating.
+// Slot mapping: "vllm.models.minimax_m3.amd.mono.dispatch", _slots_shared.
+//
+// One warp quantises one row.  Lane l owns elements 4l .. 4l+3 (a float4), so
+// the 8 lanes 8b .. 8b+7 hold block b; the block maximum is an xor-shuffle
+// over those 8 lanes.  Each lane writes its 2 code bytes (the warp writes the
+// 64 data bytes contiguously) and lane 0 writes the row's 4 scale bytes.
+#include "common.cuh"
+
+namespace mx4 {
+
+// E2M1 magnitude code (0..7) of a = |y| < 8: the number of rounding thresholds
+// that a lies above.  A tie sits exactly on a threshold and goes to the
+// neighbour with an even mantissa bit, so the comparison is strict (>) where
+// the even neighbour is the lower one (0.25, 1.25, 2.5, 5) and non-strict (>=)
+// where it is the upper one (0.75, 1.75, 3.5).  Values above 6 saturate to 7.
+__device__ __forceinline__ uint32_t e2m1_magnitude_code(float a) {
+  return (uint32_t)(a > 0.25f) + (uint32_t)(a >= 0.75f) + (uint32_t)(a > 1.25f) +
+         (uint32_t)(a >= 1.75f) + (uint32_t)(a > 2.5f) + (uint32_t)(a >= 3.5f) +
+         (uint32_t)(a > 5.0f);
+}
+
+// Shared exponent E = floor(log2(amax)) - 2 clamped to [-127, 127], read from
+// the fp32 exponent field (exact).  amax == 0 and subnormal amax give -127;
+// finite amax never exceeds E = 125.
+__device__ __forceinline__ int block_exponent(float amax) {
+  uint32_t ef = (__float_as_uint(amax) >> 23) & 0xFFu;
+  int E = (int)ef - 127 - 2;
+  return (ef == 0u || E < -127) ? -127 : E;
+}
+
+__global__ void __launch_bounds__(256)
+insert_kernel(const float* __restrict__ k, const float* __restrict__ v,
+              const float* __restrict__ idx_k, int64_t T, int Hkv,
+              const int64_t* __restrict__ slot_mapping, uint8_t* __restrict__ k_pages,
+              uint8_t* __restrict__ v_pages, int64_t kv_page_stride, int64_t kv_head_stride,
+              uint8_t* __restrict__ idx_pages, int64_t idx_page_stride, int64_t num_pages,
+              uint32_t* status) {
+  const int lane = threadIdx.x & 31;
+  const int rows_per_token = 2 * Hkv + 1;  // K heads, V heads, index key
+  const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (warp >= T * rows_per_token) return;
+  const int64_t t = warp / rows_per_token;
+  const int r = (int)(warp % rows_per_token);
+
+  const int64_t slot = slot_mapping[t];
+  if (slot < 0) return;
+  const int64_t page = slot / kPageTokens;
+  const int row = (int)(slot % kPageTokens);
+  if (page >= num_pages) {
+    if (lane == 0) flag(status, MX4_STATUS_BAD_SLOT);
+    return;
+  }
+
+  const float* src;
+  uint8_t* dst;
+  if (r < Hkv) {
+    src = k + (t * Hkv + r) * kHeadDim;
+    dst = k_pages + page * kv_page_stride + (int64_t)r * kv_head_stride;
+  } else if (r < 2 * Hkv) {
+    src = v + (t * Hkv + (r - Hkv)) * kHeadDim;
+    dst = v_pages + page * kv_page_stride + (int64_t)(r - Hkv) * kv_head_stride;
+  } else {
+    src = idx_k + t * kHeadDim;
+    dst = idx_pages + page * idx_page_stride;
+  }
+
+  const float4 x = reinterpret_cast<const float4*>(src)[lane];
+  const bool finite = isfinite(x.x) && isfinite(x.y) && isfinite(x.z) && isfinite(x.w);
+  if (!__all_sync(0xFFFFFFFFu, finite) && lane == 0) flag(status, MX4_STATUS_BAD_VALUE);
+
+  float amax = fmaxf(fmaxf(fabsf(x.x), fabsf(x.y)), fmaxf(fabsf(x.z), fabsf(x.w)));
+#pragma unroll
+  for (int o = 1; o < 8; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, o));
+  const int E = block_exponent(amax);
+  // 2^-E is a normal fp32 for every E in [-127, 125]; the product is exact.
+  const float inv = __uint_as_float((uint32_t)(127 - E) << 23);
+
+  const float xs[4] = {x.x, x.y, x.z, x.w};
+  uint32_t packed = 0;
+#pragma unroll
+  for (int e = 0; e < 4; ++e) {
+    const uint32_t code = e2m1_magnitude_code(fabsf(xs[e] * inv)) |
+                          ((__float_as_uint(xs[e]) >> 28) & 8u);
+    packed |= code << (4 * e);
+  }
+  reinterpret_cast<uint16_t*>(dst + row * kRowDataBytes)[lane] = (uint16_t)packed;
+
+  // scale bytes of blocks 0..3 live in lanes 0, 8, 16, 24
+  const uint32_t sb = (uint32_t)(E + 127);
+  const uint32_t s1 = __shfl_sync(0xFFFFFFFFu, sb, 8);
+  const uint32_t s2 = __shfl_sync(0xFFFFFFFFu, sb, 16);
+  const uint32_t s3 = __shfl_sync(0xFFFFFFFFu, sb, 24);
+  if (lane == 0)
+    *reinterpret_cast<uint32_t*>(dst + kScaleOffset + row * kRowScaleBytes) =
+        sb | (s1 << 8) | (s2 << 16) | (s3 << 24);
+}
+
+cudaError_t launch_insert(const float* k, const float* v, const float* idx_k, int64_t T, int Hkv,
+                          const int64_t* slot_mapping, uint8_t* k_pages, uint8_t* v_pages,
+                          int64_t kv_page_stride, int64_t kv_head_stride, uint8_t* idx_pages,
+                          int64_t idx_page_stride, int64_t num_pages, uint32_t* status,
+                          cudaStream_t stream) {
+  const int64_t warps = T * (2 * Hkv + 1);
+  const int threads = 256;
+  const int64_t blocks = (warps + (threads / 32) - 1) / (threads / 32);
+  insert_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
+      k, v, idx_k, T, Hkv, slot_mapping, k_pages, v_pages, kv_page_stride, kv_head_stride,
+      idx_pages, idx_page_stride, num_pages, status);
+  return cudaGetLastError();
+}
+
+}  // namespace mx4

@@ -1,0 +1,245 @@
+// C-ABI entry points of the MXFP4 sparse paged decode library (mx4sp.h).
+//
+// Host side only: argument validation in the style of the pages' own checks
+// ("vllm.models.minimax_m3.amd.ops.mxfp4_pages", mxfp4_page_views: uint8 pages
+// with a trailing 8704-byte contiguous axis, else an error; "vllm.models.
+// minimax_m3.amd.mono.dispatch", _step_refusal: a reason string instead of a
+// wrong result), the per-device status word, and the kernel launches.
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace mx4 {
+cudaError_t launch_insert(const float*, const float*, const float*, int64_t, int, const int64_t*,
+                          uint8_t*, uint8_t*, int64_t, int64_t, uint8_t*, int64_t, int64_t,
+                          uint32_t*, cudaStream_t);
+cudaError_t launch_index_score(const uint16_t*, int, const uint8_t*, int64_t, int64_t,
+                               const int32_t*, int, int64_t, const int32_t*, float*, int64_t,
+                               uint32_t*, int, cudaStream_t);
+cudaError_t launch_topk(const float*, int64_t, const int32_t*, int64_t, int, int, int32_t*,
+                        uint32_t*, cudaStream_t);
+cudaError_t launch_decode(const uint16_t*, int64_t, int, const uint8_t*, const uint8_t*, int64_t,
+                          int64_t, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
+                          float, float*, void*, uint32_t*, cudaStream_t);
+size_t decode_workspace_bytes(int64_t, int);
+}  // namespace mx4
+
+// Device status word: kernels OR MX4_STATUS_* bits into it when they skip bad
+// data; mx4_check_status reads and clears it.
+static __device__ uint32_t g_status;
+
+namespace {
+
+thread_local char g_err[512];
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof g_err, fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_err[0] = '\0';
+  return MX4_OK;
+}
+
+constexpr int kMaxDevices = 64;
+struct DeviceInfo {
+  bool ready = false;
+  uint32_t* status = nullptr;
+  int num_sms = 0;
+};
+DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;
+
+// Per-device set-up (first call on a device): the status word's device address
+// and the SM count.  Done before any launch, outside stream capture.
+int device_info(DeviceInfo** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MX4_ERR_UNSUPPORTED, "device id %d", dev);
+  DeviceInfo& d = g_dev[dev];
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!d.ready) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_status);
+    if (e != cudaSuccess)
+      return fail(MX4_ERR_CUDA, "cudaGetSymbolAddress(status): %s", cudaGetErrorString(e));
+    e = cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess)
+      return fail(MX4_ERR_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    d.status = static_cast<uint32_t*>(p);
+    d.ready = true;
+  }
+  *out = &d;
+  return MX4_OK;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int cuda_result(cudaError_t e, const char* what) {
+  if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* mx4_last_error(void) { return g_err; }
+
+size_t mx4_page_bytes(void) { return (size_t)mx4::kPageBytes; }
+
+int mx4_insert(const float* k, const float* v, const float* idx_k, int64_t T, int Hkv,
+               const int64_t* slot_mapping, uint8_t* k_pages, uint8_t* v_pages,
+               int64_t kv_page_stride, int64_t kv_head_stride, uint8_t* idx_pages,
+               int64_t idx_page_stride, int64_t num_pages, void* stream) {
+  if (T < 0) return fail(MX4_ERR_INVALID, "mx4_insert: T = %lld < 0", (long long)T);
+  if (Hkv < 1 || Hkv > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "mx4_insert: Hkv = %d (supported 1..8)", Hkv);
+  if (T == 0) return ok();
+  if (!k || !v || !idx_k || !slot_mapping || !k_pages || !v_pages || !idx_pages)
+    return fail(MX4_ERR_INVALID, "mx4_insert: NULL pointer");
+  if (!aligned(k, 16) || !aligned(v, 16) || !aligned(idx_k, 16))
+    return fail(MX4_ERR_INVALID, "mx4_insert: fp32 rows must be 16-byte aligned");
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(idx_pages, 16) ||
+      kv_page_stride % 16 || kv_head_stride % 16 || idx_page_stride % 16)
+    return fail(MX4_ERR_INVALID, "mx4_insert: pages must be 16-byte aligned with 16-byte strides");
+  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || idx_page_stride < mx4::kPageBytes ||
+      (Hkv > 1 && kv_head_stride < mx4::kPageBytes))
+    return fail(MX4_ERR_INVALID, "mx4_insert: num_pages < 1 or a stride below 8704 bytes");
+  if (T * (2 * Hkv + 1) > (int64_t)8 * 0x7FFFFFFF)
+    return fail(MX4_ERR_UNSUPPORTED, "mx4_insert: T too large");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(mx4::launch_insert(k, v, idx_k, T, Hkv, slot_mapping, k_pages, v_pages,
+                                        kv_page_stride, kv_head_stride, idx_pages,
+                                        idx_page_stride, num_pages, d->status,
+                                        static_cast<cudaStream_t>(stream)),
+                     "mx4_insert");
+}
+
+int index_score(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx_pages,
+                int64_t idx_page_stride, int64_t num_pages, const int32_t* block_table,
+                int64_t B, int64_t bt_width, const int32_t* seq_lens, float* scores,
+                int64_t ld_scores, void* stream) {
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "index_score: q_per_seq = %d (supported 1..8)", q_per_seq);
+  if (B < 0 || B > 65535) return fail(MX4_ERR_UNSUPPORTED, "index_score: B = %lld", (long long)B);
+  if (T != B * q_per_seq)
+    return fail(MX4_ERR_INVALID, "index_score: T = %lld != B * q_per_seq", (long long)T);
+  if (B == 0) return ok();
+  if (!iq || !idx_pages || !block_table || !seq_lens || !scores)
+    return fail(MX4_ERR_INVALID, "index_score: NULL pointer");
+  if (!aligned(iq, 16) || !aligned(idx_pages, 16) || idx_page_stride % 16 || !aligned(scores, 4))
+    return fail(MX4_ERR_INVALID, "index_score: misaligned iq, pages or page stride");
+  if (num_pages < 1 || idx_page_stride < mx4::kPageBytes || bt_width < 1 || ld_scores < 1)
+    return fail(MX4_ERR_INVALID, "index_score: num_pages, page stride, bt_width or ld invalid");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(mx4::launch_index_score(iq, q_per_seq, idx_pages, idx_page_stride,
+                                             num_pages, block_table, (int)B, bt_width, seq_lens,
+                                             scores, ld_scores, d->status, d->num_sms,
+                                             static_cast<cudaStream_t>(stream)),
+                     "index_score");
+}
+
+size_t topk_select_workspace(int64_t T, int k, int64_t ld_scores) {
+  (void)T;
+  (void)k;
+  (void)ld_scores;
+  return 0;
+}
+
+int topk_select(const float* scores, int64_t ld_scores, const int32_t* seq_lens, int64_t B,
+                int q_per_seq, int k, int32_t* topk_idx, void* ws, size_t ws_bytes,
+                void* stream) {
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "topk_select: q_per_seq = %d (supported 1..8)", q_per_seq);
+  if (k < 1 || k > 65536) return fail(MX4_ERR_UNSUPPORTED, "topk_select: k = %d", k);
+  if (B < 0 || B * q_per_seq > 0x7FFFFFFF)
+    return fail(MX4_ERR_INVALID, "topk_select: B = %lld", (long long)B);
+  const int64_t T = B * q_per_seq;
+  if (ws_bytes < topk_select_workspace(T, k, ld_scores))
+    return fail(MX4_ERR_WORKSPACE, "topk_select: workspace too small");
+  (void)ws;
+  if (T == 0) return ok();
+  if (!scores || !seq_lens || !topk_idx) return fail(MX4_ERR_INVALID, "topk_select: NULL pointer");
+  if (ld_scores < 1) return fail(MX4_ERR_INVALID, "topk_select: ld_scores < 1");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(mx4::launch_topk(scores, ld_scores, seq_lens, T, q_per_seq, k, topk_idx,
+                                      d->status, static_cast<cudaStream_t>(stream)),
+                     "topk_select");
+}
+
+size_t sparse_paged_decode_workspace(int64_t T, int k) {
+  if (T < 0 || k < 1) return 0;
+  return mx4::decode_workspace_bytes(T, k);
+}
+
+int sparse_paged_decode(const uint16_t* q, int64_t T, int q_per_seq, int H, int Hkv,
+                        const uint8_t* k_pages, const uint8_t* v_pages, int64_t kv_page_stride,
+                        int64_t kv_head_stride, int64_t num_pages, const int32_t* block_table,
+                        int64_t B, int64_t bt_width, const int32_t* seq_lens,
+                        const int32_t* topk_idx, int k, float scale, float* out, void* ws,
+                        size_t ws_bytes, void* stream) {
+  if (H != 16 || Hkv != 1)
+    return fail(MX4_ERR_UNSUPPORTED,
+                "sparse_paged_decode: H = %d, Hkv = %d (this build: 16 query heads, 1 KV head)",
+                H, Hkv);
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode: q_per_seq = %d", q_per_seq);
+  if (k < 1 || k > 65536) return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode: k = %d", k);
+  if (B < 0 || T != B * q_per_seq)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode: T != B * q_per_seq");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode: scale is not finite");
+  if (ws_bytes < sparse_paged_decode_workspace(T, k))
+    return fail(MX4_ERR_WORKSPACE, "sparse_paged_decode: workspace %zu < %zu bytes", ws_bytes,
+                sparse_paged_decode_workspace(T, k));
+  if (T == 0) return ok();
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !topk_idx || !out || !ws)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode: NULL pointer");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 16) || !aligned(k_pages, 16) ||
+      !aligned(v_pages, 16) || kv_page_stride % 16 || kv_head_stride % 16)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode: misaligned buffer or stride");
+  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || bt_width < 1)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode: num_pages, page stride or bt_width");
+  (void)kv_head_stride;  // one KV head: head 0 sits at the page base
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(mx4::launch_decode(q, T, q_per_seq, k_pages, v_pages, kv_page_stride,
+                                        num_pages, block_table, bt_width, seq_lens, topk_idx, k,
+                                        scale, out, ws, d->status,
+                                        static_cast<cudaStream_t>(stream)),
+                     "sparse_paged_decode");
+}
+
+int mx4_check_status(void* stream, uint32_t* bits) {
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t h = 0;
+  cudaError_t e = cudaMemcpyAsync(&h, d->status, sizeof h, cudaMemcpyDeviceToHost, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d->status, 0, sizeof h, s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "mx4_check_status: %s", cudaGetErrorString(e));
+  if (bits) *bits = h;
+  if (h)
+    return fail(MX4_ERR_BOUNDS, "kernels skipped bad data: status bits 0x%x%s%s%s%s%s", h,
+                (h & MX4_STATUS_BAD_SLOT) ? " bad-slot" : "",
+                (h & MX4_STATUS_BAD_PAGE) ? " bad-page" : "",
+                (h & MX4_STATUS_BAD_LEN) ? " bad-seq-len" : "",
+                (h & MX4_STATUS_BAD_INDEX) ? " bad-topk-index" : "",
+                (h & MX4_STATUS_BAD_VALUE) ? " non-finite-input" : "");
+  return ok();
+}
+
+}  // extern "C"

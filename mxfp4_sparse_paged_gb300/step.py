@@ -1,0 +1,146 @@
+"""Resident MXFP4 page caches and one decode step through the C ABI.
+
+`PagedCaches` owns the three page pools of one layer (K and V [pages, 1, 8704],
+index-K [pages, 8704]) in device memory, poisoned with 0xFF so a read of a
+never-written row shows up as NaN, and fills them from a workload with
+mx4_insert through the shared page-128 slot mapping ("vllm.models.minimax_m3.
+amd.mono.dispatch", _slots_shared).
+
+`DecodeStep` holds the per-step buffers and workspaces and issues, on one
+stream, the hot path of a decode step: [mx4_insert of the new tokens] ->
+index_score -> topk_select -> sparse_paged_decode.  It allocates nothing per
+step.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import (index_score, mx4_insert, sparse_paged_decode, sparse_paged_decode_workspace,
+               topk_select, topk_select_workspace)
+from . import workloads as W
+
+
+class PagedCaches:
+    def __init__(self, num_pages: int, device="cuda", kv_heads: int = 1):
+        self.num_pages = num_pages
+        self.k_pages = torch.full((num_pages, kv_heads, W.PAGE_BYTES), W.POISON, dtype=torch.uint8,
+                                  device=device)
+        self.v_pages = torch.full_like(self.k_pages, W.POISON)
+        self.idx_pages = torch.full((num_pages, W.PAGE_BYTES), W.POISON, dtype=torch.uint8,
+                                    device=device)
+
+    def nbytes(self) -> int:
+        return 3 * self.num_pages * W.PAGE_BYTES
+
+    def insert_rows(self, k, v, idx_k, slots, stream=None):
+        mx4_insert(k, v, idx_k, slots, self.k_pages, self.v_pages, self.idx_pages, stream=stream)
+
+    def fill(self, wl: W.Workload, chunk: int = 32768, sequences=None):
+        """Insert tokens 0 .. prefilled(s)-1 of every (or the given) sequence."""
+        dev = self.k_pages.device
+        seqs = range(wl.B) if sequences is None else sequences
+        for s in seqs:
+            n = wl.prefilled(s)
+            for a in range(0, n, chunk):
+                b = min(n, a + chunk)
+                k = torch.from_numpy(wl.rows(s, W.K_ROWS, a, b)).to(dev).view(b - a, 1, W.HEAD_DIM)
+                v = torch.from_numpy(wl.rows(s, W.V_ROWS, a, b)).to(dev).view(b - a, 1, W.HEAD_DIM)
+                ik = torch.from_numpy(wl.rows(s, W.IDX_ROWS, a, b)).to(dev)
+                slots = torch.from_numpy(wl.slots(s, np.arange(a, b))).to(dev)
+                self.insert_rows(k, v, ik, slots)
+
+
+def step_inputs_host(wl: W.Workload):
+    """Host (numpy) inputs of one decode step: q/iq bf16 bits, the new tokens'
+    rows and slots (empty unless the workload inserts in the step)."""
+    q_bits, iq_bits = W.queries_bf16(wl)
+    if wl.spec.insert_in_step:
+        pos = wl.positions()
+        s_of_t = np.repeat(np.arange(wl.B), wl.q)
+        k = np.stack([wl.rows(int(s), W.K_ROWS, int(p), int(p) + 1)[0] for s, p in zip(s_of_t, pos)])
+        v = np.stack([wl.rows(int(s), W.V_ROWS, int(p), int(p) + 1)[0] for s, p in zip(s_of_t, pos)])
+        ik = np.stack([wl.rows(int(s), W.IDX_ROWS, int(p), int(p) + 1)[0]
+                       for s, p in zip(s_of_t, pos)])
+        slots = wl.step_slots()
+    else:
+        k = v = ik = np.zeros((0, W.HEAD_DIM), np.float32)
+        slots = np.zeros(0, np.int64)
+    return {"q": q_bits, "iq": iq_bits, "k": k, "v": v, "idx_k": ik, "slots": slots}
+
+
+class DecodeStep:
+    """Buffers and the kernel sequence of one decode step of workload `wl`."""
+
+    def __init__(self, wl: W.Workload, caches: PagedCaches, device="cuda"):
+        self.wl = wl
+        self.caches = caches
+        T, k = wl.T, wl.k
+        self.ld = int(wl.max_len)
+        self.scale = 1.0 / math.sqrt(W.HEAD_DIM)
+        self.block_table = torch.from_numpy(wl.block_table).to(device)
+        self.seq_lens = torch.from_numpy(wl.seq_lens).to(device)
+        self.q = torch.empty((T, W.Q_HEADS, W.HEAD_DIM), dtype=torch.bfloat16, device=device)
+        self.iq = torch.empty((T, W.HEAD_DIM), dtype=torch.bfloat16, device=device)
+        n_ins = T if wl.spec.insert_in_step else 0
+        self.k_new = torch.empty((n_ins, 1, W.HEAD_DIM), dtype=torch.float32, device=device)
+        self.v_new = torch.empty_like(self.k_new)
+        self.idx_new = torch.empty((n_ins, W.HEAD_DIM), dtype=torch.float32, device=device)
+        self.slots = torch.empty(n_ins, dtype=torch.int64, device=device)
+        self.scores = torch.empty((T, self.ld), dtype=torch.float32, device=device)
+        self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=device)
+        self.out = torch.empty((T, W.Q_HEADS, W.HEAD_DIM), dtype=torch.float32, device=device)
+        tws = topk_select_workspace(T, k, self.ld)
+        self.topk_ws = torch.empty(max(tws, 16), dtype=torch.uint8, device=device) if tws else None
+        self.dec_ws = torch.empty(sparse_paged_decode_workspace(T, k), dtype=torch.uint8,
+                                  device=device)
+
+    def load_inputs(self, host: dict, non_blocking=False):
+        """Copy one step's host inputs (numpy or pinned torch) into the device buffers."""
+        def put(dst, src, view_dtype=None):
+            if isinstance(src, np.ndarray):
+                src = torch.from_numpy(src)
+            if view_dtype is not None:
+                src = src.view(view_dtype)
+            dst.copy_(src.view(dst.shape), non_blocking=non_blocking)
+        put(self.q, host["q"].view(np.int16) if isinstance(host["q"], np.ndarray) else host["q"],
+            torch.bfloat16)
+        put(self.iq, host["iq"].view(np.int16) if isinstance(host["iq"], np.ndarray) else host["iq"],
+            torch.bfloat16)
+        if self.slots.numel():
+            put(self.k_new, host["k"])
+            put(self.v_new, host["v"])
+            put(self.idx_new, host["idx_k"])
+            put(self.slots, host["slots"])
+
+    def run(self, stream=None, events=None):
+        """Enqueue the step on `stream`.  `events` (optional dict name -> (start, end)
+        CUDA events) brackets each kernel for per-kernel timing."""
+        c = self.caches
+        wl = self.wl
+
+        def timed(name, fn):
+            if events and name in events:
+                events[name][0].record(stream)
+                fn()
+                events[name][1].record(stream)
+            else:
+                fn()
+
+        if self.slots.numel():
+            timed("mx4_insert", lambda: c.insert_rows(self.k_new, self.v_new, self.idx_new,
+                                                      self.slots, stream=stream))
+        timed("index_score", lambda: index_score(self.iq, wl.q, c.idx_pages, self.block_table,
+                                                 self.seq_lens, self.scores, stream=stream))
+        timed("topk_select", lambda: topk_select(self.scores, self.seq_lens, wl.q, wl.k,
+                                                 self.topk_idx, self.topk_ws, stream=stream))
+        timed("sparse_paged_decode", lambda: sparse_paged_decode(
+            self.q, wl.q, c.k_pages, c.v_pages, self.block_table, self.seq_lens, self.topk_idx,
+            self.scale, self.out, self.dec_ws, stream=stream))
+
+    def launches_per_step(self) -> int:
+        """Kernels this library launches per step (insert, score, top-k, decode split +
+        merge)."""
+        return (1 if self.slots.numel() else 0) + 1 + 1 + 2

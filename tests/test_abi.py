@@ -1,0 +1,98 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every entry point
+declared in include/mx4sp.h; host-side argument checks answer without a GPU
+(they return before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mx4sp.h")
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[\w]+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from mxfp4_sparse_paged_gb300 import build
+    path = build.build()
+    import mxfp4_sparse_paged_gb300 as m
+    m._load()
+    return ctypes.CDLL(path)
+
+
+def test_header_declares_the_four_steps():
+    names = _declared()
+    for n in ("mx4_insert", "index_score", "topk_select", "sparse_paged_decode",
+              "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
+              "mx4_last_error", "mx4_page_bytes"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for n in _declared():
+        assert hasattr(lib, n), n
+
+
+def test_page_bytes(lib):
+    import mxfp4_sparse_paged_gb300 as m
+    assert m.mx4_page_bytes() == 8704 == 128 * 68
+
+
+def test_library_is_sm103a_only():
+    from mxfp4_sparse_paged_gb300 import build
+    assert build.ARCH == ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def _err(m):
+    return m.mx4_last_error()
+
+
+def test_host_validation_without_gpu(lib):
+    import mxfp4_sparse_paged_gb300 as m
+    L = m._load()
+    # negative T
+    assert L.mx4_insert(None, None, None, -1, 1, None, None, None, 8704, 8704, None, 8704, 1,
+                        None) == -1
+    assert "T" in _err(m)
+    # unsupported KV head count
+    assert L.mx4_insert(None, None, None, 1, 0, None, None, None, 8704, 8704, None, 8704, 1,
+                        None) == -2
+    # T == 0 is a no-op
+    assert L.mx4_insert(None, None, None, 0, 1, None, None, None, 8704, 8704, None, 8704, 1,
+                        None) == 0
+    # NULL pointers
+    assert L.mx4_insert(None, None, None, 4, 1, None, None, None, 8704, 8704, None, 8704, 1,
+                        None) == -1
+    # index_score: q out of range, T mismatch, empty batch
+    assert L.index_score(None, 1, 9, None, 8704, 1, None, 1, 1, None, None, 1, None) == -2
+    assert L.index_score(None, 3, 1, None, 8704, 1, None, 2, 1, None, None, 1, None) == -1
+    assert L.index_score(None, 0, 1, None, 8704, 1, None, 0, 1, None, None, 1, None) == 0
+    # topk: k out of range
+    assert L.topk_select(None, 1, None, 1, 1, 0, None, None, 0, None) == -2
+    # decode: unsupported head geometry, workspace too small
+    assert L.sparse_paged_decode(None, 1, 1, 8, 1, None, None, 8704, 8704, 1, None, 1, 1, None,
+                                 None, 16, ctypes.c_float(0.1), None, None, 0, None) == -2
+    assert "16 query heads" in _err(m)
+    need = L.sparse_paged_decode_workspace(1, 2048)
+    assert need > 0
+    assert L.sparse_paged_decode(None, 1, 1, 16, 1, None, None, 8704, 8704, 1, None, 1, 1, None,
+                                 None, 2048, ctypes.c_float(0.1), None, None, need - 1,
+                                 None) == -3
+    assert L.sparse_paged_decode(None, 1, 1, 16, 1, None, None, 8704, 8704, 1, None, 1, 1, None,
+                                 None, 2048, ctypes.c_float(float("nan")), None, None, need,
+                                 None) == -1
+
+
+def test_workspace_sizes(lib):
+    import mxfp4_sparse_paged_gb300 as m
+    # 16 heads x (128 outputs + max + sum) fp32 per (token, split of 256 selected)
+    assert m.sparse_paged_decode_workspace(64, 2048) == 64 * 8 * 16 * 130 * 4
+    assert m.sparse_paged_decode_workspace(1, 1) == 16 * 130 * 4
+    assert m.topk_select_workspace(64, 2048, 131072) >= 0

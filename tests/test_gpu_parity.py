@@ -1,0 +1,324 @@
+"""GPU parity: every C-ABI call against the CPU oracle on the same seeded inputs.
+
+Page bytes and top-k sets are compared bit for bit (top-k: except tokens within
+1e-5 relative of the k-th score); scores within the fp32 rounding bound of a
+128-term dot product; attention outputs within max-abs 2e-3.  Small workloads
+are compared in full, the full-size ones on sampled sequences, in the launch
+configuration the benchmark times (DecodeStep).
+"""
+import dataclasses
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import mxfp4_sparse_paged_gb300 as m
+from mxfp4_sparse_paged_gb300 import workloads as W
+from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, step_inputs_host
+
+from _sides import ATTN_ABS, OracleSide, check_scores, check_topk
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")]
+
+DEV = "cuda"
+
+
+def _gpu_step(wl):
+    caches = PagedCaches(wl.num_pages, device=DEV)
+    caches.fill(wl)
+    step = DecodeStep(wl, caches, device=DEV)
+    host = step_inputs_host(wl)
+    step.load_inputs(host)
+    step.run()
+    m.mx4_check_status()
+    return caches, step, host
+
+
+def _compare(wl, seqs, caches, step, host):
+    orc = OracleSide(wl, seqs, host)
+    kp, vp, ip = (caches.k_pages.cpu().numpy(), caches.v_pages.cpu().numpy(),
+                  caches.idx_pages.cpu().numpy())
+    for s in seqs:
+        pg = orc.pages_of(s)
+        assert np.array_equal(kp[pg], orc.kp[pg]), f"K pages of sequence {s}"
+        assert np.array_equal(vp[pg], orc.vp[pg]), f"V pages of sequence {s}"
+        assert np.array_equal(ip[pg], orc.ip[pg]), f"index pages of sequence {s}"
+    sc, mag = orc.scores()
+    tok = orc.tok
+    L_tok = np.repeat(orc.lens, wl.q).astype(np.int64)
+    n_tok = wl.positions()[tok] + 1
+    check_scores(step.scores.cpu().numpy()[tok], sc, mag, L_tok)
+    sel = orc.topk(sc)
+    g_sel = step.topk_idx.cpu().numpy()[tok]
+    check_topk(g_sel, sel, sc, n_tok)
+    want = orc.attend(sel)
+    # chain output where the selections agree exactly
+    g_out = step.out.cpu().numpy()[tok]
+    same = [i for i in range(len(tok)) if np.array_equal(g_sel[i], sel[i])]
+    assert len(same) >= len(tok) // 2
+    err = max(float(np.abs(g_out[i] - want[i]).max()) for i in same)
+    assert err <= ATTN_ABS, f"chain attention max-abs {err}"
+    # the GPU decode fed the oracle's selection: every sampled token
+    idx = step.topk_idx.clone()
+    idx[torch.as_tensor(tok, device=DEV)] = torch.as_tensor(sel, device=DEV)
+    out = torch.empty_like(step.out)
+    m.sparse_paged_decode(step.q, wl.q, caches.k_pages, caches.v_pages, step.block_table,
+                          step.seq_lens, idx, step.scale, out, step.dec_ws)
+    m.mx4_check_status()
+    err2 = float(np.abs(out.cpu().numpy()[tok] - want).max())
+    assert err2 <= ATTN_ABS, f"decode max-abs {err2}"
+    return err, err2
+
+
+# ----------------------------------------------------------------- workloads
+
+def test_config0_tiny_full():
+    wl = W.make(0)
+    _compare(wl, [0], *_gpu_step(wl))
+
+
+def test_config1_full():
+    wl = W.make(1)
+    _compare(wl, range(wl.B), *_gpu_step(wl))
+
+
+def test_config2_sampled():
+    wl = W.make(2)
+    L = wl.seq_lens
+    seqs = sorted({int(np.argmin(L)), int(np.argmax(L)), 7, 33})
+    _compare(wl, seqs, *_gpu_step(wl))
+
+
+def test_config3_sampled_multi_token():
+    wl = W.make(3)
+    _compare(wl, [0, 15], *_gpu_step(wl))
+
+
+def test_config4_sampled_with_insert():
+    wl = W.make(4)
+    L = wl.seq_lens
+    short = int(np.nonzero(L < 2048)[0][0])
+    seqs = sorted({short, int(np.argmax(L)), int(np.argmin(L)), 5, 100, 250})
+    _compare(wl, seqs, *_gpu_step(wl))
+
+
+def _custom(lens, q, k, seed, insert=False, outliers=False):
+    lens = np.asarray(lens, np.int64)
+    base = W.SPECS[4 if outliers else 1]
+    spec = dataclasses.replace(base, name="custom", batch=len(lens), q=q, k=k, seed=seed,
+                               insert_in_step=insert, lens=("fixed", 0))
+    pages = (lens + 127) // 128
+    P = int(pages.sum()) + 3
+    ids = np.random.default_rng(seed).permutation(P)
+    bt = np.full((len(lens), int(pages.max())), -1, np.int32)
+    o = 0
+    for s, n in enumerate(pages):
+        bt[s, :n] = ids[o:o + n]
+        o += n
+    ch = ()
+    if outliers:
+        ch = ((3,), (64,), (127,))
+    return W.Workload(spec, lens.astype(np.int32), bt, P, ch)
+
+
+@pytest.mark.parametrize("q", [1, 2, 3, 4])
+def test_ragged_lengths_all_tokens(q):
+    # lengths around page and split boundaries, k above and below the context
+    wl = _custom([q, 127, 128, 129, 255, 256, 257, 700, 1500], q=q, k=300, seed=40 + q)
+    _compare(wl, range(wl.B), *_gpu_step(wl))
+
+
+def test_ragged_with_insert_and_outliers():
+    wl = _custom([1, 2, 129, 1000, 3000], q=1, k=2048, seed=77, insert=True, outliers=True)
+    _compare(wl, range(wl.B), *_gpu_step(wl))
+
+
+# ----------------------------------------------------------------- insert edges
+
+def _insert_both(rows):
+    """Insert rows (fp32 [n, 128]) as index keys on both sides; return both pools."""
+    n = rows.shape[0]
+    P = (n + 127) // 128
+    slots = np.arange(n, dtype=np.int64)
+    ip_o = np.full((P, 8704), 0xFF, np.uint8)
+    oracle.mx4_insert(None, None, rows, slots, None, None, ip_o)
+    kp = torch.full((P, 1, 8704), 0xFF, dtype=torch.uint8, device=DEV)
+    vp = torch.full_like(kp, 0xFF)
+    ip = torch.full((P, 8704), 0xFF, dtype=torch.uint8, device=DEV)
+    r = torch.from_numpy(rows).to(DEV)
+    m.mx4_insert(r.view(n, 1, 128), r.view(n, 1, 128), r, torch.from_numpy(slots).to(DEV),
+                 kp, vp, ip)
+    m.mx4_check_status()
+    return ip.cpu().numpy(), ip_o
+
+
+def test_insert_special_values_bit_exact():
+    rows = np.zeros((64, 128), np.float32)
+    f32 = np.finfo(np.float32)
+    rows[1, :] = -0.0
+    rows[2, 0] = f32.tiny                       # smallest normal
+    rows[3, 0] = np.float32(2.0 ** -149)        # smallest subnormal
+    rows[3, 1] = -np.float32(2.0 ** -140)
+    rows[4, :32] = f32.max
+    rows[4, 1] = -f32.max
+    rows[5, :32] = np.float32(3e38) * np.linspace(-1, 1, 32, dtype=np.float32)
+    # exact ties after scaling by 2^E (block amax 6 -> E = 0)
+    ties = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    rows[6, :7], rows[6, 7] = ties, 6.0
+    rows[6, 32:39], rows[6, 39] = -ties, -6.0
+    rows[7, :7], rows[7, 7] = ties * 2.0 ** -20, 6.0 * 2.0 ** -20
+    rows[8, :] = np.float32(7.999)              # saturation
+    rows[9, :] = np.float32(np.nextafter(np.float32(2), np.float32(0)))
+    rng = np.random.default_rng(1)
+    rows[10:] = (rng.standard_normal((54, 128)) *
+                 2.0 ** rng.integers(-140, 120, (54, 1))).astype(np.float32)
+    got, want = _insert_both(rows)
+    assert np.array_equal(got, want)
+
+
+def test_insert_dense_sweep_of_scaled_values():
+    # Every 257th fp32 bit pattern in [0, 8) (both signs), 31 per block next to an
+    # anchor of 4.0 so the block exponent is 0 and y = x.
+    pats = np.arange(0, np.float32(8.0).view(np.uint32), 257, dtype=np.uint32)
+    vals = pats.view(np.float32)
+    vals = np.concatenate([vals, -vals])
+    nb = (len(vals) + 30) // 31
+    blocks = np.zeros((nb, 32), np.float32)
+    blocks[:, 0] = 4.0
+    flat = np.zeros(nb * 31, np.float32)
+    flat[:len(vals)] = vals
+    blocks[:, 1:] = flat.reshape(nb, 31)
+    nrow = (nb + 3) // 4
+    rows = np.zeros((nrow * 4, 32), np.float32)
+    rows[:nb] = blocks
+    rows = rows.reshape(nrow, 128)
+    for a in range(0, nrow, 1 << 16):
+        got, want = _insert_both(np.ascontiguousarray(rows[a:a + (1 << 16)]))
+        assert np.array_equal(got, want)
+
+
+# ----------------------------------------------------------------- top-k exact
+
+def test_topk_bit_exact_on_shared_scores():
+    # Same fp32 scores on both sides: the selection must be identical.  Rows with
+    # heavy ties, negative values, +/-0, k below/at/above the context.
+    rng = np.random.default_rng(5)
+    B, q = 12, 2
+    lens = np.array([1, 2, 5, 300, 2047, 2048, 2049, 4097, 10000, 65536, 3, 131072], np.int32)
+    lens = np.maximum(lens, q)
+    ld = int(lens.max())
+    sc = np.full((B * q, ld), -np.inf, np.float32)
+    for t in range(B * q):
+        n = int(lens[t // q]) - q + t % q + 1
+        kind = t % 4
+        if kind == 0:
+            row = rng.standard_normal(n).astype(np.float32) * 10
+        elif kind == 1:
+            row = rng.integers(-3, 4, n).astype(np.float32)          # heavy ties
+        elif kind == 2:
+            row = np.where(rng.random(n) < 0.5, 0.0, -0.0).astype(np.float32)
+        else:
+            row = -np.abs(rng.standard_normal(n)).astype(np.float32)
+        sc[t, :n] = row
+    lens_ok = lens
+    for k in (1, 7, 2048):
+        want = oracle.topk_select(sc.astype(np.float64), lens_ok, q, k)
+        d_sc = torch.from_numpy(sc).to(DEV)
+        out = torch.empty((B * q, k), dtype=torch.int32, device=DEV)
+        ws_n = m.topk_select_workspace(B * q, k, ld)
+        ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=DEV)
+        m.topk_select(d_sc, torch.from_numpy(lens_ok).to(DEV), q, k, out, ws)
+        m.mx4_check_status()
+        assert np.array_equal(out.cpu().numpy(), want), f"k={k}"
+
+
+# ----------------------------------------------------------------- decode edges
+
+def test_decode_single_selected_token_is_exact_value_row():
+    wl = _custom([300], q=1, k=8, seed=3)
+    caches, step, host = _gpu_step(wl)
+    orc = OracleSide(wl, [0], host)
+    for i in (0, 127, 128, 299):
+        idx = torch.full((1, 8), -1, dtype=torch.int32, device=DEV)
+        idx[0, 0] = i
+        out = torch.empty_like(step.out)
+        m.sparse_paged_decode(step.q, 1, caches.k_pages, caches.v_pages, step.block_table,
+                              step.seq_lens, idx, step.scale, out, step.dec_ws)
+        pg = int(wl.block_table[0, i // 128])
+        vrow = oracle.dequant_row(orc.vp[pg, 0], i % 128)
+        assert np.array_equal(out.cpu().numpy()[0].astype(np.float64),
+                              np.broadcast_to(vrow, (16, 128)))
+
+
+def test_decode_output_invariant_to_split_boundaries():
+    # The same selection written in one list, or padded so it crosses split
+    # boundaries differently, gives the same result within fp32 rounding.
+    wl = _custom([3000], q=1, k=2048, seed=9)
+    caches, step, host = _gpu_step(wl)
+    sel = step.topk_idx.clone()
+    out1 = torch.empty_like(step.out)
+    m.sparse_paged_decode(step.q, 1, caches.k_pages, caches.v_pages, step.block_table,
+                          step.seq_lens, sel, step.scale, out1, step.dec_ws)
+    wide = torch.full((1, 4096), -1, dtype=torch.int32, device=DEV)
+    valid = sel[0][sel[0] >= 0]
+    wide[0, 100:100 + valid.numel()] = valid
+    ws = torch.empty(m.sparse_paged_decode_workspace(1, 4096), dtype=torch.uint8, device=DEV)
+    out2 = torch.empty_like(step.out)
+    m.sparse_paged_decode(step.q, 1, caches.k_pages, caches.v_pages, step.block_table,
+                          step.seq_lens, wide, step.scale, out2, ws)
+    m.mx4_check_status()
+    assert float((out1 - out2).abs().max()) <= 1e-5
+
+
+# ----------------------------------------------------------------- bad data
+
+def test_bad_slot_page_and_index_are_flagged_not_faulted():
+    wl = _custom([200, 300], q=1, k=64, seed=11)
+    caches, step, host = _gpu_step(wl)
+    P = wl.num_pages
+    # slot beyond the pool
+    r = torch.zeros((1, 1, 128), device=DEV)
+    with pytest.raises(m.Mx4Error) as ei:
+        m.mx4_insert(r, r, r[:, 0], torch.tensor([P * 128], device=DEV), caches.k_pages,
+                     caches.v_pages, caches.idx_pages)
+        m.mx4_check_status()
+    assert ei.value.bits & 0x1
+    # a block-table entry outside the pool
+    bt = step.block_table.clone()
+    bt[1, 0] = P + 5
+    with pytest.raises(m.Mx4Error) as ei:
+        m.index_score(step.iq, 1, caches.idx_pages, bt, step.seq_lens, step.scores)
+        m.mx4_check_status()
+    assert ei.value.bits & 0x2
+    # a top-k index beyond the token's position
+    idx = step.topk_idx.clone()
+    idx[0, 0] = 250
+    with pytest.raises(m.Mx4Error) as ei:
+        m.sparse_paged_decode(step.q, 1, caches.k_pages, caches.v_pages, step.block_table,
+                              step.seq_lens, idx, step.scale, step.out, step.dec_ws)
+        m.mx4_check_status()
+    assert ei.value.bits & 0x8
+    # a sequence length beyond the block table
+    sl = step.seq_lens.clone()
+    sl[0] = 10 ** 6
+    with pytest.raises(m.Mx4Error) as ei:
+        m.index_score(step.iq, 1, caches.idx_pages, step.block_table, sl, step.scores)
+        m.mx4_check_status()
+    assert ei.value.bits & 0x4
+    m.mx4_check_status()  # cleared
+
+
+def test_empty_batch_is_a_no_op():
+    z = torch.empty((0, 128), dtype=torch.bfloat16, device=DEV)
+    pages = torch.zeros((1, 8704), dtype=torch.uint8, device=DEV)
+    m.index_score(z, 1, pages, torch.zeros((0, 1), dtype=torch.int32, device=DEV),
+                  torch.zeros(0, dtype=torch.int32, device=DEV),
+                  torch.zeros((0, 1), dtype=torch.float32, device=DEV))
+    r = torch.empty((0, 1, 128), device=DEV)
+    kv = torch.zeros((1, 1, 8704), dtype=torch.uint8, device=DEV)
+    m.mx4_insert(r, r, r[:, 0], torch.empty(0, dtype=torch.int64, device=DEV), kv, kv.clone(),
+                 pages)
+    m.mx4_check_status()
