@@ -181,6 +181,33 @@ int sparse_paged_decode(const uint16_t *q, int64_t T, int q_per_seq, int H, int 
 size_t sparse_paged_decode_workspace(int64_t T, int k);
 
 /* ---------------------------------------------------------------------------
+ * sparse_paged_decode_noalloc -- sparse_paged_decode without a caller
+ * workspace.  The paper has no counterpart for it: it exists for callers that cannot
+ * allocate device memory (a host framework that owns all device memory and
+ * gives an extension only the operation's inputs and outputs, or a C or
+ * foreign-language runtime with no device allocator).  Same arguments, result
+ * and errors as sparse_paged_decode, minus ws/ws_bytes.
+ *
+ * The split workspace lives in a fixed array inside the library of
+ * MX4_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory, which every GPU that
+ * loads the library holds until the process exits.  A call whose workspace
+ * (sparse_paged_decode_workspace(T, k)) exceeds it returns MX4_ERR_WORKSPACE
+ * without launching.  The call allocates and frees nothing.  The first call on
+ * a device looks up the array's device address (cudaGetSymbolAddress) with
+ * that device current: make it before any stream capture.  All calls on a
+ * device share the array, so calls that overlap on the GPU race; nothing in it
+ * needs clearing between calls.
+ * ------------------------------------------------------------------------- */
+#define MX4_NOALLOC_SCRATCH_BYTES (32u << 20)
+int sparse_paged_decode_noalloc(const uint16_t *q, int64_t T, int q_per_seq, int H, int Hkv,
+                                const uint8_t *k_pages, const uint8_t *v_pages,
+                                int64_t kv_page_stride, int64_t kv_head_stride,
+                                int64_t num_pages, const int32_t *block_table, int64_t B,
+                                int64_t bt_width, const int32_t *seq_lens,
+                                const int32_t *topk_idx, int k, float scale, float *out,
+                                void *stream);
+
+/* ---------------------------------------------------------------------------
  * mx4_check_status -- synchronise `stream`, return MX4_OK if no kernel of this
  * library has flagged bad data on the current device since the last check,
  * else MX4_ERR_BOUNDS with the flagged MX4_STATUS_* bits in *bits (if bits is

@@ -20,12 +20,14 @@ import torch
 
 __all__ = ["mx4_insert", "index_score", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
+           "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
            "mx4_last_error", "mx4_page_bytes", "library_path", "Mx4Error", "PAGE_BYTES",
            "PAGE_TOKENS", "HEAD_DIM"]
 
 PAGE_BYTES = 8704
 PAGE_TOKENS = 128
 HEAD_DIM = 128
+NOALLOC_SCRATCH_BYTES = 32 << 20
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "_build", "libmx4sp.so")
@@ -75,6 +77,9 @@ def _load():
                                             i64, P, P, i32, ctypes.c_float, P, P, sz, P]
         lib.sparse_paged_decode_workspace.restype = sz
         lib.sparse_paged_decode_workspace.argtypes = [i64, i32]
+        lib.sparse_paged_decode_noalloc.restype = i32
+        lib.sparse_paged_decode_noalloc.argtypes = [P, i64, i32, i32, i32, P, P, i64, i64, i64, P,
+                                                    i64, i64, P, P, i32, ctypes.c_float, P, P]
         lib.mx4_check_status.restype = i32
         lib.mx4_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         _lib = lib
@@ -195,6 +200,29 @@ def sparse_paged_decode(q, q_per_seq, k_pages, v_pages, block_table, seq_lens, t
         k_pages.stride(0), k_pages.stride(1), int(k_pages.shape[0]), _ptr(block_table),
         int(seq_lens.shape[0]), int(block_table.shape[1]), _ptr(seq_lens), _ptr(topk_idx),
         int(topk_idx.shape[1]), float(scale), _ptr(out), _ptr(ws), ws_bytes, _stream(stream)))
+
+
+def sparse_paged_decode_noalloc(q, q_per_seq, k_pages, v_pages, block_table, seq_lens, topk_idx,
+                                scale, out, stream=None):
+    """sparse_paged_decode for callers that cannot allocate device memory: the split
+    workspace is the library's own fixed NOALLOC_SCRATCH_BYTES array, so no
+    workspace argument is taken and nothing is allocated.  Calls on one device
+    share that array and must not overlap on the GPU."""
+    _need(q, torch.bfloat16, "q")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _need(out, torch.float32, "out")
+    _pages(k_pages, "k_pages", 3)
+    _pages(v_pages, "v_pages", 3)
+    if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    T, H = int(q.shape[0]), int(q.shape[1])
+    _check(_load().sparse_paged_decode_noalloc(
+        _ptr(q), T, int(q_per_seq), H, int(k_pages.shape[1]), _ptr(k_pages), _ptr(v_pages),
+        k_pages.stride(0), k_pages.stride(1), int(k_pages.shape[0]), _ptr(block_table),
+        int(seq_lens.shape[0]), int(block_table.shape[1]), _ptr(seq_lens), _ptr(topk_idx),
+        int(topk_idx.shape[1]), float(scale), _ptr(out), _stream(stream)))
 
 
 def mx4_check_status(stream=None) -> int:

@@ -243,3 +243,90 @@ int mx4_check_status(void* stream, uint32_t* bits) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// sparse_paged_decode_noalloc: sparse_paged_decode for callers that cannot
+// allocate device memory.
+//
+// Some callers of this library have no way to obtain scratch memory: a host
+// framework that owns every byte of device memory through its own pool and
+// hands an extension only the operation's inputs and outputs, or a plain C or
+// foreign-language runtime that can pass through buffers it was given but has
+// no device allocator of its own.  For them this entry point keeps the split
+// workspace in a fixed array of device memory that belongs to the library
+// (every GPU that loads the library holds it until the process exits), so the
+// call itself allocates nothing.
+//
+// The array's host-side name is not a device address, so its address is taken
+// with cudaGetSymbolAddress once per device, by the first call on that device
+// with the device current; make that first call before any stream capture.
+// All calls on a device share the array: two calls whose kernels overlap on
+// the GPU (different streams, no ordering between them) race on it.  Nothing in
+// it needs to start at zero -- the split kernel writes every (max, sum, output)
+// entry it owns before the merge kernel reads it -- so the previous call's
+// contents are harmless.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[MX4_NOALLOC_SCRATCH_BYTES];
+
+namespace {
+void* g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev < 0 || dev >= kMaxDevices) return fail(MX4_ERR_UNSUPPORTED, "device id %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess || p == nullptr)
+      return fail(MX4_ERR_CUDA, "cudaGetSymbolAddress(scratch): %s", cudaGetErrorString(e));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return MX4_OK;
+}
+}  // namespace
+
+extern "C" int sparse_paged_decode_noalloc(
+    const uint16_t* q, int64_t T, int q_per_seq, int H, int Hkv, const uint8_t* k_pages,
+    const uint8_t* v_pages, int64_t kv_page_stride, int64_t kv_head_stride, int64_t num_pages,
+    const int32_t* block_table, int64_t B, int64_t bt_width, const int32_t* seq_lens,
+    const int32_t* topk_idx, int k, float scale, float* out, void* stream) {
+  if (H != 16 || Hkv != 1)
+    return fail(MX4_ERR_UNSUPPORTED,
+                "sparse_paged_decode_noalloc: H = %d, Hkv = %d (16 query heads, 1 KV head)", H,
+                Hkv);
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode_noalloc: q_per_seq = %d", q_per_seq);
+  if (k < 1 || k > 65536)
+    return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode_noalloc: k = %d", k);
+  if (B < 0 || T != B * q_per_seq)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: T != B * q_per_seq");
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: scale is not finite");
+  const size_t need = mx4::decode_workspace_bytes(T, k);
+  if (need > (size_t)MX4_NOALLOC_SCRATCH_BYTES)
+    return fail(MX4_ERR_WORKSPACE,
+                "sparse_paged_decode_noalloc: T = %lld, k = %d needs %zu bytes of scratch, more "
+                "than the library's fixed %zu; use sparse_paged_decode with a caller workspace",
+                (long long)T, k, need, (size_t)MX4_NOALLOC_SCRATCH_BYTES);
+  if (T == 0) return ok();
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !topk_idx || !out)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: NULL pointer");
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+      kv_page_stride % 16 || kv_head_stride % 16)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: misaligned buffer or stride");
+  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || bt_width < 1)
+    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: num_pages, page stride or bt_width");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  void* scratch = nullptr;
+  if (int rc = noalloc_scratch(&scratch)) return rc;
+  return cuda_result(mx4::launch_decode(q, T, q_per_seq, k_pages, v_pages, kv_page_stride,
+                                        num_pages, block_table, bt_width, seq_lens, topk_idx, k,
+                                        scale, out, scratch, d->status,
+                                        static_cast<cudaStream_t>(stream)),
+                     "sparse_paged_decode_noalloc");
+}
