@@ -6,40 +6,147 @@
 // mxfp4_pages", mxfp4_page_views: the [pages, heads, 128, 64] /
 // [pages, heads, 128, 4] pair pa_decode takes).  Head geometry: one rank's
 // q(2048) | k(128) | v(128) rows ("vllm.models.minimax_m3.amd.mono.weights",
-// _build_cp_qkv), i.e. 16 query heads over one KV head.
+// _build_cp_qkv), i.e. 16 query heads over one KV head, which makes the 16
+// heads the M = 16 side of a tensor-core MMA.
 //
-// split kernel: one CTA per (decode token, split of kSplitTokens selected
-//   entries).  Phase 1 resolves the split's indices to page rows; phase 2
-//   gathers those K and V rows (data + scales) into shared memory with
-//   independent 16-byte loads; phase 3 runs the online softmax.  Thread
-//   (h, part) owns query head h = tid/8 and dims 16*part .. 16*part+15: it
-//   dots its 16 dims, the 8 threads of a head combine with xor-shuffles, and
-//   it accumulates its 16 output dims.  The split writes its unnormalised
-//   output, running max (log2 units) and running sum to the workspace.
-// merge kernel: one CTA per decode token combines the splits of each head.
+// split kernel -- one CTA of 8 warps per (decode token, split of up to 512
+// selected entries):
+//   1. Resolve the split's indices to page rows; read each entry's K and V scale
+//      words; find the split's largest K scale (all blocks) and V scale (per
+//      32-dim block); turn every entry's scales into exact f16 multipliers
+//      2^(scale - reference), so that dequantised K/V values fit f16 exactly.
+//   2. Each warp streams its 16-entry tiles through a 4-stage cp.async ring
+//      (64 B of K data + 64 B of V data per entry, rows padded to 80 B so the
+//      fragment loads are bank-conflict free).
+//   3. Per tile: e2m1 -> f16 with the hardware cvt (exact grid values), times the
+//      multiplier; S = Q K^T with mma.sync m16n8k16 (Q = 16 heads x 128, f16,
+//      scaled by a power of two so bf16 fits f16 exactly); online softmax in
+//      fp32 (log2 units, lazy rescaling); P split into f16 hi + lo parts so
+//      P V keeps ~22 bits; O += P V with mma.sync, V fragments built by zipping
+//      the nibbles of two tokens so one cvt yields a (token, token) pair.
+//   4. The 8 warps' (max, sum, O) are merged in shared memory and the split
+//      writes its unnormalised output, running max (log2 units) and sum.
+// merge kernel -- one CTA per decode token combines the splits of each head.
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 
 namespace mx4 {
 
-constexpr int kSplitTokens = 256;
-constexpr int kDecThreads = 128;  // 16 heads x 8 parts
 constexpr int kHeads = 16;
+constexpr int kDecWarps = 8;
+constexpr int kDecThreads = kDecWarps * 32;
+constexpr int kSplitTokens = 512;                   // selected entries per CTA
+constexpr int kTile = 16;                           // entries per MMA tile
+constexpr int kTilesPerWarp = kSplitTokens / kTile / kDecWarps;  // 4
+constexpr int kStages = 4;                          // cp.async ring depth per warp
+constexpr int kRowPitch = 80;                       // staged row pitch (64 B + 16 B pad)
+constexpr int kStageBytes = 2 * kTile * kRowPitch;  // K rows then V rows: 2560 B
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kPOffset = 7.f;  // p' = 2^(logit - m + 7)
+constexpr float kLazy = 8.f;     // rescale only when the max grows by more than this
+static_assert(kTilesPerWarp * kTile * kDecWarps == kSplitTokens, "split geometry");
+static_assert(2 * kDecThreads == kSplitTokens, "one entry pair per thread in the set-up phase");
+static_assert(kDecWarps * kHeads * kHeadDim * 4 <= kDecWarps * kStages * kStageBytes,
+              "merge buffer fits in the staging ring");
 
-__global__ void __launch_bounds__(kDecThreads)
+struct DecodeSmem {
+  uint8_t stage[kDecWarps][kStages][kStageBytes];  // 80 KB; reused by the final merge
+  uint32_t kmul[kSplitTokens][4];      // f16x2 (m, m): K multiplier of block b of entry r
+  uint32_t vmul[kSplitTokens / 2][4];  // f16x2 (m_2u, m_2u+1), blocks in slot order 0,2,1,3
+  int64_t off[kSplitTokens];           // byte offset of the entry's page + row*64, or -1
+  uint8_t ok[kSplitTokens];
+  float red_m[kDecWarps][kHeads];
+  float red_l[kDecWarps][kHeads];
+  uint32_t red_k[kDecWarps];
+  uint32_t red_v[kDecWarps];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0));
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+}
+
+// The four bytes of w, each e2m1x2 -> f16x2 (low nibble -> low half), exact.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
+  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
+      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
+      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+      : "r"(w));
+}
+
+__device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t lop_merge(uint32_t a, uint32_t b, uint32_t m) {
+  return (a & m) | (b & ~m);
+}
+
+__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
+                                        uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float f16_lo(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v & 0xFFFFu)));
+}
+__device__ __forceinline__ float f16_hi(uint32_t v) {
+  return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
+}
+
+// f16 bit pattern of 2^e for e <= 0: normal down to 2^-14, subnormal down to
+// 2^-24, 0 below.  A scale byte of 255 (NaN) gives an f16 NaN.
+__device__ __forceinline__ uint32_t f16_pow2(uint32_t byte, uint32_t ref) {
+  if (byte == 255u) return 0x7E00u;
+  const int e = (int)byte - (int)ref;
+  if (e >= -14) return (uint32_t)(e + 15) << 10;
+  if (e >= -24) return 1u << (e + 24);
+  return 0u;
+}
+
+__device__ __forceinline__ uint32_t max_byte(uint32_t w) {
+  w = __vmaxu4(w, w >> 16);
+  w = __vmaxu4(w, w >> 8);
+  return w & 0xFFu;
+}
+// bytes equal to 0xFF (NaN scales) do not take part in the reference maximum
+__device__ __forceinline__ uint32_t drop_nan_bytes(uint32_t w) {
+  return w & ~__vcmpeq4(w, 0xFFFFFFFFu);
+}
+
+__global__ void __launch_bounds__(kDecThreads, 2)
 decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __restrict__ k_pages,
                     const uint8_t* __restrict__ v_pages, int64_t kv_page_stride,
                     int64_t num_pages, const int32_t* __restrict__ block_table, int64_t bt_width,
                     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ topk,
-                    int kw, float scale_log2, int S, float* __restrict__ ws_o,
+                    int kw, float scale, int S, float* __restrict__ ws_o,
                     float* __restrict__ ws_ml, uint32_t* status) {
-  __shared__ __align__(16) uint8_t sK[kSplitTokens][kRowDataBytes];
-  __shared__ __align__(16) uint8_t sV[kSplitTokens][kRowDataBytes];
-  __shared__ uint32_t sKs[kSplitTokens], sVs[kSplitTokens];
-  __shared__ int64_t s_off[kSplitTokens];  // page byte offset, or -1 to skip
-  __shared__ int s_row[kSplitTokens];
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  DecodeSmem& s = *reinterpret_cast<DecodeSmem*>(smem_raw);
 
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, tig = lane & 3;
   const int64_t t = blockIdx.x / S;
   const int sp = blockIdx.x % S;
   const int64_t seq = t / Q;
@@ -47,91 +154,322 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   const int begin = sp * kSplitTokens;
   const int cnt = max(0, min(kSplitTokens, kw - begin));
 
-  // phase 1: indices -> page rows
-  for (int r = tid; r < cnt; r += kDecThreads) {
-    const int32_t i = topk[t * kw + begin + r];
+  // ---- 1. entries -> page rows, scale words, split references.  Thread tid owns
+  // the entry pair (2 tid, 2 tid + 1).
+  uint32_t kmax = 0, vmax4 = 0;
+  uint32_t ksw[2], vsw[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = 2 * tid + e;
     int64_t off = -1;
-    if (i >= 0) {
-      if (i > p || (int64_t)i / kPageTokens >= bt_width) {
-        flag(status, MX4_STATUS_BAD_INDEX);
-      } else {
-        const int32_t pid = block_table[seq * bt_width + i / kPageTokens];
-        if (pid < 0 || pid >= num_pages) flag(status, MX4_STATUS_BAD_PAGE);
-        else off = (int64_t)pid * kv_page_stride;
+    ksw[e] = vsw[e] = 0;
+    if (r < cnt) {
+      const int32_t i = topk[t * kw + begin + r];
+      if (i >= 0) {
+        if (i > p || (int64_t)i / kPageTokens >= bt_width) {
+          flag(status, MX4_STATUS_BAD_INDEX);
+        } else {
+          const int32_t pid = block_table[seq * bt_width + i / kPageTokens];
+          if (pid < 0 || pid >= num_pages) {
+            flag(status, MX4_STATUS_BAD_PAGE);
+          } else {
+            const int64_t pg = (int64_t)pid * kv_page_stride;
+            const int row = i % kPageTokens;
+            off = pg + row * kRowDataBytes;
+            ksw[e] = *reinterpret_cast<const uint32_t*>(k_pages + pg + kScaleOffset + row * 4);
+            vsw[e] = *reinterpret_cast<const uint32_t*>(v_pages + pg + kScaleOffset + row * 4);
+            kmax = max(kmax, max_byte(drop_nan_bytes(ksw[e])));
+            vmax4 = __vmaxu4(vmax4, drop_nan_bytes(vsw[e]));
+          }
+        }
       }
     }
-    s_off[r] = off;
-    s_row[r] = (i >= 0) ? (i % kPageTokens) : 0;
+    s.off[r] = off;
+    s.ok[r] = off >= 0;
+  }
+  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) vmax4 = __vmaxu4(vmax4, __shfl_xor_sync(0xFFFFFFFFu, vmax4, o));
+  if (lane == 0) {
+    s.red_k[warp] = kmax;
+    s.red_v[warp] = vmax4;
   }
   __syncthreads();
-
-  // phase 2: gather the rows (4 x 16 B of data per row and tensor, 4 B of scales)
-  for (int e = tid; e < cnt * 4; e += kDecThreads) {
-    const int r = e >> 2, part = e & 3;
-    const int64_t off = s_off[r];
-    if (off < 0) continue;
-    const int64_t base = off + s_row[r] * kRowDataBytes + part * 16;
-    *reinterpret_cast<uint4*>(&sK[r][part * 16]) = *reinterpret_cast<const uint4*>(k_pages + base);
-    *reinterpret_cast<uint4*>(&sV[r][part * 16]) = *reinterpret_cast<const uint4*>(v_pages + base);
+  uint32_t refK = 0, refV4 = 0;
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) {
+    refK = max(refK, s.red_k[w]);
+    refV4 = __vmaxu4(refV4, s.red_v[w]);
   }
-  for (int r = tid; r < cnt; r += kDecThreads) {
-    const int64_t off = s_off[r];
-    if (off < 0) continue;
-    const int64_t so = off + kScaleOffset + s_row[r] * kRowScaleBytes;
-    sKs[r] = *reinterpret_cast<const uint32_t*>(k_pages + so);
-    sVs[r] = *reinterpret_cast<const uint32_t*>(v_pages + so);
+  // multipliers (0 for invalid entries; their logits are masked below)
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = 2 * tid + e;
+    const bool ok = s.ok[r];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t m = ok ? f16_pow2((ksw[e] >> (8 * b)) & 0xFFu, refK) : 0u;
+      s.kmul[r][b] = m | (m << 16);
+    }
   }
-  __syncthreads();
-
-  // phase 3: online softmax over the split
-  const int h = tid >> 3, part = tid & 7;
-  float qv[16], o[16];
   {
-    const uint16_t* qh = q + (t * kHeads + h) * kHeadDim + part * 16;
+    const bool ok0 = s.ok[2 * tid], ok1 = s.ok[2 * tid + 1];
 #pragma unroll
-    for (int d = 0; d < 16; ++d) {
-      qv[d] = bf16_bits_to_float(qh[d]) * scale_log2;
-      o[d] = 0.f;
+    for (int slot = 0; slot < 4; ++slot) {
+      const int b = (slot >> 1) + 2 * (slot & 1);  // slot order 0, 2, 1, 3
+      const uint32_t ref = (refV4 >> (8 * b)) & 0xFFu;
+      const uint32_t m0 = ok0 ? f16_pow2((vsw[0] >> (8 * b)) & 0xFFu, ref) : 0u;
+      const uint32_t m1 = ok1 ? f16_pow2((vsw[1] >> (8 * b)) & 0xFFu, ref) : 0u;
+      s.vmul[tid][slot] = m0 | (m1 << 16);
     }
   }
-  float m = -INFINITY, l = 0.f;
-  const int blk = part >> 1;  // scale block of dims 16*part .. 16*part+15
-  for (int r = 0; r < cnt; ++r) {
-    if (s_off[r] < 0) continue;
-    const uint2 kd = *reinterpret_cast<const uint2*>(&sK[r][part * 8]);
-    const float ks = e8m0_to_float((sKs[r] >> (8 * blk)) & 0xFFu);
-    float dot = 0.f;
+  __syncthreads();
+
+  // ---- Q as f16 A fragments, scaled by 2^sigma so that bf16 fits f16 exactly
+  uint32_t qa[8][4];
+  int sigma;
+  {
+    float qf[2][4][8];
+    uint32_t amax = 0;
 #pragma unroll
-    for (int d = 0; d < 16; ++d) {
-      const uint32_t w = d < 8 ? kd.x : kd.y;
-      dot = fmaf(qv[d], e2m1_to_float(w >> (4 * (d & 7))), dot);
-    }
-    dot *= ks;  // this thread's 16 dims share one scale block
-    dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 1);
-    dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 2);
-    dot += __shfl_xor_sync(0xFFFFFFFFu, dot, 4);
-    const float logit = dot;  // log2 units
-    const float m_new = fmaxf(m, logit);
-    const float corr = exp2f(m - m_new);
-    const float pw = exp2f(logit - m_new);
-    l = l * corr + pw;
-    m = m_new;
-    const uint2 vd = *reinterpret_cast<const uint2*>(&sV[r][part * 8]);
-    const float vs = e8m0_to_float((sVs[r] >> (8 * blk)) & 0xFFu) * pw;
+    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-    for (int d = 0; d < 16; ++d) {
-      const uint32_t w = d < 8 ? vd.x : vd.y;
-      o[d] = fmaf(e2m1_to_float(w >> (4 * (d & 7))), vs, o[d] * corr);
-    }
+      for (int b = 0; b < 4; ++b) {
+        const uint4 v = *reinterpret_cast<const uint4*>(
+            q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          qf[hh][b][2 * j] = __uint_as_float(w[j] << 16);
+          qf[hh][b][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
+          amax = max(amax, (w[j] << 17) >> 1);          // |low bf16| as fp32 bits
+          amax = max(amax, (w[j] & 0x7FFF0000u));       // |high bf16|
+        }
+      }
+    amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+    const int e = (int)(amax >> 23) - 127;
+    sigma = (amax == 0u) ? 0 : min(127, max(-126, 14 - e));
+    const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        // slice 2b+h: k = 2tig,2tig+1 <-> dims 32b+8tig+4h+{0,1}; k = 2tig+8,+9 <-> +{2,3}
+        qa[2 * b + h][0] = pack_f16x2(qf[0][b][4 * h] * sc, qf[0][b][4 * h + 1] * sc);
+        qa[2 * b + h][1] = pack_f16x2(qf[1][b][4 * h] * sc, qf[1][b][4 * h + 1] * sc);
+        qa[2 * b + h][2] = pack_f16x2(qf[0][b][4 * h + 2] * sc, qf[0][b][4 * h + 3] * sc);
+        qa[2 * b + h][3] = pack_f16x2(qf[1][b][4 * h + 2] * sc, qf[1][b][4 * h + 3] * sc);
+      }
   }
-  const int64_t slot = (t * S + sp) * kHeads + h;
-  float* wo = ws_o + slot * kHeadDim + part * 16;
+  // logit (log2 units) = S * cK
+  const float cK = ldexpf(scale * kLog2e, (int)refK - 127 - sigma);
+
+  // ---- 2/3. this warp's tiles through the cp.async ring
+  const int n_tiles = (cnt + kTile - 1) / kTile;
+  const int n_my = n_tiles > warp ? (n_tiles - warp + kDecWarps - 1) / kDecWarps : 0;
+  const uint32_t stage0 = smem_u32(&s.stage[warp][0][0]);
+
+  auto issue = [&](int u) {
+    const int tb = (warp + kDecWarps * u) * kTile;
+    const int e = lane >> 1, half = lane & 1;
+    const int r = tb + e;
+    const int64_t off = (r < cnt) ? s.off[r] : -1;
+    const bool ok = off >= 0;
+    const uint32_t dst = stage0 + (u % kStages) * kStageBytes + e * kRowPitch + half * 32;
+    const uint8_t* ks = k_pages + (ok ? off : 0) + half * 32;
+    const uint8_t* vs = v_pages + (ok ? off : 0) + half * 32;
+    cp_async16(dst, ks, ok);
+    cp_async16(dst + 16, ks + 16, ok);
+    cp_async16(dst + kTile * kRowPitch, vs, ok);
+    cp_async16(dst + kTile * kRowPitch + 16, vs + 16, ok);
+  };
+
+  float o[16][4];
 #pragma unroll
-  for (int d = 0; d < 16; d += 4)
-    *reinterpret_cast<float4*>(wo + d) = make_float4(o[d], o[d + 1], o[d + 2], o[d + 3]);
-  if (part == 0) {
-    ws_ml[slot * 2 + 0] = m;
-    ws_ml[slot * 2 + 1] = l;
+  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+  float m_used[2] = {-INFINITY, -INFINITY};
+  float lsum[2] = {0.f, 0.f};
+
+#pragma unroll
+  for (int u = 0; u < kStages - 1; ++u) {
+    if (u < n_my) issue(u);
+    cp_async_commit();
+  }
+  for (int u = 0; u < n_my; ++u) {
+    if (u + kStages - 1 < n_my) issue(u + kStages - 1);
+    cp_async_commit();
+    cp_async_wait<kStages - 1>();
+    __syncwarp();
+    const uint8_t* sk = &s.stage[warp][u % kStages][0];
+    const uint8_t* sv = sk + kTile * kRowPitch;
+    const int tb = (warp + kDecWarps * u) * kTile;
+
+    // S = Q K^T for tokens tb .. tb+15 (two n8 tiles)
+    float c[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+      const uint8_t* row = sk + (nt * 8 + g) * kRowPitch;
+      const uint4 km = *reinterpret_cast<const uint4*>(&s.kmul[tb + nt * 8 + g][0]);
+      const uint32_t kmb[4] = {km.x, km.y, km.z, km.w};
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        uint32_t f[4];
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(row + (4 * b + tig) * 4), f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) f[j] = hmul2(f[j], kmb[b]);
+        mma_f16(c[nt], qa[2 * b][0], qa[2 * b][1], qa[2 * b][2], qa[2 * b][3], f[0], f[1]);
+        mma_f16(c[nt], qa[2 * b + 1][0], qa[2 * b + 1][1], qa[2 * b + 1][2], qa[2 * b + 1][3],
+                f[2], f[3]);
+      }
+    }
+    // logits, masked entries -> -inf
+    const uint16_t ok01 = *reinterpret_cast<const uint16_t*>(&s.ok[tb + 2 * tig]);
+    const uint16_t ok89 = *reinterpret_cast<const uint16_t*>(&s.ok[tb + 8 + 2 * tig]);
+    float lg[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint16_t okw = nt ? ok89 : ok01;
+      lg[nt][0] = (okw & 0x00FF) ? c[nt][0] * cK : -INFINITY;
+      lg[nt][1] = (okw & 0xFF00) ? c[nt][1] * cK : -INFINITY;
+      lg[nt][2] = (okw & 0x00FF) ? c[nt][2] * cK : -INFINITY;
+      lg[nt][3] = (okw & 0xFF00) ? c[nt][3] * cK : -INFINITY;
+    }
+    float mx[2];
+    mx[0] = fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1]));
+    mx[1] = fmaxf(fmaxf(lg[0][2], lg[0][3]), fmaxf(lg[1][2], lg[1][3]));
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xFFFFFFFFu, mx[rr], 1));
+      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xFFFFFFFFu, mx[rr], 2));
+    }
+    const bool need = mx[0] > m_used[0] + kLazy || mx[1] > m_used[1] + kLazy;
+    if (__any_sync(0xFFFFFFFFu, need)) {
+      float corr[2];
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const float nm = mx[rr] > m_used[rr] + kLazy ? mx[rr] : m_used[rr];
+        corr[rr] = (nm == m_used[rr]) ? 1.f : exp2f(m_used[rr] - nm);
+        m_used[rr] = nm;
+        lsum[rr] *= corr[rr];
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        o[j][0] *= corr[0];
+        o[j][1] *= corr[0];
+        o[j][2] *= corr[1];
+        o[j][3] *= corr[1];
+      }
+    }
+    const float mb0 = (m_used[0] == -INFINITY) ? 0.f : m_used[0] - kPOffset;
+    const float mb1 = (m_used[1] == -INFINITY) ? 0.f : m_used[1] - kPOffset;
+    float pw[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      pw[nt][0] = exp2f(lg[nt][0] - mb0);
+      pw[nt][1] = exp2f(lg[nt][1] - mb0);
+      pw[nt][2] = exp2f(lg[nt][2] - mb1);
+      pw[nt][3] = exp2f(lg[nt][3] - mb1);
+    }
+    lsum[0] += (pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]);
+    lsum[1] += (pw[0][2] + pw[0][3]) + (pw[1][2] + pw[1][3]);
+    // P = hi + lo, both f16
+    uint32_t ph[4], pl[4];
+    ph[0] = pack_f16x2(pw[0][0], pw[0][1]);
+    ph[1] = pack_f16x2(pw[0][2], pw[0][3]);
+    ph[2] = pack_f16x2(pw[1][0], pw[1][1]);
+    ph[3] = pack_f16x2(pw[1][2], pw[1][3]);
+    pl[0] = pack_f16x2(pw[0][0] - f16_lo(ph[0]), pw[0][1] - f16_hi(ph[0]));
+    pl[1] = pack_f16x2(pw[0][2] - f16_lo(ph[1]), pw[0][3] - f16_hi(ph[1]));
+    pl[2] = pack_f16x2(pw[1][0] - f16_lo(ph[2]), pw[1][1] - f16_hi(ph[2]));
+    pl[3] = pack_f16x2(pw[1][2] - f16_lo(ph[3]), pw[1][3] - f16_hi(ph[3]));
+
+    // O += P V: dim tile j = 8h + i, column g <-> dim 8(g + 8h) + i
+    const uint2 vm01 = *reinterpret_cast<const uint2*>(&s.vmul[(tb >> 1) + tig][(g >> 2) * 2]);
+    const uint2 vm89 =
+        *reinterpret_cast<const uint2*>(&s.vmul[(tb >> 1) + 4 + tig][(g >> 2) * 2]);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int wi = (g + 8 * h) * 4;
+      const uint32_t wA = *reinterpret_cast<const uint32_t*>(sv + (2 * tig) * kRowPitch + wi);
+      const uint32_t wB = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 1) * kRowPitch + wi);
+      const uint32_t wC = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 8) * kRowPitch + wi);
+      const uint32_t wD = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 9) * kRowPitch + wi);
+      // nibble zip: byte q of ze = (A.dim 2q) | (B.dim 2q) << 4; zo likewise for 2q+1
+      uint32_t ze01[4], zo01[4], ze89[4], zo89[4];
+      e2m1x8_to_f16x2(lop_merge(wA, wB << 4, 0x0F0F0F0Fu), ze01);
+      e2m1x8_to_f16x2(lop_merge(wA >> 4, wB, 0x0F0F0F0Fu), zo01);
+      e2m1x8_to_f16x2(lop_merge(wC, wD << 4, 0x0F0F0F0Fu), ze89);
+      e2m1x8_to_f16x2(lop_merge(wC >> 4, wD, 0x0F0F0F0Fu), zo89);
+      const uint32_t m01 = h ? vm01.y : vm01.x;
+      const uint32_t m89 = h ? vm89.y : vm89.x;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const uint32_t b0 = hmul2((i & 1) ? zo01[i >> 1] : ze01[i >> 1], m01);
+        const uint32_t b1 = hmul2((i & 1) ? zo89[i >> 1] : ze89[i >> 1], m89);
+        mma_f16(o[8 * h + i], ph[0], ph[1], ph[2], ph[3], b0, b1);
+        mma_f16(o[8 * h + i], pl[0], pl[1], pl[2], pl[3], b0, b1);
+      }
+    }
+    __syncwarp();
+  }
+  cp_async_wait<0>();
+
+  // ---- 4. merge the warps' partial results in shared memory
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr) {
+    lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 1);
+    lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 2);
+  }
+  __syncthreads();  // every warp is done with its ring
+  if (tig == 0) {
+    s.red_m[warp][g] = m_used[0];
+    s.red_m[warp][g + 8] = m_used[1];
+    s.red_l[warp][g] = lsum[0];
+    s.red_l[warp][g + 8] = lsum[1];
+  }
+  __syncthreads();
+  float M[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) {
+    M[0] = fmaxf(M[0], s.red_m[w][g]);
+    M[1] = fmaxf(M[1], s.red_m[w][g + 8]);
+  }
+  float fw[2];
+#pragma unroll
+  for (int rr = 0; rr < 2; ++rr)
+    fw[rr] = (m_used[rr] == -INFINITY) ? 0.f : exp2f(m_used[rr] - M[rr]);
+  float* red_o = reinterpret_cast<float*>(&s.stage[0][0][0]);  // [warp][head][dim]
+  float fv[4];
+#pragma unroll
+  for (int b = 0; b < 4; ++b) fv[b] = ldexpf(1.f, (int)((refV4 >> (8 * b)) & 0xFFu) - 127);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const int h = j >> 3, i = j & 7;
+    const int d0 = 8 * (2 * tig + 8 * h) + i, d1 = d0 + 8;
+    const float f = fv[(2 * tig + 8 * h) >> 2];
+    red_o[(warp * kHeads + g) * kHeadDim + d0] = o[j][0] * fw[0] * f;
+    red_o[(warp * kHeads + g) * kHeadDim + d1] = o[j][1] * fw[0] * f;
+    red_o[(warp * kHeads + g + 8) * kHeadDim + d0] = o[j][2] * fw[1] * f;
+    red_o[(warp * kHeads + g + 8) * kHeadDim + d1] = o[j][3] * fw[1] * f;
+  }
+  __syncthreads();
+  const int64_t slot0 = (t * S + sp) * kHeads;
+  for (int e = tid; e < kHeads * kHeadDim; e += kDecThreads) {
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) acc += red_o[w * kHeads * kHeadDim + e];
+    ws_o[slot0 * kHeadDim + e] = acc;
+  }
+  if (tid < kHeads) {
+    float Mh = -INFINITY;
+    for (int w = 0; w < kDecWarps; ++w) Mh = fmaxf(Mh, s.red_m[w][tid]);
+    float l = 0.f;
+    if (Mh != -INFINITY)
+      for (int w = 0; w < kDecWarps; ++w)
+        if (s.red_m[w][tid] != -INFINITY) l += s.red_l[w][tid] * exp2f(s.red_m[w][tid] - Mh);
+    ws_ml[(slot0 + tid) * 2 + 0] = Mh;
+    ws_ml[(slot0 + tid) * 2 + 1] = l;
   }
 }
 
@@ -174,10 +512,14 @@ cudaError_t launch_decode(const uint16_t* q, int64_t T, int Q, const uint8_t* k_
   const int S = decode_splits(kw);
   float* ws_o = static_cast<float*>(ws);
   float* ws_ml = ws_o + T * S * kHeads * kHeadDim;
-  decode_split_kernel<<<(unsigned)(T * S), kDecThreads, 0, stream>>>(
+  const int smem = (int)sizeof(DecodeSmem);
+  cudaError_t err =
+      cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  decode_split_kernel<<<(unsigned)(T * S), kDecThreads, smem, stream>>>(
       q, Q, k_pages, v_pages, kv_page_stride, num_pages, block_table, bt_width, seq_lens, topk, kw,
-      scale * kLog2e, S, ws_o, ws_ml, status);
-  cudaError_t err = cudaGetLastError();
+      scale, S, ws_o, ws_ml, status);
+  err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   decode_merge_kernel<<<(unsigned)T, kHeadDim, 0, stream>>>(ws_o, ws_ml, S, out);
   return cudaGetLastError();

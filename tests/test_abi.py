@@ -92,7 +92,7 @@ def test_host_validation_without_gpu(lib):
 
 def test_workspace_sizes(lib):
     import mxfp4_sparse_paged_gb300 as m
-    # 16 heads x (128 outputs + max + sum) fp32 per (token, split of 256 selected)
-    assert m.sparse_paged_decode_workspace(64, 2048) == 64 * 8 * 16 * 130 * 4
+    # 16 heads x (128 outputs + max + sum) fp32 per (token, split of 512 selected)
+    assert m.sparse_paged_decode_workspace(64, 2048) == 64 * 4 * 16 * 130 * 4
     assert m.sparse_paged_decode_workspace(1, 1) == 16 * 130 * 4
     assert m.topk_select_workspace(64, 2048, 131072) >= 0
