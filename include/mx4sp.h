@@ -61,6 +61,7 @@ typedef enum {
 #define MX4_STATUS_BAD_LEN 0x4u    /* seq_len < q, or beyond the block table / ld */
 #define MX4_STATUS_BAD_INDEX 0x8u  /* top-k index outside [0, position] */
 #define MX4_STATUS_BAD_VALUE 0x10u /* non-finite fp32 input to mx4_insert */
+#define MX4_STATUS_TIMEOUT 0x20u   /* a kernel gave up a bounded wait (should not happen) */
 
 #define MX4_PAGE_TOKENS 128
 #define MX4_HEAD_DIM 128

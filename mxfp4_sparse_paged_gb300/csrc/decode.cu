@@ -21,7 +21,8 @@
 //   3. Per tile: e2m1 -> f16 with the hardware cvt (exact grid values), times the
 //      multiplier; S = Q K^T with mma.sync m16n8k16 (Q = 16 heads x 128, f16,
 //      scaled by a power of two so bf16 fits f16 exactly); online softmax in
-//      fp32 (log2 units, lazy rescaling); P split into f16 hi + lo parts so
+//      fp32 (log2 units, lazy rescaling; weights scaled by 2^7 so the f16 P
+//      stays normal); P split into f16 hi + lo parts so
 //      P V keeps ~22 bits; O += P V with mma.sync, V fragments built by zipping
 //      the nibbles of two tokens so one cvt yields a (token, token) pair.
 //   4. The 8 warps' (max, sum, O) are merged in shared memory and the split
@@ -43,7 +44,7 @@ constexpr int kStages = 4;                          // cp.async ring depth per w
 constexpr int kRowPitch = 80;                       // staged row pitch (64 B + 16 B pad)
 constexpr int kStageBytes = 2 * kTile * kRowPitch;  // K rows then V rows: 2560 B
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kPOffset = 7.f;  // p' = 2^(logit - m + 7)
+constexpr float kPScale = 128.f;  // p' = 2^(logit - m) * 2^7, at most 2^15 in f16
 constexpr float kLazy = 8.f;     // rescale only when the max grows by more than this
 static_assert(kTilesPerWarp * kTile * kDecWarps == kSplitTokens, "split geometry");
 static_assert(2 * kDecThreads == kSplitTokens, "one entry pair per thread in the set-up phase");
@@ -62,10 +63,6 @@ struct DecodeSmem {
   uint32_t red_v[kDecWarps];
 };
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0));
@@ -76,15 +73,6 @@ __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
 }
 
-// The four bytes of w, each e2m1x2 -> f16x2 (low nibble -> low half), exact.
-__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t (&r)[4]) {
-  asm("{\n .reg .b8 b0, b1, b2, b3;\n mov.b32 {b0, b1, b2, b3}, %4;\n"
-      " cvt.rn.f16x2.e2m1x2 %0, b0;\n cvt.rn.f16x2.e2m1x2 %1, b1;\n"
-      " cvt.rn.f16x2.e2m1x2 %2, b2;\n cvt.rn.f16x2.e2m1x2 %3, b3;\n}"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-      : "r"(w));
-}
-
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
   asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(d) : "r"(a), "r"(b));
@@ -93,15 +81,6 @@ __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
 
 __device__ __forceinline__ uint32_t lop_merge(uint32_t a, uint32_t b, uint32_t m) {
   return (a & m) | (b & ~m);
-}
-
-__device__ __forceinline__ void mma_f16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                        uint32_t a3, uint32_t b0, uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%0,%1,%2,%3};\n"
-      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
@@ -267,7 +246,7 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   // ---- 2/3. this warp's tiles through the cp.async ring
   const int n_tiles = (cnt + kTile - 1) / kTile;
   const int n_my = n_tiles > warp ? (n_tiles - warp + kDecWarps - 1) / kDecWarps : 0;
-  const uint32_t stage0 = smem_u32(&s.stage[warp][0][0]);
+  const uint32_t stage0 = smem_addr(&s.stage[warp][0][0]);
 
   auto issue = [&](int u) {
     const int tb = (warp + kDecWarps * u) * kTile;
@@ -318,8 +297,8 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
         e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(row + (4 * b + tig) * 4), f);
 #pragma unroll
         for (int j = 0; j < 4; ++j) f[j] = hmul2(f[j], kmb[b]);
-        mma_f16(c[nt], qa[2 * b][0], qa[2 * b][1], qa[2 * b][2], qa[2 * b][3], f[0], f[1]);
-        mma_f16(c[nt], qa[2 * b + 1][0], qa[2 * b + 1][1], qa[2 * b + 1][2], qa[2 * b + 1][3],
+        mma_m16n8k16_f16(c[nt], qa[2 * b][0], qa[2 * b][1], qa[2 * b][2], qa[2 * b][3], f[0], f[1]);
+        mma_m16n8k16_f16(c[nt], qa[2 * b + 1][0], qa[2 * b + 1][1], qa[2 * b + 1][2], qa[2 * b + 1][3],
                 f[2], f[3]);
       }
     }
@@ -361,15 +340,16 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
         o[j][3] *= corr[1];
       }
     }
-    const float mb0 = (m_used[0] == -INFINITY) ? 0.f : m_used[0] - kPOffset;
-    const float mb1 = (m_used[1] == -INFINITY) ? 0.f : m_used[1] - kPOffset;
+    // p' = 2^(logit - m) * 2^7: the largest logit gets exactly 128
+    const float mb0 = (m_used[0] == -INFINITY) ? 0.f : m_used[0];
+    const float mb1 = (m_used[1] == -INFINITY) ? 0.f : m_used[1];
     float pw[2][4];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      pw[nt][0] = exp2f(lg[nt][0] - mb0);
-      pw[nt][1] = exp2f(lg[nt][1] - mb0);
-      pw[nt][2] = exp2f(lg[nt][2] - mb1);
-      pw[nt][3] = exp2f(lg[nt][3] - mb1);
+      pw[nt][0] = exp2f(lg[nt][0] - mb0) * kPScale;
+      pw[nt][1] = exp2f(lg[nt][1] - mb0) * kPScale;
+      pw[nt][2] = exp2f(lg[nt][2] - mb1) * kPScale;
+      pw[nt][3] = exp2f(lg[nt][3] - mb1) * kPScale;
     }
     lsum[0] += (pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]);
     lsum[1] += (pw[0][2] + pw[0][3]) + (pw[1][2] + pw[1][3]);
@@ -407,8 +387,8 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
       for (int i = 0; i < 8; ++i) {
         const uint32_t b0 = hmul2((i & 1) ? zo01[i >> 1] : ze01[i >> 1], m01);
         const uint32_t b1 = hmul2((i & 1) ? zo89[i >> 1] : ze89[i >> 1], m89);
-        mma_f16(o[8 * h + i], ph[0], ph[1], ph[2], ph[3], b0, b1);
-        mma_f16(o[8 * h + i], pl[0], pl[1], pl[2], pl[3], b0, b1);
+        mma_m16n8k16_f16(o[8 * h + i], ph[0], ph[1], ph[2], ph[3], b0, b1);
+        mma_m16n8k16_f16(o[8 * h + i], pl[0], pl[1], pl[2], pl[3], b0, b1);
       }
     }
     __syncwarp();
@@ -473,26 +453,40 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   }
 }
 
-__global__ void __launch_bounds__(kHeadDim)
+// One CTA per decode token; thread (h, part) merges dims 8*part .. 8*part+7 of
+// head h over the splits: out = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
+constexpr int kMergeThreads = kHeads * (kHeadDim / 8);
+__global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int S,
                     float* __restrict__ out) {
   const int64_t t = blockIdx.x;
-  const int d = threadIdx.x;
-  for (int h = 0; h < kHeads; ++h) {
-    float m = -INFINITY;
-    for (int sp = 0; sp < S; ++sp) m = fmaxf(m, ws_ml[((t * S + sp) * kHeads + h) * 2]);
-    float l = 0.f, acc = 0.f;
-    if (m != -INFINITY) {
-      for (int sp = 0; sp < S; ++sp) {
-        const int64_t slot = (t * S + sp) * kHeads + h;
-        const float ms = ws_ml[slot * 2];
-        if (ms == -INFINITY) continue;
-        const float w = exp2f(ms - m);
-        l = fmaf(ws_ml[slot * 2 + 1], w, l);
-        acc = fmaf(ws_o[slot * kHeadDim + d], w, acc);
-      }
+  const int h = threadIdx.x / (kHeadDim / 8), d0 = (threadIdx.x % (kHeadDim / 8)) * 8;
+  float M = -INFINITY;
+  for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ws_ml[((t * S + sp) * kHeads + h) * 2]);
+  float l = 0.f;
+  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+  if (M != -INFINITY) {
+    for (int sp = 0; sp < S; ++sp) {
+      const int64_t slot = (t * S + sp) * kHeads + h;
+      const float ms = ws_ml[slot * 2];
+      if (ms == -INFINITY) continue;
+      const float w = exp2f(ms - M);
+      l = fmaf(ws_ml[slot * 2 + 1], w, l);
+      const float4 x0 = *reinterpret_cast<const float4*>(ws_o + slot * kHeadDim + d0);
+      const float4 x1 = *reinterpret_cast<const float4*>(ws_o + slot * kHeadDim + d0 + 4);
+      a0.x = fmaf(x0.x, w, a0.x); a0.y = fmaf(x0.y, w, a0.y);
+      a0.z = fmaf(x0.z, w, a0.z); a0.w = fmaf(x0.w, w, a0.w);
+      a1.x = fmaf(x1.x, w, a1.x); a1.y = fmaf(x1.y, w, a1.y);
+      a1.z = fmaf(x1.z, w, a1.z); a1.w = fmaf(x1.w, w, a1.w);
     }
-    out[(t * kHeads + h) * kHeadDim + d] = (l > 0.f) ? acc / l : 0.f;
+  }
+  float* o = out + (t * kHeads + h) * kHeadDim + d0;
+  if (l > 0.f) {
+    *reinterpret_cast<float4*>(o) = make_float4(a0.x / l, a0.y / l, a0.z / l, a0.w / l);
+    *reinterpret_cast<float4*>(o + 4) = make_float4(a1.x / l, a1.y / l, a1.z / l, a1.w / l);
+  } else {
+    *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
+    *reinterpret_cast<float4*>(o + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
@@ -521,7 +515,7 @@ cudaError_t launch_decode(const uint16_t* q, int64_t T, int Q, const uint8_t* k_
       scale, S, ws_o, ws_ml, status);
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  decode_merge_kernel<<<(unsigned)T, kHeadDim, 0, stream>>>(ws_o, ws_ml, S, out);
+  decode_merge_kernel<<<(unsigned)T, kMergeThreads, 0, stream>>>(ws_o, ws_ml, S, out);
   return cudaGetLastError();
 }
 

@@ -6,43 +6,53 @@
 // the index scorers read); pages are found through the block table shared with
 // the K/V cache ("vllm.models.minimax_m3.amd.mono.dispatch", _slots_shared).
 //
-// Work decomposition: a work item is (sequence, chunk of kChunkPages pages).
-// Persistent CTAs walk the items round-robin; the item -> sequence map is a
-// block-wide prefix sum over seq_lens, recomputed by each CTA tile by tile,
-// so the call needs no workspace and no host knowledge of the lengths.  All q
-// decode tokens of a sequence are scored in the same pass over its pages.
+// Work: the pages of all sequences, flattened in order, are cut into equal
+// contiguous ranges, one per CTA (a block-wide prefix sum over seq_lens in
+// shared memory maps a flat page number to (sequence, page)).  All q decode
+// tokens of a sequence are scored in one pass over its pages.
 //
-// Inside an item a warp reads 8 token rows per step: lane l takes row l/4 and
-// block b = l%4 (16 data bytes = 32 elements as one 16-B load, plus that
-// block's scale byte).  The 32-element partial dot is scaled by 2^(scale-127)
-// and the four blocks of a row are summed with two xor-shuffles.
+// Pipeline: warp 4 is the producer.  It resolves pages through the block table
+// (32 lanes at a time) and streams each 8704-byte page, plus the sequence's
+// index-q rows, into a 5-stage shared-memory ring with bulk copies (TMA engine)
+// that complete on the stage's "full" mbarrier.  Warps 0-3 consume: each takes
+// two 16-row tiles of the page.
+//
+// Math (per tile, tensor cores): A = 16 index-key rows x 128 dims, decoded by
+// the hardware e2m1 -> f16 conversion (exact); thread t of a quad owns the 32
+// dims of scale block t.  B = index-q, bf16 scaled by a power of two into f16
+// (exact), laid out so that output column n = 4*query + block: a column only
+// sees the dims of its own block, so C holds per-block partial dots.  The
+// scores are then sum_b C[row][4q+b] * 2^(scale_b - 127) in fp32 (exact
+// scaling), combined across the quad with one shuffle.
 #include "common.cuh"
 
 namespace mx4 {
 
-constexpr int kScoreThreads = 256;
-constexpr int kChunkPages = 2;
+constexpr int kScoreConsumers = 4;
+constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;
+constexpr int kScoreStages = 5;
+constexpr int kMaxQ = 8;
+constexpr int kStageIqBytes = kMaxQ * kHeadDim * 2;
+constexpr int kScoreStageBytes = kPageBytes + kStageIqBytes;  // 10752, a multiple of 16
+constexpr int kScoreMaxBatch = 2048;                           // sequences per launch
+static_assert(kScoreStageBytes % 16 == 0, "bulk-copy alignment");
 
-template <int Q>
-__device__ __forceinline__ void score_rows(const uint8_t* __restrict__ page, int row, int b,
-                                           const float* __restrict__ s_iq, float (&acc)[Q]) {
-  const uint4 d = *reinterpret_cast<const uint4*>(page + row * kRowDataBytes + b * 16);
-  const float sc = e8m0_to_float(page[kScaleOffset + row * kRowScaleBytes + b]);
-  const uint32_t w[4] = {d.x, d.y, d.z, d.w};
-#pragma unroll
-  for (int qq = 0; qq < Q; ++qq) acc[qq] = 0.f;
-#pragma unroll
-  for (int wi = 0; wi < 4; ++wi) {
-#pragma unroll
-    for (int n = 0; n < 8; ++n) {
-      const int j = wi * 8 + n;  // element 32b + j of the row
-      const float f = e2m1_to_float(w[wi] >> (4 * n));
-#pragma unroll
-      for (int qq = 0; qq < Q; ++qq) acc[qq] = fmaf(s_iq[qq * kHeadDim + j * 4 + b], f, acc[qq]);
-    }
-  }
-#pragma unroll
-  for (int qq = 0; qq < Q; ++qq) acc[qq] *= sc;
+struct ScoreSmem {
+  uint8_t stage[kScoreStages][kScoreStageBytes];
+  int pref[kScoreMaxBatch];  // inclusive prefix sum of pages per sequence
+  int info_seq[kScoreStages];
+  int info_page[kScoreStages];
+  int info_len[kScoreStages];
+  int info_ok[kScoreStages];
+  int warp_sum[kScoreThreads / 32];
+  unsigned long long full[kScoreStages];
+  unsigned long long empty[kScoreStages];
+  volatile int abort_flag;
+};
+
+__device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
+  const __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
 }
 
 template <int Q>
@@ -52,101 +62,215 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
                    const int32_t* __restrict__ block_table, int B, int64_t bt_width,
                    const int32_t* __restrict__ seq_lens, float* __restrict__ scores, int64_t ld,
                    uint32_t* status) {
-  __shared__ int s_pref[kScoreThreads];      // inclusive prefix of items in this tile
-  __shared__ float s_iq[Q * kHeadDim];       // [q][j][b]: element 32b+j at j*4+b
-  __shared__ int s_warp[kScoreThreads / 32];
-
+  constexpr int NT = (Q + 1) / 2;  // n8 tiles: 4 block-columns per query
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  ScoreSmem& s = *reinterpret_cast<ScoreSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int64_t grid = gridDim.x;
-  int64_t base_item = 0;
 
-  for (int tile = 0; tile < B; tile += kScoreThreads) {
-    // items of the sequences tile .. tile+255
-    const int s = tile + tid;
-    int n = 0;
-    if (s < B) {
-      const int64_t L = seq_lens[s];
+  // ---- pages per sequence and their prefix sum (contiguous segment per thread)
+  {
+    const int per = (B + kScoreThreads - 1) / kScoreThreads;
+    const int s0 = min(B, tid * per), s1 = min(B, s0 + per);
+    int sum = 0;
+    for (int sq = s0; sq < s1; ++sq) {
+      const int64_t L = seq_lens[sq];
       const bool ok = L >= Q && L <= bt_width * kPageTokens && L <= ld;
       if (!ok && blockIdx.x == 0) flag(status, MX4_STATUS_BAD_LEN);
-      const int64_t pages = (L + kPageTokens - 1) / kPageTokens;
-      n = ok ? (int)((pages + kChunkPages - 1) / kChunkPages) : 0;
+      sum += ok ? (int)((L + kPageTokens - 1) / kPageTokens) : 0;
     }
-    // block inclusive scan of n
-    int x = n;
+    int inc = sum;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xFFFFFFFFu, x, o);
-      if (lane >= o) x += y;
+      const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+      if (lane >= o) inc += y;
     }
-    if (lane == 31) s_warp[warp] = x;
+    if (lane == 31) s.warp_sum[warp] = inc;
     __syncthreads();
-    if (warp == 0) {
-      int w = lane < kScoreThreads / 32 ? s_warp[lane] : 0;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, w, o);
-        if (lane >= o) w += y;
-      }
-      if (lane < kScoreThreads / 32) s_warp[lane] = w;
+    int before = inc - sum;
+    for (int w = 0; w < warp; ++w) before += s.warp_sum[w];
+    for (int sq = s0; sq < s1; ++sq) {
+      const int64_t L = seq_lens[sq];
+      const bool ok = L >= Q && L <= bt_width * kPageTokens && L <= ld;
+      before += ok ? (int)((L + kPageTokens - 1) / kPageTokens) : 0;
+      s.pref[sq] = before;
     }
-    __syncthreads();
-    s_pref[tid] = x + (warp > 0 ? s_warp[warp - 1] : 0);
-    __syncthreads();
-    const int64_t total = s_pref[kScoreThreads - 1];
+  }
+  if (tid == 0) {
+    for (int i = 0; i < kScoreStages; ++i) {
+      mbar_init(smem_addr(&s.full[i]), 1);
+      mbar_init(smem_addr(&s.empty[i]), kScoreConsumers);
+    }
+    s.abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
 
-    // this CTA's items in [base_item, base_item + total)
-    int64_t it = base_item + (((int64_t)blockIdx.x - base_item) % grid + grid) % grid;
-    for (; it < base_item + total; it += grid) {
-      const int local = (int)(it - base_item);
-      int lo = 0, hi = kScoreThreads - 1;  // first index with s_pref > local
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (s_pref[mid] > local) hi = mid; else lo = mid + 1;
-      }
-      const int seq = tile + lo;
-      const int chunk = local - (lo > 0 ? s_pref[lo - 1] : 0);
-      const int64_t L = seq_lens[seq];
+  const int total = B > 0 ? s.pref[B - 1] : 0;
+  const int G = gridDim.x;
+  const int p0 = (int)((int64_t)total * blockIdx.x / G);
+  const int n = (int)((int64_t)total * (blockIdx.x + 1) / G) - p0;
 
-      __syncthreads();  // previous item's readers of s_iq are done
-      for (int e = tid; e < Q * kHeadDim; e += kScoreThreads) {
-        const int qq = e / kHeadDim, d = e % kHeadDim;
-        s_iq[qq * kHeadDim + (d % 32) * 4 + d / 32] =
-            bf16_bits_to_float(iq[((int64_t)seq * Q + qq) * kHeadDim + d]);
-      }
-      __syncthreads();
-
-      const int64_t npages = (L + kPageTokens - 1) / kPageTokens;
-      for (int cp = 0; cp < kChunkPages; ++cp) {
-        const int64_t pg = (int64_t)chunk * kChunkPages + cp;
-        if (pg >= npages) break;
-        const int32_t pid = block_table[(int64_t)seq * bt_width + pg];
-        if (pid < 0 || pid >= num_pages) {
-          if (tid == 0) flag(status, MX4_STATUS_BAD_PAGE);
-          continue;
+  if (warp == kScoreConsumers) {
+    // ================= producer
+    for (int base = 0; base < n; base += 32) {
+      if (__any_sync(0xFFFFFFFFu, s.abort_flag != 0)) break;
+      const int k = base + lane;
+      int seqk = 0, jk = 0, lenk = 0, okk = 0;
+      const uint8_t* src = idx_pages;
+      if (k < n) {
+        const int P = p0 + k;
+        int lo = 0, hi = B - 1;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (s.pref[mid] > P) hi = mid; else lo = mid + 1;
         }
-        const uint8_t* page = idx_pages + (int64_t)pid * idx_page_stride;
-        for (int r0 = warp * 8; r0 < kPageTokens; r0 += kScoreThreads / 4) {
-          const int row = r0 + (lane >> 2), b = lane & 3;
-          const int64_t i = pg * kPageTokens + row;
-          float acc[Q];
-          score_rows<Q>(page, row, b, s_iq, acc);
-#pragma unroll
-          for (int qq = 0; qq < Q; ++qq) {
-            acc[qq] += __shfl_xor_sync(0xFFFFFFFFu, acc[qq], 1);
-            acc[qq] += __shfl_xor_sync(0xFFFFFFFFu, acc[qq], 2);
+        seqk = lo;
+        jk = P - (lo > 0 ? s.pref[lo - 1] : 0);
+        lenk = seq_lens[seqk];
+        const int32_t pid = block_table[(int64_t)seqk * bt_width + jk];
+        okk = (pid >= 0 && pid < num_pages) ? 1 : 0;
+        if (!okk) flag(status, MX4_STATUS_BAD_PAGE);
+        else src = idx_pages + (int64_t)pid * idx_page_stride;
+      }
+      const int cnt = min(32, n - base);
+      for (int l = 0; l < cnt; ++l) {
+        if (lane == l) {
+          const int kk = base + l, st = kk % kScoreStages, round = kk / kScoreStages;
+          bool go = !s.abort_flag;
+          if (go && round > 0 && !mbar_wait(smem_addr(&s.empty[st]), (round - 1) & 1)) {
+            flag(status, MX4_STATUS_TIMEOUT);
+            s.abort_flag = 1;
+            go = false;
           }
-          if (b == 0 && i < L) {
-#pragma unroll
-            for (int qq = 0; qq < Q; ++qq) {
-              const int64_t p = L - Q + qq;
-              scores[((int64_t)seq * Q + qq) * ld + i] = (i <= p) ? acc[qq] : -INFINITY;
+          if (go) {
+            s.info_seq[st] = seqk;
+            s.info_page[st] = jk;
+            s.info_len[st] = lenk;
+            s.info_ok[st] = okk;
+            const uint32_t fb = smem_addr(&s.full[st]);
+            if (okk) {
+              mbar_arrive_expect_tx(fb, kPageBytes + Q * kHeadDim * 2);
+              bulk_copy_g2s(smem_addr(&s.stage[st][0]), src, kPageBytes, fb);
+              bulk_copy_g2s(smem_addr(&s.stage[st][kPageBytes]),
+                            iq + (int64_t)seqk * Q * kHeadDim, Q * kHeadDim * 2, fb);
+            } else {
+              mbar_arrive(fb);
             }
           }
         }
+        __syncwarp();
       }
     }
-    base_item += total;
-    __syncthreads();
+    return;
+  }
+
+  // ================= consumers
+  const int g = lane >> 2, tig = lane & 3;
+  uint32_t breg[NT][8][2];
+  float inv_scale[Q];
+  int cur_seq = -1;
+#pragma unroll
+  for (int qq = 0; qq < Q; ++qq) inv_scale[qq] = 1.f;
+
+  for (int kk = 0; kk < n; ++kk) {
+    const int st = kk % kScoreStages, round = kk / kScoreStages;
+    bool landed = false;
+    for (uint32_t i = 0; i < kWaitPolls && !landed; ++i) {
+      landed = mbar_test(smem_addr(&s.full[st]), round & 1);
+      if (!landed && s.abort_flag) break;
+    }
+    if (!__all_sync(0xFFFFFFFFu, landed)) {
+      if (lane == 0) flag(status, MX4_STATUS_TIMEOUT);
+      s.abort_flag = 1;
+      break;
+    }
+    const int seq = s.info_seq[st], pg = s.info_page[st], L = s.info_len[st];
+    if (s.info_ok[st]) {
+      const uint8_t* page = &s.stage[st][0];
+      if (seq != cur_seq) {
+        // index-q of this sequence -> f16 B fragments, scaled by 2^sigma per query
+        const uint16_t* qs = reinterpret_cast<const uint16_t*>(page + kPageBytes);
+        float sc[Q];
+#pragma unroll
+        for (int qq = 0; qq < Q; ++qq) {
+          const uint2 v = *reinterpret_cast<const uint2*>(qs + qq * kHeadDim + 4 * lane);
+          uint32_t a = max(max((v.x << 17) >> 1, v.x & 0x7FFF0000u),
+                           max((v.y << 17) >> 1, v.y & 0x7FFF0000u));
+          a = __reduce_max_sync(0xFFFFFFFFu, a);
+          const int sigma = (a == 0u) ? 0 : min(127, max(-126, 14 - ((int)(a >> 23) - 127)));
+          sc[qq] = __uint_as_float((uint32_t)(127 + sigma) << 23);
+          inv_scale[qq] = __uint_as_float((uint32_t)(127 - sigma) << 23);
+        }
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          const int qq = 2 * nt + (g >> 2);
+          const bool active = ((g & 3) == tig) && qq < Q;
+          const uint16_t* qv = qs + (qq < Q ? qq : 0) * kHeadDim + 32 * tig;
+          const float f = active ? sc[qq < Q ? qq : 0] : 0.f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const uint2 v = *reinterpret_cast<const uint2*>(qv + 4 * j);
+            breg[nt][j][0] = active ? pack_half2(bf16_bits_to_float(v.x & 0xFFFFu) * f,
+                                                 bf16_bits_to_float(v.x >> 16) * f)
+                                    : 0u;
+            breg[nt][j][1] = active ? pack_half2(bf16_bits_to_float(v.y & 0xFFFFu) * f,
+                                                 bf16_bits_to_float(v.y >> 16) * f)
+                                    : 0u;
+          }
+        }
+        cur_seq = seq;
+      }
+#pragma unroll
+      for (int tt = 0; tt < 2; ++tt) {
+        const int r0 = (warp + kScoreConsumers * tt) * 16;
+        const uint4 x = *reinterpret_cast<const uint4*>(page + (r0 + g) * kRowDataBytes + 16 * tig);
+        const uint4 y =
+            *reinterpret_cast<const uint4*>(page + (r0 + g + 8) * kRowDataBytes + 16 * tig);
+        const uint32_t sx = *reinterpret_cast<const uint32_t*>(page + kScaleOffset + (r0 + g) * 4);
+        const uint32_t sy =
+            *reinterpret_cast<const uint32_t*>(page + kScaleOffset + (r0 + g + 8) * 4);
+        const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+        float c[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
+#pragma unroll
+        for (int wi = 0; wi < 4; ++wi) {
+          uint32_t fx[4], fy[4];
+          e2m1x8_to_f16x2(xw[wi], fx);
+          e2m1x8_to_f16x2(yw[wi], fy);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            mma_m16n8k16_f16(c[nt], fx[0], fy[0], fx[1], fy[1], breg[nt][2 * wi][0],
+                             breg[nt][2 * wi][1]);
+            mma_m16n8k16_f16(c[nt], fx[2], fy[2], fx[3], fy[3], breg[nt][2 * wi + 1][0],
+                             breg[nt][2 * wi + 1][1]);
+          }
+        }
+        const int b0 = 2 * (tig & 1);
+        const float sx0 = e8m0_to_float((sx >> (8 * b0)) & 0xFFu);
+        const float sx1 = e8m0_to_float((sx >> (8 * b0 + 8)) & 0xFFu);
+        const float sy0 = e8m0_to_float((sy >> (8 * b0)) & 0xFFu);
+        const float sy1 = e8m0_to_float((sy >> (8 * b0 + 8)) & 0xFFu);
+        const int64_t i_g = (int64_t)pg * kPageTokens + r0 + g;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          float vg = c[nt][0] * sx0 + c[nt][1] * sx1;
+          float vg8 = c[nt][2] * sy0 + c[nt][3] * sy1;
+          vg += __shfl_xor_sync(0xFFFFFFFFu, vg, 1);
+          vg8 += __shfl_xor_sync(0xFFFFFFFFu, vg8, 1);
+          const int qq = 2 * nt + (tig >> 1);
+          if ((tig & 1) == 0 && qq < Q) {
+            const float isc = inv_scale[qq < Q ? qq : 0];
+            const int64_t p = (int64_t)L - Q + qq;
+            float* out = scores + ((int64_t)seq * Q + qq) * ld;
+            if (i_g < L) out[i_g] = (i_g <= p) ? vg * isc : -INFINITY;
+            if (i_g + 8 < L) out[i_g + 8] = (i_g + 8 <= p) ? vg8 * isc : -INFINITY;
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_addr(&s.empty[st]));
   }
 }
 
@@ -156,10 +280,20 @@ static cudaError_t launch_q(int grid, const uint16_t* iq, const uint8_t* idx_pag
                             const int32_t* block_table, int B, int64_t bt_width,
                             const int32_t* seq_lens, float* scores, int64_t ld, uint32_t* status,
                             cudaStream_t stream) {
-  index_score_kernel<Q><<<grid, kScoreThreads, 0, stream>>>(
-      iq, idx_pages, idx_page_stride, num_pages, block_table, B, bt_width, seq_lens, scores, ld,
-      status);
-  return cudaGetLastError();
+  const int smem = (int)sizeof(ScoreSmem);
+  cudaError_t err = cudaFuncSetAttribute(index_score_kernel<Q>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (err != cudaSuccess) return err;
+  for (int b0 = 0; b0 < B; b0 += kScoreMaxBatch) {
+    const int nb = min(kScoreMaxBatch, B - b0);
+    index_score_kernel<Q><<<grid, kScoreThreads, smem, stream>>>(
+        iq + (int64_t)b0 * Q * kHeadDim, idx_pages, idx_page_stride, num_pages,
+        block_table + (int64_t)b0 * bt_width, nb, bt_width, seq_lens + b0,
+        scores + (int64_t)b0 * Q * ld, ld, status);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  return cudaSuccess;
 }
 
 cudaError_t launch_index_score(const uint16_t* iq, int q, const uint8_t* idx_pages,
@@ -167,7 +301,7 @@ cudaError_t launch_index_score(const uint16_t* iq, int q, const uint8_t* idx_pag
                                const int32_t* block_table, int B, int64_t bt_width,
                                const int32_t* seq_lens, float* scores, int64_t ld,
                                uint32_t* status, int num_sms, cudaStream_t stream) {
-  const int grid = num_sms * 8;
+  const int grid = num_sms * 3;
   switch (q) {
     case 1: return launch_q<1>(grid, iq, idx_pages, idx_page_stride, num_pages, block_table, B,
                                bt_width, seq_lens, scores, ld, status, stream);
