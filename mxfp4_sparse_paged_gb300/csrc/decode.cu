@@ -11,25 +11,28 @@
 //
 // split kernel -- one CTA of 8 warps per (decode token, split of up to 512
 // selected entries):
-//   1. Resolve the split's indices to page rows; read each entry's K and V scale
-//      words; find the split's largest K scale (all blocks) and V scale (per
-//      32-dim block); turn every entry's scales into exact f16 multipliers
-//      2^(scale - reference), so that dequantised K/V values fit f16 exactly.
-//   2. Each warp streams its 16-entry tiles through a 4-stage cp.async ring
-//      (64 B of K data + 64 B of V data per entry, rows padded to 80 B so the
-//      fragment loads are bank-conflict free).
-//   3. Per tile: e2m1 -> f16 with the hardware cvt (exact grid values), times the
-//      multiplier; S = Q K^T with mma.sync m16n8k16 (Q = 16 heads x 128, f16,
-//      scaled by a power of two so bf16 fits f16 exactly); online softmax in
-//      fp32 (log2 units, lazy rescaling; weights scaled by 2^7 so the f16 P
-//      stays normal); P split into f16 hi + lo parts so
-//      P V keeps ~22 bits; O += P V with mma.sync, V fragments built by zipping
-//      the nibbles of two tokens so one cvt yields a (token, token) pair.
-//   4. The 8 warps' (max, sum, O) are merged in shared memory and the split
-//      writes its unnormalised output, running max (log2 units) and sum.
-// merge kernel -- one CTA per decode token combines the splits of each head.
-#include <cuda_fp16.h>
-
+//   1. Load the split's indices, the sequence's block-table row (into shared
+//      memory) and Q, all at once.  Resolve every entry to its page row and
+//      issue, in one batch, cp.async gathers of its 64 B of K data, 64 B of V
+//      data and the two 4-byte scale words into shared memory (rows padded to
+//      80 B so the fragment loads are bank-conflict free).
+//   2. From the staged scale words: the split's largest K scale (all blocks)
+//      and V scale (per 32-dim block), and for every entry exact f16
+//      multipliers 2^(scale - reference), so dequantised K/V values fit f16.
+//   3. Each warp computes its four 16-entry tiles: e2m1 -> f16 with the
+//      hardware cvt (exact grid values) times the multiplier; S = Q K^T with
+//      mma.sync m16n8k16 (Q = 16 heads x 128 in f16, scaled by a power of two
+//      so bf16 fits exactly); online softmax in fp32 (log2 units, lazy
+//      rescaling; weights scaled by 2^7 so the f16 P stays normal); P split into
+//      f16 hi + lo parts so P V keeps ~22 bits; O += P V with mma.sync, V
+//      fragments built by zipping the nibbles of two tokens so one cvt yields a
+//      (token, token) pair.
+//   4. The 8 warps' (max, sum, O) are merged in shared memory, in the MMA
+//      fragment order (bank-conflict free), and the split writes its
+//      unnormalised output in that order plus its running max (log2 units) and
+//      sum per head.
+// merge kernel -- one CTA per decode token combines the splits and maps the
+// fragment order back to [head][dim].
 #include "common.cuh"
 
 namespace mx4 {
@@ -39,23 +42,26 @@ constexpr int kDecWarps = 8;
 constexpr int kDecThreads = kDecWarps * 32;
 constexpr int kSplitTokens = 512;                   // selected entries per CTA
 constexpr int kTile = 16;                           // entries per MMA tile
-constexpr int kTilesPerWarp = kSplitTokens / kTile / kDecWarps;  // 4
-constexpr int kStages = 4;                          // cp.async ring depth per warp
+constexpr int kTiles = kSplitTokens / kTile;        // 32
+constexpr int kTilesPerWarp = kTiles / kDecWarps;   // 4
 constexpr int kRowPitch = 80;                       // staged row pitch (64 B + 16 B pad)
 constexpr int kStageBytes = 2 * kTile * kRowPitch;  // K rows then V rows: 2560 B
+constexpr int kBtCache = 2048;                      // block-table entries kept in smem
+constexpr int kFrag = kHeads * kHeadDim;            // 2048 outputs per split
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 128.f;  // p' = 2^(logit - m) * 2^7, at most 2^15 in f16
-constexpr float kLazy = 8.f;     // rescale only when the max grows by more than this
-static_assert(kTilesPerWarp * kTile * kDecWarps == kSplitTokens, "split geometry");
+constexpr float kLazy = 8.f;      // rescale only when the max grows by more than this
+static_assert(kTilesPerWarp * kDecWarps == kTiles, "split geometry");
 static_assert(2 * kDecThreads == kSplitTokens, "one entry pair per thread in the set-up phase");
-static_assert(kDecWarps * kHeads * kHeadDim * 4 <= kDecWarps * kStages * kStageBytes,
-              "merge buffer fits in the staging ring");
+static_assert(kDecWarps * kFrag * 4 <= kTiles * kStageBytes, "merge buffer fits in the stage");
 
 struct DecodeSmem {
-  uint8_t stage[kDecWarps][kStages][kStageBytes];  // 80 KB; reused by the final merge
+  uint8_t stage[kTiles][kStageBytes];  // 80 KB; reused by the final merge
   uint32_t kmul[kSplitTokens][4];      // f16x2 (m, m): K multiplier of block b of entry r
   uint32_t vmul[kSplitTokens / 2][4];  // f16x2 (m_2u, m_2u+1), blocks in slot order 0,2,1,3
-  int64_t off[kSplitTokens];           // byte offset of the entry's page + row*64, or -1
+  uint32_t ksw[kSplitTokens];          // staged K scale words
+  uint32_t vsw[kSplitTokens];          // staged V scale words
+  int32_t bt[kBtCache];                // the sequence's block-table row
   uint8_t ok[kSplitTokens];
   float red_m[kDecWarps][kHeads];
   float red_l[kDecWarps][kHeads];
@@ -67,11 +73,12 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool v
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
                "r"(valid ? 16 : 0));
 }
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N));
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 4 : 0));
 }
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n"); }
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -133,96 +140,79 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   const int begin = sp * kSplitTokens;
   const int cnt = max(0, min(kSplitTokens, kw - begin));
 
-  // ---- 1. entries -> page rows, scale words, split references.  Thread tid owns
-  // the entry pair (2 tid, 2 tid + 1).
-  uint32_t kmax = 0, vmax4 = 0;
-  uint32_t ksw[2], vsw[2];
+  // ---- 1a. indices, block-table row, Q: independent loads issued together
+  int32_t idx[2];
 #pragma unroll
   for (int e = 0; e < 2; ++e) {
     const int r = 2 * tid + e;
-    int64_t off = -1;
-    ksw[e] = vsw[e] = 0;
-    if (r < cnt) {
-      const int32_t i = topk[t * kw + begin + r];
-      if (i >= 0) {
-        if (i > p || (int64_t)i / kPageTokens >= bt_width) {
-          flag(status, MX4_STATUS_BAD_INDEX);
+    idx[e] = (r < cnt) ? topk[t * kw + begin + r] : -1;
+  }
+  const int64_t npg = min(bt_width, max((int64_t)0, p / kPageTokens + 1));
+  for (int j = tid; j < min(npg, (int64_t)kBtCache); j += kDecThreads)
+    s.bt[j] = block_table[seq * bt_width + j];
+  uint4 qraw[2][4];
+#pragma unroll
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      qraw[hh][b] = *reinterpret_cast<const uint4*>(
+          q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
+  __syncthreads();
+
+  // ---- 1b. resolve entries, gather rows and scale words (one cp.async batch)
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = 2 * tid + e;
+    const int32_t i = idx[e];
+    bool ok = false;
+    const uint8_t* kp = k_pages;
+    const uint8_t* vp = v_pages;
+    if (i >= 0) {
+      if (i > p || (int64_t)i / kPageTokens >= bt_width) {
+        flag(status, MX4_STATUS_BAD_INDEX);
+      } else {
+        const int64_t slot = i / kPageTokens;
+        const int32_t pid =
+            slot < kBtCache ? s.bt[slot] : block_table[seq * bt_width + slot];
+        if (pid < 0 || pid >= num_pages) {
+          flag(status, MX4_STATUS_BAD_PAGE);
         } else {
-          const int32_t pid = block_table[seq * bt_width + i / kPageTokens];
-          if (pid < 0 || pid >= num_pages) {
-            flag(status, MX4_STATUS_BAD_PAGE);
-          } else {
-            const int64_t pg = (int64_t)pid * kv_page_stride;
-            const int row = i % kPageTokens;
-            off = pg + row * kRowDataBytes;
-            ksw[e] = *reinterpret_cast<const uint32_t*>(k_pages + pg + kScaleOffset + row * 4);
-            vsw[e] = *reinterpret_cast<const uint32_t*>(v_pages + pg + kScaleOffset + row * 4);
-            kmax = max(kmax, max_byte(drop_nan_bytes(ksw[e])));
-            vmax4 = __vmaxu4(vmax4, drop_nan_bytes(vsw[e]));
-          }
+          const int64_t pg = (int64_t)pid * kv_page_stride;
+          kp = k_pages + pg;
+          vp = v_pages + pg;
+          ok = true;
         }
       }
     }
-    s.off[r] = off;
-    s.ok[r] = off >= 0;
-  }
-  kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+    s.ok[r] = ok;
+    const int row = ok ? (i % kPageTokens) : 0;
+    const uint32_t dk = smem_addr(&s.stage[r / kTile][(r % kTile) * kRowPitch]);
+    const uint32_t dv = dk + kTile * kRowPitch;
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) vmax4 = __vmaxu4(vmax4, __shfl_xor_sync(0xFFFFFFFFu, vmax4, o));
-  if (lane == 0) {
-    s.red_k[warp] = kmax;
-    s.red_v[warp] = vmax4;
-  }
-  __syncthreads();
-  uint32_t refK = 0, refV4 = 0;
-#pragma unroll
-  for (int w = 0; w < kDecWarps; ++w) {
-    refK = max(refK, s.red_k[w]);
-    refV4 = __vmaxu4(refV4, s.red_v[w]);
-  }
-  // multipliers (0 for invalid entries; their logits are masked below)
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = 2 * tid + e;
-    const bool ok = s.ok[r];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t m = ok ? f16_pow2((ksw[e] >> (8 * b)) & 0xFFu, refK) : 0u;
-      s.kmul[r][b] = m | (m << 16);
+    for (int c = 0; c < 4; ++c) {
+      cp_async16(dk + 16 * c, kp + row * kRowDataBytes + 16 * c, ok);
+      cp_async16(dv + 16 * c, vp + row * kRowDataBytes + 16 * c, ok);
     }
+    cp_async4(smem_addr(&s.ksw[r]), kp + kScaleOffset + row * kRowScaleBytes, ok);
+    cp_async4(smem_addr(&s.vsw[r]), vp + kScaleOffset + row * kRowScaleBytes, ok);
   }
-  {
-    const bool ok0 = s.ok[2 * tid], ok1 = s.ok[2 * tid + 1];
-#pragma unroll
-    for (int slot = 0; slot < 4; ++slot) {
-      const int b = (slot >> 1) + 2 * (slot & 1);  // slot order 0, 2, 1, 3
-      const uint32_t ref = (refV4 >> (8 * b)) & 0xFFu;
-      const uint32_t m0 = ok0 ? f16_pow2((vsw[0] >> (8 * b)) & 0xFFu, ref) : 0u;
-      const uint32_t m1 = ok1 ? f16_pow2((vsw[1] >> (8 * b)) & 0xFFu, ref) : 0u;
-      s.vmul[tid][slot] = m0 | (m1 << 16);
-    }
-  }
-  __syncthreads();
+  cp_async_commit();
 
-  // ---- Q as f16 A fragments, scaled by 2^sigma so that bf16 fits f16 exactly
+  // ---- Q as f16 A fragments (while the gathers are in flight), scaled by
+  // 2^sigma so that bf16 fits f16 exactly
   uint32_t qa[8][4];
   int sigma;
   {
-    float qf[2][4][8];
     uint32_t amax = 0;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint4 v = *reinterpret_cast<const uint4*>(
-            q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t w[4] = {qraw[hh][b].x, qraw[hh][b].y, qraw[hh][b].z, qraw[hh][b].w};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-          qf[hh][b][2 * j] = __uint_as_float(w[j] << 16);
-          qf[hh][b][2 * j + 1] = __uint_as_float(w[j] & 0xFFFF0000u);
-          amax = max(amax, (w[j] << 17) >> 1);          // |low bf16| as fp32 bits
-          amax = max(amax, (w[j] & 0x7FFF0000u));       // |high bf16|
+          amax = max(amax, (w[j] << 17) >> 1);     // |low bf16| as fp32 bits
+          amax = max(amax, (w[j] & 0x7FFF0000u));  // |high bf16|
         }
       }
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
@@ -234,54 +224,91 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         // slice 2b+h: k = 2tig,2tig+1 <-> dims 32b+8tig+4h+{0,1}; k = 2tig+8,+9 <-> +{2,3}
-        qa[2 * b + h][0] = pack_f16x2(qf[0][b][4 * h] * sc, qf[0][b][4 * h + 1] * sc);
-        qa[2 * b + h][1] = pack_f16x2(qf[1][b][4 * h] * sc, qf[1][b][4 * h + 1] * sc);
-        qa[2 * b + h][2] = pack_f16x2(qf[0][b][4 * h + 2] * sc, qf[0][b][4 * h + 3] * sc);
-        qa[2 * b + h][3] = pack_f16x2(qf[1][b][4 * h + 2] * sc, qf[1][b][4 * h + 3] * sc);
+        const uint32_t w0 = h ? qraw[0][b].z : qraw[0][b].x, w1 = h ? qraw[0][b].w : qraw[0][b].y;
+        const uint32_t u0 = h ? qraw[1][b].z : qraw[1][b].x, u1 = h ? qraw[1][b].w : qraw[1][b].y;
+        qa[2 * b + h][0] = pack_f16x2(bf16_bits_to_float(w0 & 0xFFFFu) * sc,
+                                      bf16_bits_to_float(w0 >> 16) * sc);
+        qa[2 * b + h][1] = pack_f16x2(bf16_bits_to_float(u0 & 0xFFFFu) * sc,
+                                      bf16_bits_to_float(u0 >> 16) * sc);
+        qa[2 * b + h][2] = pack_f16x2(bf16_bits_to_float(w1 & 0xFFFFu) * sc,
+                                      bf16_bits_to_float(w1 >> 16) * sc);
+        qa[2 * b + h][3] = pack_f16x2(bf16_bits_to_float(u1 & 0xFFFFu) * sc,
+                                      bf16_bits_to_float(u1 >> 16) * sc);
       }
   }
+  cp_async_wait_all();
+  __syncthreads();
+
+  // ---- 2. split references and per-entry multipliers
+  {
+    uint32_t kmax = 0, vmax4 = 0;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int r = 2 * tid + e;
+      if (s.ok[r]) {
+        kmax = max(kmax, max_byte(drop_nan_bytes(s.ksw[r])));
+        vmax4 = __vmaxu4(vmax4, drop_nan_bytes(s.vsw[r]));
+      }
+    }
+    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+      vmax4 = __vmaxu4(vmax4, __shfl_xor_sync(0xFFFFFFFFu, vmax4, o));
+    if (lane == 0) {
+      s.red_k[warp] = kmax;
+      s.red_v[warp] = vmax4;
+    }
+  }
+  __syncthreads();
+  uint32_t refK = 0, refV4 = 0;
+#pragma unroll
+  for (int w = 0; w < kDecWarps; ++w) {
+    refK = max(refK, s.red_k[w]);
+    refV4 = __vmaxu4(refV4, s.red_v[w]);
+  }
+  {
+    const bool ok0 = s.ok[2 * tid], ok1 = s.ok[2 * tid + 1];
+    const uint32_t k0 = s.ksw[2 * tid], k1 = s.ksw[2 * tid + 1];
+    const uint32_t v0 = s.vsw[2 * tid], v1 = s.vsw[2 * tid + 1];
+    uint32_t km0[4], km1[4], vm[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t m0 = ok0 ? f16_pow2((k0 >> (8 * b)) & 0xFFu, refK) : 0u;
+      const uint32_t m1 = ok1 ? f16_pow2((k1 >> (8 * b)) & 0xFFu, refK) : 0u;
+      km0[b] = m0 | (m0 << 16);
+      km1[b] = m1 | (m1 << 16);
+    }
+#pragma unroll
+    for (int slot = 0; slot < 4; ++slot) {
+      const int b = (slot >> 1) + 2 * (slot & 1);  // slot order 0, 2, 1, 3
+      const uint32_t ref = (refV4 >> (8 * b)) & 0xFFu;
+      const uint32_t m0 = ok0 ? f16_pow2((v0 >> (8 * b)) & 0xFFu, ref) : 0u;
+      const uint32_t m1 = ok1 ? f16_pow2((v1 >> (8 * b)) & 0xFFu, ref) : 0u;
+      vm[slot] = m0 | (m1 << 16);
+    }
+    *reinterpret_cast<uint4*>(&s.kmul[2 * tid][0]) = make_uint4(km0[0], km0[1], km0[2], km0[3]);
+    *reinterpret_cast<uint4*>(&s.kmul[2 * tid + 1][0]) =
+        make_uint4(km1[0], km1[1], km1[2], km1[3]);
+    *reinterpret_cast<uint4*>(&s.vmul[tid][0]) = make_uint4(vm[0], vm[1], vm[2], vm[3]);
+  }
+  __syncthreads();
   // logit (log2 units) = S * cK
   const float cK = ldexpf(scale * kLog2e, (int)refK - 127 - sigma);
 
-  // ---- 2/3. this warp's tiles through the cp.async ring
+  // ---- 3. this warp's tiles
   const int n_tiles = (cnt + kTile - 1) / kTile;
-  const int n_my = n_tiles > warp ? (n_tiles - warp + kDecWarps - 1) / kDecWarps : 0;
-  const uint32_t stage0 = smem_addr(&s.stage[warp][0][0]);
-
-  auto issue = [&](int u) {
-    const int tb = (warp + kDecWarps * u) * kTile;
-    const int e = lane >> 1, half = lane & 1;
-    const int r = tb + e;
-    const int64_t off = (r < cnt) ? s.off[r] : -1;
-    const bool ok = off >= 0;
-    const uint32_t dst = stage0 + (u % kStages) * kStageBytes + e * kRowPitch + half * 32;
-    const uint8_t* ks = k_pages + (ok ? off : 0) + half * 32;
-    const uint8_t* vs = v_pages + (ok ? off : 0) + half * 32;
-    cp_async16(dst, ks, ok);
-    cp_async16(dst + 16, ks + 16, ok);
-    cp_async16(dst + kTile * kRowPitch, vs, ok);
-    cp_async16(dst + kTile * kRowPitch + 16, vs + 16, ok);
-  };
-
   float o[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m_used[2] = {-INFINITY, -INFINITY};
   float lsum[2] = {0.f, 0.f};
 
-#pragma unroll
-  for (int u = 0; u < kStages - 1; ++u) {
-    if (u < n_my) issue(u);
-    cp_async_commit();
-  }
-  for (int u = 0; u < n_my; ++u) {
-    if (u + kStages - 1 < n_my) issue(u + kStages - 1);
-    cp_async_commit();
-    cp_async_wait<kStages - 1>();
-    __syncwarp();
-    const uint8_t* sk = &s.stage[warp][u % kStages][0];
+  for (int u = 0; u < kTilesPerWarp; ++u) {
+    const int tile = warp + kDecWarps * u;
+    if (tile >= n_tiles) break;
+    const uint8_t* sk = &s.stage[tile][0];
     const uint8_t* sv = sk + kTile * kRowPitch;
-    const int tb = (warp + kDecWarps * u) * kTile;
+    const int tb = tile * kTile;
 
     // S = Q K^T for tokens tb .. tb+15 (two n8 tiles)
     float c[2][4];
@@ -391,17 +418,15 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
         mma_m16n8k16_f16(o[8 * h + i], pl[0], pl[1], pl[2], pl[3], b0, b1);
       }
     }
-    __syncwarp();
   }
-  cp_async_wait<0>();
 
-  // ---- 4. merge the warps' partial results in shared memory
+  // ---- 4. merge the warps' partial results (fragment order, conflict free)
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr) {
     lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 1);
     lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 2);
   }
-  __syncthreads();  // every warp is done with its ring
+  __syncthreads();  // every warp is done with the staged rows
   if (tig == 0) {
     s.red_m[warp][g] = m_used[0];
     s.red_m[warp][g + 8] = m_used[1];
@@ -419,27 +444,25 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
 #pragma unroll
   for (int rr = 0; rr < 2; ++rr)
     fw[rr] = (m_used[rr] == -INFINITY) ? 0.f : exp2f(m_used[rr] - M[rr]);
-  float* red_o = reinterpret_cast<float*>(&s.stage[0][0][0]);  // [warp][head][dim]
   float fv[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) fv[b] = ldexpf(1.f, (int)((refV4 >> (8 * b)) & 0xFFu) - 127);
+  // element (j, c) of lane l lives at red[warp][(4 j + c) * 32 + l]
+  float* red = reinterpret_cast<float*>(&s.stage[0][0]);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    const int h = j >> 3, i = j & 7;
-    const int d0 = 8 * (2 * tig + 8 * h) + i, d1 = d0 + 8;
-    const float f = fv[(2 * tig + 8 * h) >> 2];
-    red_o[(warp * kHeads + g) * kHeadDim + d0] = o[j][0] * fw[0] * f;
-    red_o[(warp * kHeads + g) * kHeadDim + d1] = o[j][1] * fw[0] * f;
-    red_o[(warp * kHeads + g + 8) * kHeadDim + d0] = o[j][2] * fw[1] * f;
-    red_o[(warp * kHeads + g + 8) * kHeadDim + d1] = o[j][3] * fw[1] * f;
+    const float f = fv[(2 * tig + 8 * (j >> 3)) >> 2];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      red[warp * kFrag + (4 * j + c) * 32 + lane] = o[j][c] * fw[c >> 1] * f;
   }
   __syncthreads();
-  const int64_t slot0 = (t * S + sp) * kHeads;
-  for (int e = tid; e < kHeads * kHeadDim; e += kDecThreads) {
+  const int64_t split = t * S + sp;
+  for (int e = tid; e < kFrag; e += kDecThreads) {
     float acc = 0.f;
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) acc += red_o[w * kHeads * kHeadDim + e];
-    ws_o[slot0 * kHeadDim + e] = acc;
+    for (int w = 0; w < kDecWarps; ++w) acc += red[w * kFrag + e];
+    ws_o[split * kFrag + e] = acc;
   }
   if (tid < kHeads) {
     float Mh = -INFINITY;
@@ -448,45 +471,46 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
     if (Mh != -INFINITY)
       for (int w = 0; w < kDecWarps; ++w)
         if (s.red_m[w][tid] != -INFINITY) l += s.red_l[w][tid] * exp2f(s.red_m[w][tid] - Mh);
-    ws_ml[(slot0 + tid) * 2 + 0] = Mh;
-    ws_ml[(slot0 + tid) * 2 + 1] = l;
+    ws_ml[(split * kHeads + tid) * 2 + 0] = Mh;
+    ws_ml[(split * kHeads + tid) * 2 + 1] = l;
   }
 }
 
-// One CTA per decode token; thread (h, part) merges dims 8*part .. 8*part+7 of
-// head h over the splits: out = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).
-constexpr int kMergeThreads = kHeads * (kHeadDim / 8);
+// One CTA per decode token.  Split s holds, for fragment element e, the
+// unnormalised output O_s[e]; the head's max m_s and sum l_s are per head.
+// out = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).  Element e maps back to
+// (head, dim): lane = e % 32 (g = lane/4, tig = lane%4), c = (e/32) % 4,
+// j = e / 128; head = g + 8 (c/2); dim = 8 (2 tig + c%2 + 8 (j/8)) + j%8.
+constexpr int kMergeThreads = 256;
+constexpr int kMaxSplits = 128;
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int S,
                     float* __restrict__ out) {
+  __shared__ float s_w[kMaxSplits][kHeads];
+  __shared__ float s_l[kHeads];
   const int64_t t = blockIdx.x;
-  const int h = threadIdx.x / (kHeadDim / 8), d0 = (threadIdx.x % (kHeadDim / 8)) * 8;
-  float M = -INFINITY;
-  for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ws_ml[((t * S + sp) * kHeads + h) * 2]);
-  float l = 0.f;
-  float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
-  if (M != -INFINITY) {
+  const int tid = threadIdx.x;
+  if (tid < kHeads) {
+    float M = -INFINITY;
+    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ws_ml[((t * S + sp) * kHeads + tid) * 2]);
+    float l = 0.f;
     for (int sp = 0; sp < S; ++sp) {
-      const int64_t slot = (t * S + sp) * kHeads + h;
-      const float ms = ws_ml[slot * 2];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
-      l = fmaf(ws_ml[slot * 2 + 1], w, l);
-      const float4 x0 = *reinterpret_cast<const float4*>(ws_o + slot * kHeadDim + d0);
-      const float4 x1 = *reinterpret_cast<const float4*>(ws_o + slot * kHeadDim + d0 + 4);
-      a0.x = fmaf(x0.x, w, a0.x); a0.y = fmaf(x0.y, w, a0.y);
-      a0.z = fmaf(x0.z, w, a0.z); a0.w = fmaf(x0.w, w, a0.w);
-      a1.x = fmaf(x1.x, w, a1.x); a1.y = fmaf(x1.y, w, a1.y);
-      a1.z = fmaf(x1.z, w, a1.z); a1.w = fmaf(x1.w, w, a1.w);
+      const float ms = ws_ml[((t * S + sp) * kHeads + tid) * 2];
+      const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
+      s_w[sp][tid] = w;
+      l = fmaf(ws_ml[((t * S + sp) * kHeads + tid) * 2 + 1], w, l);
     }
+    s_l[tid] = l;
   }
-  float* o = out + (t * kHeads + h) * kHeadDim + d0;
-  if (l > 0.f) {
-    *reinterpret_cast<float4*>(o) = make_float4(a0.x / l, a0.y / l, a0.z / l, a0.w / l);
-    *reinterpret_cast<float4*>(o + 4) = make_float4(a1.x / l, a1.y / l, a1.z / l, a1.w / l);
-  } else {
-    *reinterpret_cast<float4*>(o) = make_float4(0.f, 0.f, 0.f, 0.f);
-    *reinterpret_cast<float4*>(o + 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  for (int e = tid; e < kFrag; e += kMergeThreads) {
+    const int lane = e & 31, c = (e >> 5) & 3, j = e >> 7;
+    const int head = (lane >> 2) + 8 * (c >> 1);
+    const int dim = 8 * (2 * (lane & 3) + (c & 1) + 8 * (j >> 3)) + (j & 7);
+    float acc = 0.f;
+    for (int sp = 0; sp < S; ++sp) acc = fmaf(ws_o[(t * S + sp) * kFrag + e], s_w[sp][head], acc);
+    const float l = s_l[head];
+    out[(t * kHeads + head) * kHeadDim + dim] = (l > 0.f) ? acc / l : 0.f;
   }
 }
 
@@ -504,8 +528,9 @@ cudaError_t launch_decode(const uint16_t* q, int64_t T, int Q, const uint8_t* k_
                           uint32_t* status, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
   const int S = decode_splits(kw);
+  if (S > kMaxSplits) return cudaErrorInvalidValue;
   float* ws_o = static_cast<float*>(ws);
-  float* ws_ml = ws_o + T * S * kHeads * kHeadDim;
+  float* ws_ml = ws_o + T * S * kFrag;
   const int smem = (int)sizeof(DecodeSmem);
   cudaError_t err =
       cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);

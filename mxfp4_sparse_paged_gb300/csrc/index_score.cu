@@ -11,11 +11,11 @@
 // shared memory maps a flat page number to (sequence, page)).  All q decode
 // tokens of a sequence are scored in one pass over its pages.
 //
-// Pipeline: warp 4 is the producer.  It resolves pages through the block table
+// Pipeline: warp 8 is the producer.  It resolves pages through the block table
 // (32 lanes at a time) and streams each 8704-byte page, plus the sequence's
 // index-q rows, into a 5-stage shared-memory ring with bulk copies (TMA engine)
-// that complete on the stage's "full" mbarrier.  Warps 0-3 consume: each takes
-// two 16-row tiles of the page.
+// that complete on the stage's "full" mbarrier.  Warps 0-7 consume: each takes
+// one 16-row tile of the page.
 //
 // Math (per tile, tensor cores): A = 16 index-key rows x 128 dims, decoded by
 // the hardware e2m1 -> f16 conversion (exact); thread t of a quad owns the 32
@@ -28,7 +28,7 @@
 
 namespace mx4 {
 
-constexpr int kScoreConsumers = 4;
+constexpr int kScoreConsumers = 8;
 constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;
 constexpr int kScoreStages = 5;
 constexpr int kMaxQ = 8;
@@ -221,7 +221,7 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
         cur_seq = seq;
       }
 #pragma unroll
-      for (int tt = 0; tt < 2; ++tt) {
+      for (int tt = 0; tt < kPageTokens / 16 / kScoreConsumers; ++tt) {
         const int r0 = (warp + kScoreConsumers * tt) * 16;
         const uint4 x = *reinterpret_cast<const uint4*>(page + (r0 + g) * kRowDataBytes + 16 * tig);
         const uint4 y =

@@ -33,6 +33,7 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kCand = 8192;
 constexpr int kSample = 2048;
+constexpr int kUnroll = 4;  // row loads in flight per lane in the candidate passes
 static_assert(kTopkWarps <= 32 && kTopkThreads >= 256, "one scan warp; 256 radix bins");
 
 struct TopkSmem {
@@ -115,7 +116,9 @@ __device__ void radix_select_smem(const uint32_t* keys, int C, uint32_t rank, ui
   *want = w;
 }
 
-// Keys of the 4 (VEC) or 1 elements at i .. of the row; i beyond n -> no key.
+// Keys of the 4 (VEC) or 1 elements at i .. of the row, in k[0..m); elements at
+// or beyond n are not loaded.  Returns m.  (Static indexing only, so the keys
+// stay in registers.)
 template <bool VEC>
 __device__ __forceinline__ int load_keys(const float* row, int64_t i, int64_t n, uint32_t (&k)[4]) {
   if (VEC && i + 3 < n) {
@@ -126,11 +129,10 @@ __device__ __forceinline__ int load_keys(const float* row, int64_t i, int64_t n,
     k[3] = order_key(v.w);
     return 4;
   }
-  int c = 0;
 #pragma unroll
-  for (int e = 0; e < (VEC ? 4 : 1); ++e)
-    if (i + e < n) k[c++] = order_key(row[i + e]);
-  return c;
+  for (int e = 0; e < 4; ++e) k[e] = (e < (VEC ? 4 : 1) && i + e < n) ? order_key(row[i + e]) : 0u;
+  const int64_t m = n - i;
+  return m <= 0 ? 0 : (int)min(m, (int64_t)(VEC ? 4 : 1));
 }
 
 // Candidate pass over the row: keys >= thr, in index order.  Returns the total
@@ -142,12 +144,18 @@ __device__ int collect_candidates(const float* row, int64_t n, uint32_t thr, Top
   const int64_t per_it = 32 * E;
   const int64_t chunk = ((n + kTopkWarps - 1) / kTopkWarps + per_it - 1) / per_it * per_it;
   const int64_t c0 = min(n, (int64_t)warp * chunk), c1 = min(n, c0 + chunk);
-  // counting pass
+  // counting pass (kUnroll loads in flight per lane)
   int cnt = 0;
-  for (int64_t b = c0; b < c1; b += per_it) {
-    uint32_t k[4];
-    const int m = load_keys<VEC>(row, b + (int64_t)lane * E, c1, k);
-    for (int e = 0; e < m; ++e) cnt += k[e] >= thr;
+  for (int64_t b = c0; b < c1; b += per_it * kUnroll) {
+    uint32_t k[kUnroll][4];
+    int m[kUnroll];
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+      m[u] = load_keys<VEC>(row, b + per_it * u + (int64_t)lane * E, c1, k[u]);
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) cnt += (e < m[u] && k[u][e] >= thr) ? 1 : 0;
   }
   cnt = __reduce_add_sync(0xFFFFFFFFu, cnt);
   if (lane == 0) s.warp_base[warp] = cnt;
@@ -167,26 +175,34 @@ __device__ int collect_candidates(const float* row, int64_t n, uint32_t thr, Top
   const int total = s.tmp[0];
   if (total <= kCand) {
     int pos = s.warp_base[warp];
-    for (int64_t b = c0; b < c1; b += per_it) {
-      uint32_t k[4];
-      const int64_t i0 = b + (int64_t)lane * E;
-      const int m = load_keys<VEC>(row, i0, c1, k);
-      int mine = 0;
-      for (int e = 0; e < m; ++e) mine += k[e] >= thr;
-      int inc = mine;
+    for (int64_t b = c0; b < c1; b += per_it * kUnroll) {
+      uint32_t k[kUnroll][4];
+      int m[kUnroll];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += y;
-      }
-      int w = pos + inc - mine;
-      for (int e = 0; e < m; ++e)
-        if (k[e] >= thr) {
-          s.ckey[w] = k[e];
-          s.cidx[w] = (uint32_t)(i0 + e);
-          ++w;
+      for (int u = 0; u < kUnroll; ++u)
+        m[u] = load_keys<VEC>(row, b + per_it * u + (int64_t)lane * E, c1, k[u]);
+#pragma unroll
+      for (int u = 0; u < kUnroll; ++u) {
+        const int64_t i0 = b + per_it * u + (int64_t)lane * E;
+        int mine = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) mine += (e < m[u] && k[u][e] >= thr) ? 1 : 0;
+        int inc = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+          if (lane >= o) inc += y;
         }
-      pos += __shfl_sync(0xFFFFFFFFu, inc, 31);
+        int w = pos + inc - mine;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (e < m[u] && k[u][e] >= thr) {
+            s.ckey[w] = k[u][e];
+            s.cidx[w] = (uint32_t)(i0 + e);
+            ++w;
+          }
+        pos += __shfl_sync(0xFFFFFFFFu, inc, 31);
+      }
     }
   }
   __syncthreads();
