@@ -64,7 +64,7 @@ def _config(wl):
 # --------------------------------------------------------------------------- clocks
 
 class Clocks:
-    """nvidia-smi sampled every 200 ms during the timed region."""
+    """nvidia-smi sampled every 50 ms during the timed region."""
 
     def __init__(self, index: int):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
@@ -73,7 +73,7 @@ class Clocks:
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
         try:
             self.p = subprocess.Popen(["nvidia-smi", f"--id={index}", f"--query-gpu={q}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                       "--format=csv,noheader,nounits", "-lms", "50"],
                                       stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.p = None
@@ -292,13 +292,21 @@ def run_gpu(args):
 
 
 def _ncu_traffic(name):
-    """dram bytes per index_score launch from the committed ncu summary, if one
-    was taken on the current kernel for this workload."""
+    """dram bytes (read + write) per index_score launch from the committed ncu
+    record for this workload, or None when there is none or the kernel's sources
+    changed since the counters were taken."""
+    import hashlib
     p = os.path.join(ROOT, "profiles", "index_score_traffic.json")
     try:
         with open(p) as f:
-            d = json.load(f)
-        return d.get(name)
+            rec = json.load(f)[name]
+        h = hashlib.sha256()
+        for src in rec["kernel_sources"]:
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != rec["kernel_sources_sha256_16"]:
+            return None
+        return int(rec["traffic_bytes_per_launch"])
     except Exception:
         return None
 
