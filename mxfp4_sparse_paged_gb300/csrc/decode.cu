@@ -29,10 +29,9 @@
 //      (token, token) pair.
 //   4. The 8 warps' (max, sum, O) are merged in shared memory, in the MMA
 //      fragment order (bank-conflict free), and the split writes its
-//      unnormalised output in that order plus its running max (log2 units) and
+//      unnormalised [head][dim] output plus its running max (log2 units) and
 //      sum per head.
-// merge kernel -- one CTA per decode token combines the splits and maps the
-// fragment order back to [head][dim].
+// merge kernel -- one CTA per decode token combines the splits.
 #include "common.cuh"
 
 namespace mx4 {
@@ -457,12 +456,17 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
       red[warp * kFrag + (4 * j + c) * 32 + lane] = o[j][c] * fw[c >> 1] * f;
   }
   __syncthreads();
+  // fragment element e -> (head, dim): lane = e % 32 (g = lane/4, tig = lane%4),
+  // c = (e/32) % 4, j = e / 128; head = g + 8 (c/2); dim = 8 (2 tig + c%2 + 8 (j/8)) + j%8
   const int64_t split = t * S + sp;
   for (int e = tid; e < kFrag; e += kDecThreads) {
     float acc = 0.f;
 #pragma unroll
     for (int w = 0; w < kDecWarps; ++w) acc += red[w * kFrag + e];
-    ws_o[split * kFrag + e] = acc;
+    const int ln = e & 31, c = (e >> 5) & 3, j = e >> 7;
+    const int head = (ln >> 2) + 8 * (c >> 1);
+    const int dim = 8 * (2 * (ln & 3) + (c & 1) + 8 * (j >> 3)) + (j & 7);
+    ws_o[split * kFrag + head * kHeadDim + dim] = acc;
   }
   if (tid < kHeads) {
     float Mh = -INFINITY;
@@ -476,42 +480,38 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   }
 }
 
-// One CTA per decode token.  Split s holds, for fragment element e, the
-// unnormalised output O_s[e]; the head's max m_s and sum l_s are per head.
-// out = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M).  Element e maps back to
-// (head, dim): lane = e % 32 (g = lane/4, tig = lane%4), c = (e/32) % 4,
-// j = e / 128; head = g + 8 (c/2); dim = 8 (2 tig + c%2 + 8 (j/8)) + j%8.
-constexpr int kMergeThreads = 256;
+// One CTA per decode token; thread (h, part) combines dims 4*part .. 4*part+3 of
+// head h over the splits: out = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M),
+// with O_s the split's unnormalised [head][dim] output and (m_s, l_s) its
+// running max (log2 units) and sum for the head.
+constexpr int kMergeThreads = kHeads * (kHeadDim / 4);  // 512
 constexpr int kMaxSplits = 128;
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int S,
                     float* __restrict__ out) {
-  __shared__ float s_w[kMaxSplits][kHeads];
-  __shared__ float s_l[kHeads];
   const int64_t t = blockIdx.x;
-  const int tid = threadIdx.x;
-  if (tid < kHeads) {
-    float M = -INFINITY;
-    for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ws_ml[((t * S + sp) * kHeads + tid) * 2]);
-    float l = 0.f;
+  const int h = threadIdx.x / (kHeadDim / 4), d0 = 4 * (threadIdx.x % (kHeadDim / 4));
+  float M = -INFINITY;
+  for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ws_ml[((t * S + sp) * kHeads + h) * 2]);
+  float l = 0.f;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (M != -INFINITY) {
     for (int sp = 0; sp < S; ++sp) {
-      const float ms = ws_ml[((t * S + sp) * kHeads + tid) * 2];
-      const float w = (M == -INFINITY || ms == -INFINITY) ? 0.f : exp2f(ms - M);
-      s_w[sp][tid] = w;
-      l = fmaf(ws_ml[((t * S + sp) * kHeads + tid) * 2 + 1], w, l);
+      const int64_t slot = (t * S + sp) * kHeads + h;
+      const float ms = ws_ml[slot * 2];
+      if (ms == -INFINITY) continue;
+      const float w = exp2f(ms - M);
+      l = fmaf(ws_ml[slot * 2 + 1], w, l);
+      const float4 x = *reinterpret_cast<const float4*>(ws_o + slot * kHeadDim + d0);
+      acc.x = fmaf(x.x, w, acc.x);
+      acc.y = fmaf(x.y, w, acc.y);
+      acc.z = fmaf(x.z, w, acc.z);
+      acc.w = fmaf(x.w, w, acc.w);
     }
-    s_l[tid] = l;
   }
-  __syncthreads();
-  for (int e = tid; e < kFrag; e += kMergeThreads) {
-    const int lane = e & 31, c = (e >> 5) & 3, j = e >> 7;
-    const int head = (lane >> 2) + 8 * (c >> 1);
-    const int dim = 8 * (2 * (lane & 3) + (c & 1) + 8 * (j >> 3)) + (j & 7);
-    float acc = 0.f;
-    for (int sp = 0; sp < S; ++sp) acc = fmaf(ws_o[(t * S + sp) * kFrag + e], s_w[sp][head], acc);
-    const float l = s_l[head];
-    out[(t * kHeads + head) * kHeadDim + dim] = (l > 0.f) ? acc / l : 0.f;
-  }
+  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (l > 0.f) r = make_float4(acc.x / l, acc.y / l, acc.z / l, acc.w / l);
+  *reinterpret_cast<float4*>(out + (t * kHeads + h) * kHeadDim + d0) = r;
 }
 
 int decode_splits(int kw) { return (kw + kSplitTokens - 1) / kSplitTokens; }
