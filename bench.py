@@ -4,7 +4,8 @@ A step is the whole hot path on one batch: mx4_insert of the decode tokens'
 K/V/index-K rows (when the workload inserts in the step), index_score over
 every cached index key, topk_select, sparse_paged_decode (split + merge).
 Inputs are resident in HBM when the timed region starts; the L2 is flushed
-(a 256 MiB write) between timed steps, outside the per-step CUDA events.
+(a 256 MiB write, then a read of it so the write-back of its dirty lines
+falls outside the step) between timed steps, outside the per-step CUDA events.
 
 Default workload: 256 sequences, lognormal contexts (median 8192, capped at
 131072), one decode token each inserted in the step, top-2048 -- the only
@@ -57,7 +58,8 @@ def _config(wl):
                                                 "max": int(L.max()), "sum": int(L.sum())},
             "top_k": wl.k, "q_heads": W.Q_HEADS, "kv_heads": W.KV_HEADS, "head_dim": W.HEAD_DIM,
             "insert_in_step": wl.spec.insert_in_step, "seed": wl.spec.seed,
-            "l2": "flushed between timed steps (256 MiB write, outside the step events)",
+            "l2": "flushed between timed steps (256 MiB written then read back, outside the "
+                  "step events, so no dirty lines of the flush are written back inside them)",
             "parallelism": "replicas (one independent batch per GPU)"}
 
 
@@ -184,6 +186,12 @@ def run_gpu(args):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2(v):
+        # Write a buffer twice the L2 size, then read it back: the read evicts the
+        # written lines, so their write-back lands here rather than in the step.
+        flush.fill_(v)
+        flush.view(torch.int32).sum()
     ab = W.algorithmic_bytes(wl)
 
     # The in-step insert rewrites the decode tokens' rows with the same values, so
@@ -192,21 +200,20 @@ def run_gpu(args):
         ["index_score", "topk_select", "sparse_paged_decode"]
     step.load_inputs(host)
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush_l2(1)
         step.run(stream=stream)
     m.mx4_check_status()
 
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names}
     st = [(ev(), ev()) for _ in range(args.steps)]
     clocks = Clocks(local)
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i & 0xFF)
         st[i][0].record(stream)
-        step.run(stream=stream, events={n: per[n][i] for n in names})
+        step.run(stream=stream)
         st[i][1].record(stream)
     torch.cuda.synchronize()
     barrier()
@@ -214,6 +221,15 @@ def run_gpu(args):
     ck = clocks.stop()
     m.mx4_check_status()
     step_ms = [a.elapsed_time(b) for a, b in st]
+    # Per-kernel times: the same steps again with an event pair around each entry
+    # point (events between kernels stop a kernel from starting early under the
+    # previous one, so they are kept out of the step timing above).
+    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names}
+    for i in range(args.steps):
+        flush_l2(i & 0xFF)
+        step.run(stream=stream, events={n: per[n][i] for n in names})
+    torch.cuda.synchronize()
+    m.mx4_check_status()
     kern_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in per[n]) for n in names}
     total_ms = sum(step_ms)
     if world > 1:
@@ -237,7 +253,7 @@ def run_gpu(args):
     barrier()
     torch.cuda.synchronize()
     for i in range(args.steps):
-        flush.fill_(i & 0xFF)
+        flush_l2(i & 0xFF)
         e_st[i][0].record(stream)
         step.load_inputs(pin, non_blocking=True)
         step.run(stream=stream)

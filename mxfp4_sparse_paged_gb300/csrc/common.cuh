@@ -36,6 +36,34 @@ __device__ __forceinline__ float e2m1_to_float(uint32_t c) {
   return __uint_as_float(__float_as_uint(mag) | ((c & 8u) << 28));
 }
 
+// Programmatic dependent launch.  Every kernel of the library is launched with
+// launch_pdl and signals its dependents as soon as it starts, so the next kernel
+// in the stream can be scheduled while this one drains.  A kernel may run code
+// before pdl_wait() only if it reads inputs no kernel of the library writes
+// (sequence lengths, block tables) and writes nothing but shared memory;
+// pdl_wait() returns once the previous kernel in the stream has completed and
+// its writes are visible (at once when there is none).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) {
   return __uint_as_float(b << 16);
 }

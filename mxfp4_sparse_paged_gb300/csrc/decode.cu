@@ -131,6 +131,7 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   DecodeSmem& s = *reinterpret_cast<DecodeSmem*>(smem_raw);
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_launch_dependents();
   const int g = lane >> 2, tig = lane & 3;
   const int64_t t = blockIdx.x / S;
   const int sp = blockIdx.x % S;
@@ -139,13 +140,7 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   const int begin = sp * kSplitTokens;
   const int cnt = max(0, min(kSplitTokens, kw - begin));
 
-  // ---- 1a. indices, block-table row, Q: independent loads issued together
-  int32_t idx[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = 2 * tid + e;
-    idx[e] = (r < cnt) ? topk[t * kw + begin + r] : -1;
-  }
+  // ---- 1a. block-table row, Q, then (after the top-k kernel) the indices
   const int64_t npg = min(bt_width, max((int64_t)0, p / kPageTokens + 1));
   for (int j = tid; j < min(npg, (int64_t)kBtCache); j += kDecThreads)
     s.bt[j] = block_table[seq * bt_width + j];
@@ -156,6 +151,13 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
     for (int b = 0; b < 4; ++b)
       qraw[hh][b] = *reinterpret_cast<const uint4*>(
           q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
+  pdl_wait();  // top-k indices and pages are touched from here on
+  int32_t idx[2];
+#pragma unroll
+  for (int e = 0; e < 2; ++e) {
+    const int r = 2 * tid + e;
+    idx[e] = (r < cnt) ? topk[t * kw + begin + r] : -1;
+  }
   __syncthreads();
 
   // ---- 1b. resolve entries, gather rows and scale words (one cp.async batch)
@@ -489,6 +491,8 @@ constexpr int kMaxSplits = 128;
 __global__ void __launch_bounds__(kMergeThreads)
 decode_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int S,
                     float* __restrict__ out) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int64_t t = blockIdx.x;
   const int h = threadIdx.x / (kHeadDim / 4), d0 = 4 * (threadIdx.x % (kHeadDim / 4));
   float M = -INFINITY;
@@ -535,13 +539,12 @@ cudaError_t launch_decode(const uint16_t* q, int64_t T, int Q, const uint8_t* k_
   cudaError_t err =
       cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  decode_split_kernel<<<(unsigned)(T * S), kDecThreads, smem, stream>>>(
-      q, Q, k_pages, v_pages, kv_page_stride, num_pages, block_table, bt_width, seq_lens, topk, kw,
-      scale, S, ws_o, ws_ml, status);
-  err = cudaGetLastError();
+  err = launch_pdl(decode_split_kernel, dim3((unsigned)(T * S)), dim3(kDecThreads), smem, stream,
+                   q, Q, k_pages, v_pages, kv_page_stride, num_pages, block_table, bt_width,
+                   seq_lens, topk, kw, scale, S, ws_o, ws_ml, status);
   if (err != cudaSuccess) return err;
-  decode_merge_kernel<<<(unsigned)T, kMergeThreads, 0, stream>>>(ws_o, ws_ml, S, out);
-  return cudaGetLastError();
+  return launch_pdl(decode_merge_kernel, dim3((unsigned)T), dim3(kMergeThreads), 0, stream,
+                    (const float*)ws_o, (const float*)ws_ml, S, out);
 }
 
 }  // namespace mx4

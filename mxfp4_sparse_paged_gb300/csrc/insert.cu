@@ -43,6 +43,8 @@ insert_kernel(const float* __restrict__ k, const float* __restrict__ v,
               uint8_t* __restrict__ v_pages, int64_t kv_page_stride, int64_t kv_head_stride,
               uint8_t* __restrict__ idx_pages, int64_t idx_page_stride, int64_t num_pages,
               uint32_t* status) {
+  pdl_launch_dependents();
+  pdl_wait();
   const int lane = threadIdx.x & 31;
   const int rows_per_token = 2 * Hkv + 1;  // K heads, V heads, index key
   const int64_t warp = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -111,10 +113,9 @@ cudaError_t launch_insert(const float* k, const float* v, const float* idx_k, in
   const int64_t warps = T * (2 * Hkv + 1);
   const int threads = 256;
   const int64_t blocks = (warps + (threads / 32) - 1) / (threads / 32);
-  insert_kernel<<<(unsigned)blocks, threads, 0, stream>>>(
-      k, v, idx_k, T, Hkv, slot_mapping, k_pages, v_pages, kv_page_stride, kv_head_stride,
-      idx_pages, idx_page_stride, num_pages, status);
-  return cudaGetLastError();
+  return launch_pdl(insert_kernel, dim3((unsigned)blocks), dim3(threads), 0, stream, k, v, idx_k,
+                    T, Hkv, slot_mapping, k_pages, v_pages, kv_page_stride, kv_head_stride,
+                    idx_pages, idx_page_stride, num_pages, status);
 }
 
 }  // namespace mx4

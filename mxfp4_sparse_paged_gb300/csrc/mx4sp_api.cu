@@ -20,7 +20,8 @@ cudaError_t launch_index_score(const uint16_t*, int, const uint8_t*, int64_t, in
                                const int32_t*, int, int64_t, const int32_t*, float*, int64_t,
                                uint32_t*, int, cudaStream_t);
 cudaError_t launch_topk(const float*, int64_t, const int32_t*, int64_t, int, int, int32_t*,
-                        uint32_t*, cudaStream_t);
+                        void*, uint32_t*, int, cudaStream_t);
+size_t topk_workspace_bytes(int64_t, int, int64_t);
 cudaError_t launch_decode(const uint16_t*, int64_t, int, const uint8_t*, const uint8_t*, int64_t,
                           int64_t, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
                           float, float*, void*, uint32_t*, cudaStream_t);
@@ -151,10 +152,7 @@ int index_score(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx
 }
 
 size_t topk_select_workspace(int64_t T, int k, int64_t ld_scores) {
-  (void)T;
-  (void)k;
-  (void)ld_scores;
-  return 0;
+  return mx4::topk_workspace_bytes(T, k, ld_scores);
 }
 
 int topk_select(const float* scores, int64_t ld_scores, const int32_t* seq_lens, int64_t B,
@@ -166,16 +164,22 @@ int topk_select(const float* scores, int64_t ld_scores, const int32_t* seq_lens,
   if (B < 0 || B * q_per_seq > 0x7FFFFFFF)
     return fail(MX4_ERR_INVALID, "topk_select: B = %lld", (long long)B);
   const int64_t T = B * q_per_seq;
-  if (ws_bytes < topk_select_workspace(T, k, ld_scores))
-    return fail(MX4_ERR_WORKSPACE, "topk_select: workspace too small");
-  (void)ws;
+  if (ld_scores < 1) return fail(MX4_ERR_INVALID, "topk_select: ld_scores < 1");
+  if (T > 65535) return fail(MX4_ERR_UNSUPPORTED, "topk_select: %lld tokens (max 65535)", (long long)T);
+  if ((ld_scores + 16383) / 16384 > 512)
+    return fail(MX4_ERR_UNSUPPORTED, "topk_select: ld_scores = %lld (max 8388608)",
+                (long long)ld_scores);
+  const size_t need = topk_select_workspace(T, k, ld_scores);
+  if (ws_bytes < need) return fail(MX4_ERR_WORKSPACE, "topk_select: workspace too small");
+  if (need > 0 && (!ws || !aligned(ws, 16)))
+    return fail(MX4_ERR_INVALID, "topk_select: workspace NULL or not 16-byte aligned");
   if (T == 0) return ok();
   if (!scores || !seq_lens || !topk_idx) return fail(MX4_ERR_INVALID, "topk_select: NULL pointer");
-  if (ld_scores < 1) return fail(MX4_ERR_INVALID, "topk_select: ld_scores < 1");
   DeviceInfo* d;
   if (int rc = device_info(&d)) return rc;
   return cuda_result(mx4::launch_topk(scores, ld_scores, seq_lens, T, q_per_seq, k, topk_idx,
-                                      d->status, static_cast<cudaStream_t>(stream)),
+                                      need > 0 ? ws : nullptr, d->status, d->num_sms,
+                                      static_cast<cudaStream_t>(stream)),
                      "topk_select");
 }
 

@@ -141,6 +141,7 @@ class DecodeStep:
             self.scale, self.out, self.dec_ws, stream=stream))
 
     def launches_per_step(self) -> int:
-        """Kernels this library launches per step (insert, score, top-k, decode split +
-        merge)."""
-        return (1 if self.slots.numel() else 0) + 1 + 1 + 2
+        """Kernels this library launches per step: insert, score, top-k (threshold and
+        segment filter when rows can exceed the candidate capacity, then select), decode
+        split + merge."""
+        return (1 if self.slots.numel() else 0) + 1 + (3 if self.topk_ws is not None else 1) + 2

@@ -95,4 +95,9 @@ def test_workspace_sizes(lib):
     # 16 heads x (128 outputs + max + sum) fp32 per (token, split of 512 selected)
     assert m.sparse_paged_decode_workspace(64, 2048) == 64 * 4 * 16 * 130 * 4
     assert m.sparse_paged_decode_workspace(1, 1) == 16 * 130 * 4
-    assert m.topk_select_workspace(64, 2048, 131072) >= 0
+    # count [T] | threshold [T] | (offset, count) per 16384-score segment | kCand = 8192
+    # keys and indices, each section padded to 16 bytes
+    assert m.topk_select_workspace(64, 2048, 131072) == 2 * 64 * 4 + 64 * 8 * 8 + 2 * 64 * 8192 * 4
+    assert m.topk_select_workspace(3, 2048, 20000) == 2 * 16 + 48 + 2 * 3 * 8192 * 4
+    assert m.topk_select_workspace(64, 2048, 8192) == 0      # no row exceeds the capacity
+    assert m.topk_select_workspace(64, 9000, 131072) == 0    # k above the capacity

@@ -235,6 +235,38 @@ def test_topk_bit_exact_on_shared_scores():
         assert np.array_equal(out.cpu().numpy(), want), f"k={k}"
 
 
+def test_topk_segment_filter_paths():
+    # Rows longer than one filter segment: candidates spread evenly, concentrated
+    # in the last segment (recency-biased scores), all in one segment, k above the
+    # candidate capacity (workspace-free exact path), and an odd row stride
+    # (scalar loads).
+    rng = np.random.default_rng(11)
+    lens = np.array([40000, 131072, 70001, 16385, 99999, 8193], np.int32)
+    B, q = len(lens), 1
+    for ld_pad, ks in ((0, (2048, 9000)), (1, (2048,))):
+        ld = int(lens.max()) + ld_pad
+        sc = np.full((B, ld), -np.inf, np.float32)
+        for t in range(B):
+            n = int(lens[t])
+            row = rng.standard_normal(n).astype(np.float32)
+            if t % 3 == 1:
+                row += np.linspace(0, 6, n, dtype=np.float32)      # recency bias
+            elif t % 3 == 2:
+                a = rng.integers(0, max(1, n - 3000))
+                row[a:a + 3000] += 8                               # one hot window
+            sc[t, :n] = row
+        d_sc = torch.from_numpy(sc).to(DEV)
+        d_lens = torch.from_numpy(lens).to(DEV)
+        for k in ks:
+            want = oracle.topk_select(sc.astype(np.float64), lens, q, k)
+            out = torch.empty((B, k), dtype=torch.int32, device=DEV)
+            ws_n = m.topk_select_workspace(B, k, ld)
+            ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=DEV)
+            m.topk_select(d_sc, d_lens, q, k, out, ws)
+            m.mx4_check_status()
+            assert np.array_equal(out.cpu().numpy(), want), f"k={k} ld={ld}"
+
+
 # ----------------------------------------------------------------- decode edges
 
 def test_decode_single_selected_token_is_exact_value_row():
