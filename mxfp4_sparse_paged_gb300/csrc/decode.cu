@@ -10,23 +10,24 @@
 // heads the M = 16 side of a tensor-core MMA.
 //
 // split kernel -- one CTA of 8 warps per (decode token, split of up to 512
-// selected entries):
-//   1. Load the split's indices, the sequence's block-table row (into shared
-//      memory) and Q, all at once.  Resolve every entry to its page row and
-//      issue, in one batch, cp.async gathers of its 64 B of K data, 64 B of V
-//      data and the two 4-byte scale words into shared memory (rows padded to
-//      80 B so the fragment loads are bank-conflict free).
-//   2. From the staged scale words: the split's largest K scale (all blocks)
-//      and V scale (per 32-dim block), and for every entry exact f16
-//      multipliers 2^(scale - reference), so dequantised K/V values fit f16.
-//   3. Each warp computes its four 16-entry tiles: e2m1 -> f16 with the
-//      hardware cvt (exact grid values) times the multiplier; S = Q K^T with
-//      mma.sync m16n8k16 (Q = 16 heads x 128 in f16, scaled by a power of two
-//      so bf16 fits exactly); online softmax in fp32 (log2 units, lazy
-//      rescaling; weights scaled by 2^7 so the f16 P stays normal); P split into
-//      f16 hi + lo parts so P V keeps ~22 bits; O += P V with mma.sync, V
-//      fragments built by zipping the nibbles of two tokens so one cvt yields a
-//      (token, token) pair.
+// selected entries); warp w owns the 16-entry tiles w, w+8, w+16, w+24:
+//   1. The sequence's block-table row goes to shared memory and warp 0 turns Q
+//      into f16 MMA A fragments (bf16 scaled by a power of two, exact), kept in
+//      shared memory.  Each warp then resolves its tiles' entries to page rows
+//      and issues the gathers of all their scale words (one cp.async group),
+//      then of each tile's 64 B K and V rows (one group per tile; rows padded
+//      to 80 B so the fragment loads are bank-conflict free).
+//   2. When the scale words land, the warp derives, for its 64 entries, the V
+//      reference per 32-dim block (largest scale byte), K factors
+//      2^(scale - 127) and exact f16 V multipliers 2^(scale - reference).
+//   3. Each tile is processed as soon as its rows land, with no block-wide
+//      step: S = Q K^T with mma.sync m16n8k16 (K = hardware e2m1 -> f16,
+//      exact), one accumulator per 32-dim scale block, so the K scales are
+//      applied exactly in fp32; online softmax in fp32 (log2 units, lazy
+//      rescaling; weights scaled by 2^7 so the f16 P stays normal); P split
+//      into f16 hi + lo parts so P V keeps ~22 bits; O += P V with mma.sync, V
+//      fragments built by zipping the nibbles of two entries so one cvt yields
+//      an (entry, entry) pair, times the V multipliers.
 //   4. The 8 warps' (max, sum, O) are merged in shared memory, in the MMA
 //      fragment order (bank-conflict free), and the split writes its
 //      unnormalised [head][dim] output plus its running max (log2 units) and
@@ -44,28 +45,28 @@ constexpr int kTile = 16;                           // entries per MMA tile
 constexpr int kTiles = kSplitTokens / kTile;        // 32
 constexpr int kTilesPerWarp = kTiles / kDecWarps;   // 4
 constexpr int kRowPitch = 80;                       // staged row pitch (64 B + 16 B pad)
-constexpr int kStageBytes = 2 * kTile * kRowPitch;  // K rows then V rows: 2560 B
+constexpr int kTileV = kTile * kRowPitch;           // V rows follow the K rows
+constexpr int kTileSw = 2 * kTile * kRowPitch;      // then 16 K and 16 V scale words
+constexpr int kTileBytes = kTileSw + 2 * kTile * 4; // 2688 B
 constexpr int kBtCache = 2048;                      // block-table entries kept in smem
 constexpr int kFrag = kHeads * kHeadDim;            // 2048 outputs per split
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 128.f;  // p' = 2^(logit - m) * 2^7, at most 2^15 in f16
 constexpr float kLazy = 8.f;      // rescale only when the max grows by more than this
-static_assert(kTilesPerWarp * kDecWarps == kTiles, "split geometry");
-static_assert(2 * kDecThreads == kSplitTokens, "one entry pair per thread in the set-up phase");
-static_assert(kDecWarps * kFrag * 4 <= kTiles * kStageBytes, "merge buffer fits in the stage");
+static_assert(kTilesPerWarp * kDecWarps == kTiles && kTilesPerWarp == 4, "split geometry");
+static_assert(kTileBytes % 16 == 0, "16-byte aligned tiles");
+static_assert(kDecWarps * kFrag * 4 <= kDecWarps * kTilesPerWarp * kTileBytes,
+              "merge buffer fits in the tiles");
 
 struct DecodeSmem {
-  uint8_t stage[kTiles][kStageBytes];  // 80 KB; reused by the final merge
-  uint32_t kmul[kSplitTokens][4];      // f16x2 (m, m): K multiplier of block b of entry r
-  uint32_t vmul[kSplitTokens / 2][4];  // f16x2 (m_2u, m_2u+1), blocks in slot order 0,2,1,3
-  uint32_t ksw[kSplitTokens];          // staged K scale words
-  uint32_t vsw[kSplitTokens];          // staged V scale words
-  int32_t bt[kBtCache];                // the sequence's block-table row
-  uint8_t ok[kSplitTokens];
+  uint8_t tile[kDecWarps][kTilesPerWarp][kTileBytes];  // 84 KB; reused by the final merge
+  uint4 qfrag[8][32];                                  // Q A fragments, per k16 slice and lane
+  float4 kf[kDecWarps][kTilesPerWarp][kTile];          // K scale factors 2^(s_b - 127) * cQ
+  uint16_t vm16[kDecWarps][kTilesPerWarp][4][kTile];   // f16 V multipliers [tile][block][entry]
+  int32_t bt[kBtCache];                                // the sequence's block-table row
   float red_m[kDecWarps][kHeads];
   float red_l[kDecWarps][kHeads];
-  uint32_t red_k[kDecWarps];
-  uint32_t red_v[kDecWarps];
+  int sigma;
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -77,7 +78,12 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
                "r"(valid ? 4 : 0));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
+// wait until at most N of this thread's cp.async groups are pending
+template <int N>
+__device__ __forceinline__ void cp_async_wait_pending() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
 
 __device__ __forceinline__ uint32_t hmul2(uint32_t a, uint32_t b) {
   uint32_t d;
@@ -110,11 +116,6 @@ __device__ __forceinline__ uint32_t f16_pow2(uint32_t byte, uint32_t ref) {
   return 0u;
 }
 
-__device__ __forceinline__ uint32_t max_byte(uint32_t w) {
-  w = __vmaxu4(w, w >> 16);
-  w = __vmaxu4(w, w >> 8);
-  return w & 0xFFu;
-}
 // bytes equal to 0xFF (NaN scales) do not take part in the reference maximum
 __device__ __forceinline__ uint32_t drop_nan_bytes(uint32_t w) {
   return w & ~__vcmpeq4(w, 0xFFFFFFFFu);
@@ -140,70 +141,19 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   const int begin = sp * kSplitTokens;
   const int cnt = max(0, min(kSplitTokens, kw - begin));
 
-  // ---- 1a. block-table row, Q, then (after the top-k kernel) the indices
+  // ---- 1a. block-table row; Q as f16 A fragments (warp 0), scaled by 2^sigma
+  // so that bf16 fits f16 exactly
   const int64_t npg = min(bt_width, max((int64_t)0, p / kPageTokens + 1));
   for (int j = tid; j < min(npg, (int64_t)kBtCache); j += kDecThreads)
     s.bt[j] = block_table[seq * bt_width + j];
-  uint4 qraw[2][4];
+  if (warp == 0) {
+    uint4 qraw[2][4];
 #pragma unroll
-  for (int hh = 0; hh < 2; ++hh)
+    for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
-    for (int b = 0; b < 4; ++b)
-      qraw[hh][b] = *reinterpret_cast<const uint4*>(
-          q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
-  pdl_wait();  // top-k indices and pages are touched from here on
-  int32_t idx[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = 2 * tid + e;
-    idx[e] = (r < cnt) ? topk[t * kw + begin + r] : -1;
-  }
-  __syncthreads();
-
-  // ---- 1b. resolve entries, gather rows and scale words (one cp.async batch)
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    const int r = 2 * tid + e;
-    const int32_t i = idx[e];
-    bool ok = false;
-    const uint8_t* kp = k_pages;
-    const uint8_t* vp = v_pages;
-    if (i >= 0) {
-      if (i > p || (int64_t)i / kPageTokens >= bt_width) {
-        flag(status, MX4_STATUS_BAD_INDEX);
-      } else {
-        const int64_t slot = i / kPageTokens;
-        const int32_t pid =
-            slot < kBtCache ? s.bt[slot] : block_table[seq * bt_width + slot];
-        if (pid < 0 || pid >= num_pages) {
-          flag(status, MX4_STATUS_BAD_PAGE);
-        } else {
-          const int64_t pg = (int64_t)pid * kv_page_stride;
-          kp = k_pages + pg;
-          vp = v_pages + pg;
-          ok = true;
-        }
-      }
-    }
-    s.ok[r] = ok;
-    const int row = ok ? (i % kPageTokens) : 0;
-    const uint32_t dk = smem_addr(&s.stage[r / kTile][(r % kTile) * kRowPitch]);
-    const uint32_t dv = dk + kTile * kRowPitch;
-#pragma unroll
-    for (int c = 0; c < 4; ++c) {
-      cp_async16(dk + 16 * c, kp + row * kRowDataBytes + 16 * c, ok);
-      cp_async16(dv + 16 * c, vp + row * kRowDataBytes + 16 * c, ok);
-    }
-    cp_async4(smem_addr(&s.ksw[r]), kp + kScaleOffset + row * kRowScaleBytes, ok);
-    cp_async4(smem_addr(&s.vsw[r]), vp + kScaleOffset + row * kRowScaleBytes, ok);
-  }
-  cp_async_commit();
-
-  // ---- Q as f16 A fragments (while the gathers are in flight), scaled by
-  // 2^sigma so that bf16 fits f16 exactly
-  uint32_t qa[8][4];
-  int sigma;
-  {
+      for (int b = 0; b < 4; ++b)
+        qraw[hh][b] = *reinterpret_cast<const uint4*>(
+            q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
     uint32_t amax = 0;
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh)
@@ -218,7 +168,7 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
       }
     amax = __reduce_max_sync(0xFFFFFFFFu, amax);
     const int e = (int)(amax >> 23) - 127;
-    sigma = (amax == 0u) ? 0 : min(127, max(-126, 14 - e));
+    const int sigma = (amax == 0u) ? 0 : min(127, max(-126, 14 - e));
     const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
 #pragma unroll
     for (int b = 0; b < 4; ++b)
@@ -227,121 +177,154 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
         // slice 2b+h: k = 2tig,2tig+1 <-> dims 32b+8tig+4h+{0,1}; k = 2tig+8,+9 <-> +{2,3}
         const uint32_t w0 = h ? qraw[0][b].z : qraw[0][b].x, w1 = h ? qraw[0][b].w : qraw[0][b].y;
         const uint32_t u0 = h ? qraw[1][b].z : qraw[1][b].x, u1 = h ? qraw[1][b].w : qraw[1][b].y;
-        qa[2 * b + h][0] = pack_f16x2(bf16_bits_to_float(w0 & 0xFFFFu) * sc,
-                                      bf16_bits_to_float(w0 >> 16) * sc);
-        qa[2 * b + h][1] = pack_f16x2(bf16_bits_to_float(u0 & 0xFFFFu) * sc,
-                                      bf16_bits_to_float(u0 >> 16) * sc);
-        qa[2 * b + h][2] = pack_f16x2(bf16_bits_to_float(w1 & 0xFFFFu) * sc,
-                                      bf16_bits_to_float(w1 >> 16) * sc);
-        qa[2 * b + h][3] = pack_f16x2(bf16_bits_to_float(u1 & 0xFFFFu) * sc,
-                                      bf16_bits_to_float(u1 >> 16) * sc);
+        s.qfrag[2 * b + h][lane] = make_uint4(
+            pack_f16x2(bf16_bits_to_float(w0 & 0xFFFFu) * sc, bf16_bits_to_float(w0 >> 16) * sc),
+            pack_f16x2(bf16_bits_to_float(u0 & 0xFFFFu) * sc, bf16_bits_to_float(u0 >> 16) * sc),
+            pack_f16x2(bf16_bits_to_float(w1 & 0xFFFFu) * sc, bf16_bits_to_float(w1 >> 16) * sc),
+            pack_f16x2(bf16_bits_to_float(u1 & 0xFFFFu) * sc, bf16_bits_to_float(u1 >> 16) * sc));
       }
+    if (lane == 0) s.sigma = sigma;
   }
-  cp_async_wait_all();
-  __syncthreads();
+  pdl_wait();  // top-k indices and pages are touched from here on
 
-  // ---- 2. split references and per-entry multipliers
-  {
-    uint32_t kmax = 0, vmax4 = 0;
+  // ---- 1b. this warp's entries: lane l takes entry l/2 of each tile, its K row
+  // and K scale word (even l) or its V row and V scale word (odd l)
+  const int r = lane >> 1;
+  const bool isv = (lane & 1) != 0;
+  int32_t idx[kTilesPerWarp];
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      const int r = 2 * tid + e;
-      if (s.ok[r]) {
-        kmax = max(kmax, max_byte(drop_nan_bytes(s.ksw[r])));
-        vmax4 = __vmaxu4(vmax4, drop_nan_bytes(s.vsw[r]));
+  for (int u = 0; u < kTilesPerWarp; ++u) {
+    const int e = (warp + kDecWarps * u) * kTile + r;
+    idx[u] = (e < cnt) ? topk[t * kw + begin + e] : -1;
+  }
+  __syncthreads();  // block-table row and Q fragments
+  uint32_t okm[kTilesPerWarp];
+  int rows[kTilesPerWarp];
+  const uint8_t* srcs[kTilesPerWarp];
+#pragma unroll
+  for (int u = 0; u < kTilesPerWarp; ++u) {
+    const int32_t i = idx[u];
+    bool ok = false;
+    const uint8_t* src = isv ? v_pages : k_pages;
+    if (i >= 0) {
+      if (i > p || (int64_t)i / kPageTokens >= bt_width) {
+        flag(status, MX4_STATUS_BAD_INDEX);
+      } else {
+        const int64_t slot = i / kPageTokens;
+        const int32_t pid = slot < kBtCache ? s.bt[slot] : block_table[seq * bt_width + slot];
+        if (pid < 0 || pid >= num_pages) {
+          flag(status, MX4_STATUS_BAD_PAGE);
+        } else {
+          src += (int64_t)pid * kv_page_stride;
+          ok = true;
+        }
       }
     }
-    kmax = __reduce_max_sync(0xFFFFFFFFu, kmax);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-      vmax4 = __vmaxu4(vmax4, __shfl_xor_sync(0xFFFFFFFFu, vmax4, o));
-    if (lane == 0) {
-      s.red_k[warp] = kmax;
-      s.red_v[warp] = vmax4;
-    }
+    rows[u] = ok ? (i % kPageTokens) : -1;
+    srcs[u] = src;
+    okm[u] = __ballot_sync(0xFFFFFFFFu, ok);  // bit 2e: entry e of the tile is valid
+    cp_async4(smem_addr(&s.tile[warp][u][0]) + kTileSw + (isv ? kTile * 4 : 0) + r * 4,
+              src + kScaleOffset + (ok ? rows[u] : 0) * kRowScaleBytes, ok);
   }
-  __syncthreads();
-  uint32_t refK = 0, refV4 = 0;
+  cp_async_commit();  // group: the scale words of all four tiles
 #pragma unroll
-  for (int w = 0; w < kDecWarps; ++w) {
-    refK = max(refK, s.red_k[w]);
-    refV4 = __vmaxu4(refV4, s.red_v[w]);
+  for (int u = 0; u < kTilesPerWarp; ++u) {
+    const bool ok = rows[u] >= 0;
+    const uint32_t dst = smem_addr(&s.tile[warp][u][0]) + (isv ? kTileV : 0) + r * kRowPitch;
+    const uint8_t* src = srcs[u] + (ok ? rows[u] : 0) * kRowDataBytes;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) cp_async16(dst + 16 * c, src + 16 * c, ok);
+    cp_async_commit();  // group: the K and V rows of tile u
   }
-  {
-    const bool ok0 = s.ok[2 * tid], ok1 = s.ok[2 * tid + 1];
-    const uint32_t k0 = s.ksw[2 * tid], k1 = s.ksw[2 * tid + 1];
-    const uint32_t v0 = s.vsw[2 * tid], v1 = s.vsw[2 * tid + 1];
-    uint32_t km0[4], km1[4], vm[4];
+
+  // logit (log2 units) = sum_b S_b * 2^(scale_b - 127) * cQ
+  const float cQ = ldexpf(scale * kLog2e, -s.sigma);
+
+  // ---- 1c. scale tables of the warp's 64 entries (while the rows are in flight):
+  // the V reference per 32-dim block (largest valid scale byte, NaN excluded),
+  // K factors 2^(s_b - 127) * cQ and f16 V multipliers 2^(s_b - ref_b)
+  cp_async_wait_pending<kTilesPerWarp>();
+  __syncwarp();
+  uint32_t refV = 0u;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint32_t m0 = ok0 ? f16_pow2((k0 >> (8 * b)) & 0xFFu, refK) : 0u;
-      const uint32_t m1 = ok1 ? f16_pow2((k1 >> (8 * b)) & 0xFFu, refK) : 0u;
-      km0[b] = m0 | (m0 << 16);
-      km1[b] = m1 | (m1 << 16);
-    }
-#pragma unroll
-    for (int slot = 0; slot < 4; ++slot) {
-      const int b = (slot >> 1) + 2 * (slot & 1);  // slot order 0, 2, 1, 3
-      const uint32_t ref = (refV4 >> (8 * b)) & 0xFFu;
-      const uint32_t m0 = ok0 ? f16_pow2((v0 >> (8 * b)) & 0xFFu, ref) : 0u;
-      const uint32_t m1 = ok1 ? f16_pow2((v1 >> (8 * b)) & 0xFFu, ref) : 0u;
-      vm[slot] = m0 | (m1 << 16);
-    }
-    *reinterpret_cast<uint4*>(&s.kmul[2 * tid][0]) = make_uint4(km0[0], km0[1], km0[2], km0[3]);
-    *reinterpret_cast<uint4*>(&s.kmul[2 * tid + 1][0]) =
-        make_uint4(km1[0], km1[1], km1[2], km1[3]);
-    *reinterpret_cast<uint4*>(&s.vmul[tid][0]) = make_uint4(vm[0], vm[1], vm[2], vm[3]);
+  for (int h = 0; h < 2; ++h) {
+    const int u = (lane >> 4) + 2 * h, er = lane & 15;  // entries lane and lane + 32
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(&s.tile[warp][u][kTileSw]);
+    if ((okm[u] >> (2 * er)) & 1u) refV = __vmaxu4(refV, drop_nan_bytes(sw[kTile + er]));
   }
-  __syncthreads();
-  // logit (log2 units) = S * cK
-  const float cK = ldexpf(scale * kLog2e, (int)refK - 127 - sigma);
+#pragma unroll
+  for (int of = 16; of > 0; of >>= 1) refV = __vmaxu4(refV, __shfl_xor_sync(0xFFFFFFFFu, refV, of));
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    const int u = (lane >> 4) + 2 * h, er = lane & 15;
+    const uint32_t* sw = reinterpret_cast<const uint32_t*>(&s.tile[warp][u][kTileSw]);
+    const uint32_t kw4 = sw[er], vw4 = sw[kTile + er];
+    s.kf[warp][u][er] = make_float4(e8m0_to_float(kw4 & 0xFFu) * cQ,
+                                    e8m0_to_float((kw4 >> 8) & 0xFFu) * cQ,
+                                    e8m0_to_float((kw4 >> 16) & 0xFFu) * cQ,
+                                    e8m0_to_float(kw4 >> 24) * cQ);
+#pragma unroll
+    for (int b = 0; b < 4; ++b)
+      s.vm16[warp][u][b][er] =
+          (uint16_t)f16_pow2((vw4 >> (8 * b)) & 0xFFu, (refV >> (8 * b)) & 0xFFu);
+  }
+  __syncwarp();
 
   // ---- 3. this warp's tiles
-  const int n_tiles = (cnt + kTile - 1) / kTile;
   float o[16][4];
 #pragma unroll
   for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
   float m_used[2] = {-INFINITY, -INFINITY};
   float lsum[2] = {0.f, 0.f};
 
+#pragma unroll
   for (int u = 0; u < kTilesPerWarp; ++u) {
-    const int tile = warp + kDecWarps * u;
-    if (tile >= n_tiles) break;
-    const uint8_t* sk = &s.stage[tile][0];
-    const uint8_t* sv = sk + kTile * kRowPitch;
-    const int tb = tile * kTile;
+    if ((warp + kDecWarps * u) * kTile >= cnt) break;
+    if (u == 0) cp_async_wait_pending<3>();  // row groups of tiles u+1 .. 3 may be pending
+    else if (u == 1) cp_async_wait_pending<2>();
+    else if (u == 2) cp_async_wait_pending<1>();
+    else cp_async_wait_pending<0>();
+    __syncwarp();
+    const uint8_t* sk = &s.tile[warp][u][0];
+    const uint8_t* sv = sk + kTileV;
+    const uint16_t* vm = &s.vm16[warp][u][0][0];
+    const uint32_t okb = okm[u];
 
-    // S = Q K^T for tokens tb .. tb+15 (two n8 tiles)
-    float c[2][4];
+    // S = Q K^T per 32-dim scale block, two n8 tiles of entries
+    float acc[2][4][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
-      const uint8_t* row = sk + (nt * 8 + g) * kRowPitch;
-      const uint4 km = *reinterpret_cast<const uint4*>(&s.kmul[tb + nt * 8 + g][0]);
-      const uint32_t kmb[4] = {km.x, km.y, km.z, km.w};
+    for (int b = 0; b < 4; ++b) {
+      const uint4 qa0 = s.qfrag[2 * b][lane], qa1 = s.qfrag[2 * b + 1][lane];
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
+      for (int nt = 0; nt < 2; ++nt) {
+        acc[nt][b][0] = acc[nt][b][1] = acc[nt][b][2] = acc[nt][b][3] = 0.f;
         uint32_t f[4];
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(row + (4 * b + tig) * 4), f);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) f[j] = hmul2(f[j], kmb[b]);
-        mma_m16n8k16_f16(c[nt], qa[2 * b][0], qa[2 * b][1], qa[2 * b][2], qa[2 * b][3], f[0], f[1]);
-        mma_m16n8k16_f16(c[nt], qa[2 * b + 1][0], qa[2 * b + 1][1], qa[2 * b + 1][2], qa[2 * b + 1][3],
-                f[2], f[3]);
+        e2m1x8_to_f16x2(
+            *reinterpret_cast<const uint32_t*>(sk + (nt * 8 + g) * kRowPitch + (4 * b + tig) * 4),
+            f);
+        mma_m16n8k16_f16(acc[nt][b], qa0.x, qa0.y, qa0.z, qa0.w, f[0], f[1]);
+        mma_m16n8k16_f16(acc[nt][b], qa1.x, qa1.y, qa1.z, qa1.w, f[2], f[3]);
       }
     }
-    // logits, masked entries -> -inf
-    const uint16_t ok01 = *reinterpret_cast<const uint16_t*>(&s.ok[tb + 2 * tig]);
-    const uint16_t ok89 = *reinterpret_cast<const uint16_t*>(&s.ok[tb + 8 + 2 * tig]);
+    // logits of this thread's entries nt*8 + 2 tig + cc (heads g and g + 8)
     float lg[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      const uint16_t okw = nt ? ok89 : ok01;
-      lg[nt][0] = (okw & 0x00FF) ? c[nt][0] * cK : -INFINITY;
-      lg[nt][1] = (okw & 0xFF00) ? c[nt][1] * cK : -INFINITY;
-      lg[nt][2] = (okw & 0x00FF) ? c[nt][2] * cK : -INFINITY;
-      lg[nt][3] = (okw & 0xFF00) ? c[nt][3] * cK : -INFINITY;
-    }
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int cc = 0; cc < 2; ++cc) {
+        const int en = nt * 8 + 2 * tig + cc;
+        const float4 kf = s.kf[warp][u][en];
+        const float f[4] = {kf.x, kf.y, kf.z, kf.w};
+        float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          d0 = fmaf(acc[nt][b][cc], f[b], d0);
+          d1 = fmaf(acc[nt][b][cc + 2], f[b], d1);
+        }
+        const bool valid = (okb >> (2 * en)) & 1u;
+        lg[nt][cc] = valid ? d0 : -INFINITY;
+        lg[nt][cc + 2] = valid ? d1 : -INFINITY;
+      }
     float mx[2];
     mx[0] = fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1]));
     mx[1] = fmaxf(fmaxf(lg[0][2], lg[0][3]), fmaxf(lg[1][2], lg[1][3]));
@@ -392,13 +375,13 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
     pl[2] = pack_f16x2(pw[1][0] - f16_lo(ph[2]), pw[1][1] - f16_hi(ph[2]));
     pl[3] = pack_f16x2(pw[1][2] - f16_lo(ph[3]), pw[1][3] - f16_hi(ph[3]));
 
-    // O += P V: dim tile j = 8h + i, column g <-> dim 8(g + 8h) + i
-    const uint2 vm01 = *reinterpret_cast<const uint2*>(&s.vmul[(tb >> 1) + tig][(g >> 2) * 2]);
-    const uint2 vm89 =
-        *reinterpret_cast<const uint2*>(&s.vmul[(tb >> 1) + 4 + tig][(g >> 2) * 2]);
+    // O += P V: dim tile j = 8h + i, column g <-> dim 8(g + 8h) + i (block (g>>2) + 2h)
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       const int wi = (g + 8 * h) * 4;
+      const int bh = (g >> 2) + 2 * h;
+      const uint32_t m01 = *reinterpret_cast<const uint32_t*>(&vm[bh * kTile + 2 * tig]);
+      const uint32_t m89 = *reinterpret_cast<const uint32_t*>(&vm[bh * kTile + 8 + 2 * tig]);
       const uint32_t wA = *reinterpret_cast<const uint32_t*>(sv + (2 * tig) * kRowPitch + wi);
       const uint32_t wB = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 1) * kRowPitch + wi);
       const uint32_t wC = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 8) * kRowPitch + wi);
@@ -409,8 +392,6 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
       e2m1x8_to_f16x2(lop_merge(wA >> 4, wB, 0x0F0F0F0Fu), zo01);
       e2m1x8_to_f16x2(lop_merge(wC, wD << 4, 0x0F0F0F0Fu), ze89);
       e2m1x8_to_f16x2(lop_merge(wC >> 4, wD, 0x0F0F0F0Fu), zo89);
-      const uint32_t m01 = h ? vm01.y : vm01.x;
-      const uint32_t m89 = h ? vm89.y : vm89.x;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const uint32_t b0 = hmul2((i & 1) ? zo01[i >> 1] : ze01[i >> 1], m01);
@@ -420,6 +401,7 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
       }
     }
   }
+  cp_async_wait_all();  // gathers of tiles past the end land before the merge reuses them
 
   // ---- 4. merge the warps' partial results (fragment order, conflict free)
 #pragma unroll
@@ -427,7 +409,7 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
     lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 1);
     lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 2);
   }
-  __syncthreads();  // every warp is done with the staged rows
+  __syncthreads();  // every warp is done with its tiles
   if (tig == 0) {
     s.red_m[warp][g] = m_used[0];
     s.red_m[warp][g + 8] = m_used[1];
@@ -447,9 +429,9 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
     fw[rr] = (m_used[rr] == -INFINITY) ? 0.f : exp2f(m_used[rr] - M[rr]);
   float fv[4];
 #pragma unroll
-  for (int b = 0; b < 4; ++b) fv[b] = ldexpf(1.f, (int)((refV4 >> (8 * b)) & 0xFFu) - 127);
+  for (int b = 0; b < 4; ++b) fv[b] = ldexpf(1.f, (int)((refV >> (8 * b)) & 0xFFu) - 127);
   // element (j, c) of lane l lives at red[warp][(4 j + c) * 32 + l]
-  float* red = reinterpret_cast<float*>(&s.stage[0][0]);
+  float* red = reinterpret_cast<float*>(&s.tile[0][0][0]);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float f = fv[(2 * tig + 8 * (j >> 3)) >> 2];

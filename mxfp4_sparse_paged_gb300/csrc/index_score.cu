@@ -13,7 +13,7 @@
 //
 // Pipeline: warp 8 is the producer.  It resolves pages through the block table
 // (32 lanes at a time) and streams each 8704-byte page, plus the sequence's
-// index-q rows, into a 4-stage shared-memory ring with bulk copies (TMA engine)
+// index-q rows, into a 5-stage shared-memory ring with bulk copies (TMA engine)
 // that complete on the stage's "full" mbarrier.  Warps 0-7 consume: each takes
 // one 16-row tile of the page.
 //
@@ -30,7 +30,7 @@ namespace mx4 {
 
 constexpr int kScoreConsumers = 8;
 constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;
-constexpr int kScoreStages = 4;
+constexpr int kScoreStages = 5;
 constexpr int kMaxQ = 8;
 constexpr int kStageIqBytes = kMaxQ * kHeadDim * 2;
 constexpr int kScoreStageBytes = kPageBytes + kStageIqBytes;  // 10752, a multiple of 16
@@ -232,12 +232,9 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
         const uint32_t sy =
             *reinterpret_cast<const uint32_t*>(page + kScaleOffset + (r0 + g + 8) * 4);
         const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
-        // two independent accumulation chains (even / odd k16 slices)
-        float c[NT][4], c2[NT][4];
+        float c[NT][4];
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) c[nt][e] = c2[nt][e] = 0.f;
+        for (int nt = 0; nt < NT; ++nt) c[nt][0] = c[nt][1] = c[nt][2] = c[nt][3] = 0.f;
 #pragma unroll
         for (int wi = 0; wi < 4; ++wi) {
           uint32_t fx[4], fy[4];
@@ -247,14 +244,10 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
           for (int nt = 0; nt < NT; ++nt) {
             mma_m16n8k16_f16(c[nt], fx[0], fy[0], fx[1], fy[1], breg[nt][2 * wi][0],
                              breg[nt][2 * wi][1]);
-            mma_m16n8k16_f16(c2[nt], fx[2], fy[2], fx[3], fy[3], breg[nt][2 * wi + 1][0],
+            mma_m16n8k16_f16(c[nt], fx[2], fy[2], fx[3], fy[3], breg[nt][2 * wi + 1][0],
                              breg[nt][2 * wi + 1][1]);
           }
         }
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) c[nt][e] += c2[nt][e];
         const int b0 = 2 * (tig & 1);
         const float sx0 = e8m0_to_float((sx >> (8 * b0)) & 0xFFu);
         const float sx1 = e8m0_to_float((sx >> (8 * b0 + 8)) & 0xFFu);
@@ -309,7 +302,7 @@ cudaError_t launch_index_score(const uint16_t* iq, int q, const uint8_t* idx_pag
                                const int32_t* block_table, int B, int64_t bt_width,
                                const int32_t* seq_lens, float* scores, int64_t ld,
                                uint32_t* status, int num_sms, cudaStream_t stream) {
-  const int grid = num_sms * 4;  // 4 CTAs of ~51 KB shared memory per SM
+  const int grid = num_sms * 3;  // 3 CTAs of ~62 KB shared memory per SM
   switch (q) {
     case 1: return launch_q<1>(grid, iq, idx_pages, idx_page_stride, num_pages, block_table, B,
                                bt_width, seq_lens, scores, ld, status, stream);
