@@ -191,7 +191,7 @@ def run_gpu(args):
         # Write a buffer twice the L2 size, then read it back: the read evicts the
         # written lines, so their write-back lands here rather than in the step.
         flush.fill_(v)
-        flush.view(torch.int32).sum()
+        flush.view(torch.int64).sum()
     ab = W.algorithmic_bytes(wl)
 
     # The in-step insert rewrites the decode tokens' rows with the same values, so
