@@ -11,11 +11,11 @@
 // shared memory maps a flat page number to (sequence, page)).  All q decode
 // tokens of a sequence are scored in one pass over its pages.
 //
-// Pipeline: warp 8 is the producer.  It resolves pages through the block table
+// Pipeline: warp 4 is the producer.  It resolves pages through the block table
 // (32 lanes at a time) and streams each 8704-byte page, plus the sequence's
-// index-q rows, into a 5-stage shared-memory ring with bulk copies (TMA engine)
-// that complete on the stage's "full" mbarrier.  Warps 0-7 consume: each takes
-// one 16-row tile of the page.
+// index-q rows, into a 4-stage shared-memory ring with bulk copies (TMA engine)
+// that complete on the stage's "full" mbarrier.  Warps 0-3 consume: each takes
+// two 16-row tiles of the page.  Four CTAs run per SM.
 //
 // Math (per tile, tensor cores): A = 16 index-key rows x 128 dims, decoded by
 // the hardware e2m1 -> f16 conversion (exact); thread t of a quad owns the 32
@@ -28,9 +28,9 @@
 
 namespace mx4 {
 
-constexpr int kScoreConsumers = 8;
+constexpr int kScoreConsumers = 4;
 constexpr int kScoreThreads = (kScoreConsumers + 1) * 32;
-constexpr int kScoreStages = 5;
+constexpr int kScoreStages = 4;
 constexpr int kMaxQ = 8;
 constexpr int kStageIqBytes = kMaxQ * kHeadDim * 2;
 constexpr int kScoreStageBytes = kPageBytes + kStageIqBytes;  // 10752, a multiple of 16
@@ -48,7 +48,12 @@ struct ScoreSmem {
   unsigned long long full[kScoreStages];
   unsigned long long empty[kScoreStages];
   volatile int abort_flag;
+  int issued;  // pages whose copies (or bare arrival) the producer has issued
 };
+
+__device__ __forceinline__ float e8m0_fast(uint32_t word, uint32_t sel) {
+  return fmaxf(__uint_as_float(__byte_perm(word, 0u, sel) >> 1), 0x1p-127f);
+}
 
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
@@ -102,6 +107,7 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
       mbar_init(smem_addr(&s.empty[i]), kScoreConsumers);
     }
     s.abort_flag = 0;
+    s.issued = 0;
     fence_barrier_init();
   }
   __syncthreads();
@@ -158,16 +164,29 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
             } else {
               mbar_arrive(fb);
             }
+            s.issued = kk + 1;
           }
         }
         __syncwarp();
       }
+    }
+    // Drain: wait (bounded) until the copies of the last stages issued have landed,
+    // so none is in flight when the CTA exits, also after a time-out.
+    __syncwarp();
+    if (lane == 0) {
+      const int iss = s.issued;
+      for (int kk = max(0, iss - kScoreStages); kk < iss; ++kk)
+        if (!mbar_wait(smem_addr(&s.full[kk % kScoreStages]), (kk / kScoreStages) & 1))
+          flag(status, MX4_STATUS_TIMEOUT);
     }
     return;
   }
 
   // ================= consumers
   const int g = lane >> 2, tig = lane & 3;
+  // byte-permute selectors: scale byte 2 (tig & 1) (+1) of a word to byte 3, zeros below
+  const uint32_t sel0 = 0x0444u | ((uint32_t)(2 * (tig & 1)) << 12);
+  const uint32_t sel1 = 0x0444u | ((uint32_t)(2 * (tig & 1) + 1) << 12);
   uint32_t breg[NT][8][2];
   float inv_scale[Q];
   int cur_seq = -1;
@@ -248,11 +267,12 @@ index_score_kernel(const uint16_t* __restrict__ iq, const uint8_t* __restrict__ 
                              breg[nt][2 * wi + 1][1]);
           }
         }
-        const int b0 = 2 * (tig & 1);
-        const float sx0 = e8m0_to_float((sx >> (8 * b0)) & 0xFFu);
-        const float sx1 = e8m0_to_float((sx >> (8 * b0 + 8)) & 0xFFu);
-        const float sy0 = e8m0_to_float((sy >> (8 * b0)) & 0xFFu);
-        const float sy1 = e8m0_to_float((sy >> (8 * b0 + 8)) & 0xFFu);
+        // scale bytes b0, b0+1 of the two rows -> fp32 2^(byte - 127): the byte goes
+        // to bits 31..24 (byte permute), then to the exponent field (>> 1); the max
+        // with 2^-127 gives byte 0 its subnormal value.  Byte 255 gives +inf, so a
+        // poisoned scale still yields a non-finite score.
+        const float sx0 = e8m0_fast(sx, sel0), sx1 = e8m0_fast(sx, sel1);
+        const float sy0 = e8m0_fast(sy, sel0), sy1 = e8m0_fast(sy, sel1);
         const int64_t i_g = (int64_t)pg * kPageTokens + r0 + g;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
@@ -302,7 +322,7 @@ cudaError_t launch_index_score(const uint16_t* iq, int q, const uint8_t* idx_pag
                                const int32_t* block_table, int B, int64_t bt_width,
                                const int32_t* seq_lens, float* scores, int64_t ld,
                                uint32_t* status, int num_sms, cudaStream_t stream) {
-  const int grid = num_sms * 3;  // 3 CTAs of ~62 KB shared memory per SM
+  const int grid = num_sms * 4;  // 4 CTAs of ~51 KB shared memory per SM
   switch (q) {
     case 1: return launch_q<1>(grid, iq, idx_pages, idx_page_stride, num_pages, block_table, B,
                                bt_width, seq_lens, scores, ld, status, stream);

@@ -179,6 +179,38 @@ def test_insert_special_values_bit_exact():
     assert np.array_equal(got, want)
 
 
+@pytest.mark.parametrize("q", [1, 3])
+def test_index_score_special_scale_bytes(q):
+    # Index keys whose scale byte is 0 with non-zero codes (block amax just above
+    # 2^-126), all-zero blocks (byte 0, codes 0), and one row poisoned to scale
+    # 0xFF inside the valid range: finite scores match, the poisoned one is
+    # non-finite on both sides.
+    rng = np.random.default_rng(21)
+    n = 300
+    rows = rng.standard_normal((n, 128)).astype(np.float32)
+    rows[10:20, :32] = rng.uniform(-1.5, 1.5, (10, 32)).astype(np.float32) * np.float32(2.0 ** -126)
+    rows[20:30, 32:64] = 0.0
+    rows[30:35] = 0.0
+    ip, ip_o = _insert_both(rows)
+    assert np.array_equal(ip, ip_o)
+    assert (ip_o[0, 8192 + 10 * 4] == 0) and (ip_o[0, 10 * 64] != 0)
+    ip_o[0, 8192 + 40 * 4:8192 + 41 * 4] = 0xFF
+    ip[0, 8192 + 40 * 4:8192 + 41 * 4] = 0xFF
+    iq32 = rng.standard_normal((q, 128)).astype(np.float32)
+    iq = torch.from_numpy(iq32).to(torch.bfloat16)
+    iq_bits = iq.view(torch.int16).numpy().view(np.uint16)
+    lens = np.array([n], np.int32)
+    bt = np.arange(3, dtype=np.int32)[None, :]
+    want, mag = oracle.index_score(iq_bits, q, ip_o, bt, lens, n, want_mag=True)
+    got = torch.empty((q, n), dtype=torch.float32, device=DEV)
+    m.index_score(iq.to(DEV), q, torch.from_numpy(ip).to(DEV), torch.from_numpy(bt).to(DEV),
+                  torch.from_numpy(lens).to(DEV), got)
+    m.mx4_check_status()
+    g = got.cpu().numpy()
+    check_scores(g, want, mag, np.full(q, n))
+    assert not np.isfinite(g[:, 40]).any() and not np.isfinite(want[:, 40]).any()
+
+
 def test_insert_dense_sweep_of_scaled_values():
     # Every 257th fp32 bit pattern in [0, 8) (both signs), 31 per block next to an
     # anchor of 4.0 so the block exponent is 0 and y = x.
