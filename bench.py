@@ -164,7 +164,7 @@ def run_gpu(args):
     import torch.distributed as dist
 
     import mxfp4_sparse_paged_gb300 as m
-    from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, step_inputs_host
+    from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, PipelinedSteps, step_inputs_host
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -239,28 +239,28 @@ def run_gpu(args):
     ms_per_step = total_ms / args.steps
     value = wl.T * world * args.steps / (total_ms / 1e3)
 
-    # ---- end to end through the public API: host inputs -> device -> step -> host output
+    # ---- end to end through the public API: host inputs -> device -> step -> host
+    # output for every step, with the transfers of neighbouring steps overlapped
+    # (PipelinedSteps).  No flush here: each step streams the 204 MB index cache and
+    # writes and reads 134 MB of scores, more than the 129 MB L2.
     pin = {k: torch.from_numpy(np.ascontiguousarray(
         v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory() for k, v in host.items()}
-    h_out = torch.empty(step.out.shape, dtype=torch.float32).pin_memory()
+    pipe = PipelinedSteps(wl, caches, device=dev)
     h2d = sum(t.numel() * t.element_size() for t in pin.values())
-    d2h = h_out.numel() * h_out.element_size()
-    for _ in range(2):
-        step.load_inputs(pin, non_blocking=True)
-        step.run(stream=stream)
-        h_out.copy_(step.out, non_blocking=True)
-    e_st = [(ev(), ev()) for _ in range(args.steps)]
+    d2h = pipe.h_out[0].numel() * pipe.h_out[0].element_size()
+    for _ in range(4):
+        _, done = pipe.submit(pin)
+    done.synchronize()
     barrier()
     torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush_l2(i & 0xFF)
-        e_st[i][0].record(stream)
-        step.load_inputs(pin, non_blocking=True)
-        step.run(stream=stream)
-        h_out.copy_(step.out, non_blocking=True)
-        e_st[i][1].record(stream)
+    e0, e1 = ev(), ev()
+    e0.record(pipe.h2d)
+    for _ in range(args.steps):
+        _, done = pipe.submit(pin)
+    pipe.h2d.wait_event(done)
+    e1.record(pipe.h2d)
     torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e_st)
+    e2e_ms = e0.elapsed_time(e1)
     if world > 1:
         t = torch.tensor([e2e_ms], device=dev)
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -292,7 +292,11 @@ def run_gpu(args):
                          "frac": round(hot_gbs / peak, 4)},
         "kernel_ms": {n: round(v, 5) for n, v in kern_ms.items()},
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
+                "d2h_bytes_per_step": int(d2h),
+                "mode": "every step copies its inputs from pinned host memory and reads its "
+                        "output back; the copies of neighbouring steps overlap the compute "
+                        "(two buffer sets, three streams); no L2 flush (a step moves more "
+                        "than the L2 holds)"},
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": ck,
         "wall_s_timed_region": round(wall, 3),

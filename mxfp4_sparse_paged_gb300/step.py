@@ -145,3 +145,49 @@ class DecodeStep:
         segment filter when rows can exceed the candidate capacity, then select), decode
         split + merge."""
         return (1 if self.slots.numel() else 0) + 1 + (3 if self.topk_ws is not None else 1) + 2
+
+
+class PipelinedSteps:
+    """Back-to-back decode steps with the host transfers overlapped.
+
+    A serving loop's step copies its inputs (q, iq, the new tokens' rows and slots)
+    from pinned host memory and reads its output back.  Here step i+1's inputs
+    are copied on one stream while step i computes, and step i's output is copied
+    back on another while step i+1 computes.  Two DecodeStep buffer sets
+    alternate; the page caches are shared and the steps run in order on the
+    compute stream, so every insert lands before the next step's reads.
+    """
+
+    def __init__(self, wl: W.Workload, caches: PagedCaches, device="cuda"):
+        self.steps = [DecodeStep(wl, caches, device=device), DecodeStep(wl, caches, device=device)]
+        self.compute = torch.cuda.Stream(device=device)
+        self.h2d = torch.cuda.Stream(device=device)
+        self.d2h = torch.cuda.Stream(device=device)
+        self.h_out = [torch.empty(s.out.shape, dtype=torch.float32).pin_memory() for s in self.steps]
+        ev = lambda: torch.cuda.Event()  # noqa: E731
+        self.inputs_ready = [ev(), ev()]
+        self.compute_done = [ev(), ev()]
+        self.out_done = [ev(), ev()]
+        self.n = 0
+
+    def submit(self, host: dict):
+        """Enqueue one step on the pinned host inputs `host`; returns (pinned output
+        tensor, event recorded when it holds this step's result)."""
+        b = self.n & 1
+        st = self.steps[b]
+        with torch.cuda.stream(self.h2d):
+            if self.n >= 2:
+                self.h2d.wait_event(self.compute_done[b])  # step n-2 is done with buffers b
+            st.load_inputs(host, non_blocking=True)
+            self.inputs_ready[b].record(self.h2d)
+        self.compute.wait_event(self.inputs_ready[b])
+        if self.n >= 2:
+            self.compute.wait_event(self.out_done[b])  # step n-2's output has been read back
+        st.run(stream=self.compute)
+        self.compute_done[b].record(self.compute)
+        with torch.cuda.stream(self.d2h):
+            self.d2h.wait_event(self.compute_done[b])
+            self.h_out[b].copy_(st.out, non_blocking=True)
+            self.out_done[b].record(self.d2h)
+        self.n += 1
+        return self.h_out[b], self.out_done[b]

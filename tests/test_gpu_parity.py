@@ -16,7 +16,7 @@ import torch
 import oracle
 import mxfp4_sparse_paged_gb300 as m
 from mxfp4_sparse_paged_gb300 import workloads as W
-from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, step_inputs_host
+from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, PipelinedSteps, step_inputs_host
 
 from _sides import ATTN_ABS, OracleSide, check_scores, check_topk
 
@@ -297,6 +297,25 @@ def test_topk_segment_filter_paths():
             m.topk_select(d_sc, d_lens, q, k, out, ws)
             m.mx4_check_status()
             assert np.array_equal(out.cpu().numpy(), want), f"k={k} ld={ld}"
+
+
+def test_pipelined_steps_match_a_plain_step():
+    # The overlapped serving loop gives, step after step, the plain step's output.
+    wl = W.make(1)
+    caches, step, host = _gpu_step(wl)
+    want = step.out.cpu().numpy()
+    pin = {k: torch.from_numpy(np.ascontiguousarray(
+        v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory() for k, v in host.items()}
+    pipe = PipelinedSteps(wl, caches, device=DEV)
+    for _ in range(5):
+        h_out, done = pipe.submit(pin)
+        done.synchronize()
+        assert np.array_equal(h_out.numpy(), want)
+    outs = [pipe.submit(pin) for _ in range(4)]
+    torch.cuda.synchronize()
+    for h_out, _ in outs[-2:]:
+        assert np.array_equal(h_out.numpy(), want)
+    m.mx4_check_status()
 
 
 # ----------------------------------------------------------------- decode edges
