@@ -53,6 +53,22 @@ class PagedCaches:
                 self.insert_rows(k, v, ik, slots)
 
 
+def _layout(specs):
+    """Byte offsets (256-byte aligned) of named tensors packed into one buffer."""
+    out, off = {}, 0
+    for name, shape, dtype in specs:
+        nb = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        out[name] = (off, nb, tuple(shape), dtype)
+        off += (nb + 255) // 256 * 256
+    out["bytes"] = max(off, 256)
+    return out
+
+
+def _views(buf: torch.Tensor, layout: dict) -> dict:
+    return {name: buf[o:o + nb].view(dt).view(shape)
+            for name, (o, nb, shape, dt) in ((k, v) for k, v in layout.items() if k != "bytes")}
+
+
 def step_inputs_host(wl: W.Workload):
     """Host (numpy) inputs of one decode step: q/iq bf16 bits, the new tokens'
     rows and slots (empty unless the workload inserts in the step)."""
@@ -82,13 +98,21 @@ class DecodeStep:
         self.scale = 1.0 / math.sqrt(W.HEAD_DIM)
         self.block_table = torch.from_numpy(wl.block_table).to(device)
         self.seq_lens = torch.from_numpy(wl.seq_lens).to(device)
-        self.q = torch.empty((T, W.Q_HEADS, W.HEAD_DIM), dtype=torch.bfloat16, device=device)
-        self.iq = torch.empty((T, W.HEAD_DIM), dtype=torch.bfloat16, device=device)
         n_ins = T if wl.spec.insert_in_step else 0
-        self.k_new = torch.empty((n_ins, 1, W.HEAD_DIM), dtype=torch.float32, device=device)
-        self.v_new = torch.empty_like(self.k_new)
-        self.idx_new = torch.empty((n_ins, W.HEAD_DIM), dtype=torch.float32, device=device)
-        self.slots = torch.empty(n_ins, dtype=torch.int64, device=device)
+        # the step's inputs live in one device buffer (one host -> device copy a step)
+        self.input_layout = _layout([
+            ("q", (T, W.Q_HEADS, W.HEAD_DIM), torch.bfloat16),
+            ("iq", (T, W.HEAD_DIM), torch.bfloat16),
+            ("k", (n_ins, 1, W.HEAD_DIM), torch.float32),
+            ("v", (n_ins, 1, W.HEAD_DIM), torch.float32),
+            ("idx_k", (n_ins, W.HEAD_DIM), torch.float32),
+            ("slots", (n_ins,), torch.int64)])
+        self.inputs = torch.empty(self.input_layout["bytes"], dtype=torch.uint8, device=device)
+        views = _views(self.inputs, self.input_layout)
+        self.q, self.iq = views["q"], views["iq"]
+        self.k_new, self.v_new, self.idx_new = views["k"], views["v"], views["idx_k"]
+        self.slots = views["slots"]
+        self.graph = None
         self.scores = torch.empty((T, self.ld), dtype=torch.float32, device=device)
         self.topk_idx = torch.empty((T, k), dtype=torch.int32, device=device)
         self.out = torch.empty((T, W.Q_HEADS, W.HEAD_DIM), dtype=torch.float32, device=device)
@@ -96,6 +120,45 @@ class DecodeStep:
         self.topk_ws = torch.empty(max(tws, 16), dtype=torch.uint8, device=device) if tws else None
         self.dec_ws = torch.empty(sparse_paged_decode_workspace(T, k), dtype=torch.uint8,
                                   device=device)
+
+    def pack_inputs(self, host: dict) -> torch.Tensor:
+        """One step's host inputs (numpy, as from step_inputs_host) packed into a pinned
+        buffer with the layout of the device input buffer."""
+        buf = torch.empty(self.input_layout["bytes"], dtype=torch.uint8).pin_memory()
+        views = _views(buf, self.input_layout)
+        for name in ("q", "iq", "k", "v", "idx_k", "slots"):
+            a = host[name]
+            a = a.view(np.int16) if a.dtype == np.uint16 else a
+            t = torch.from_numpy(np.ascontiguousarray(a))
+            dst = views[name]
+            if t.dtype == torch.int16:
+                t = t.view(torch.bfloat16)
+            dst.copy_(t.view(dst.shape))
+        return buf
+
+    def load_packed(self, packed: torch.Tensor, non_blocking=False):
+        """Copy a packed pinned input buffer (pack_inputs) to the device: one copy."""
+        self.inputs.copy_(packed, non_blocking=non_blocking)
+
+    def capture(self):
+        """Record run() (all kernels of the step) as a CUDA graph; replay() then
+        launches the whole step at once.  The eager run that precedes the capture
+        (first-call set-up) inserts nothing: its slots are set to -1, and the input
+        buffer is restored afterwards."""
+        saved = self.inputs.clone()
+        self.slots.fill_(-1)
+        self.run()
+        self.inputs.copy_(saved)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(stream=torch.cuda.current_stream())
+        self.graph = g
+        return g
+
+    def replay(self):
+        """Launch the captured step on the current stream."""
+        self.graph.replay()
 
     def load_inputs(self, host: dict, non_blocking=False):
         """Copy one step's host inputs (numpy or pinned torch) into the device buffers."""
@@ -152,14 +215,18 @@ class PipelinedSteps:
 
     A serving loop's step copies its inputs (q, iq, the new tokens' rows and slots)
     from pinned host memory and reads its output back.  Here step i+1's inputs
-    are copied on one stream while step i computes, and step i's output is copied
-    back on another while step i+1 computes.  Two DecodeStep buffer sets
-    alternate; the page caches are shared and the steps run in order on the
-    compute stream, so every insert lands before the next step's reads.
+    (one packed buffer, one copy) go to the device on one stream while step i
+    computes, and step i's output is read back on another while step i+1
+    computes.  Each step is one CUDA-graph launch of all its kernels.  Two
+    DecodeStep buffer sets alternate; the page caches are shared and the steps run
+    in order on the compute stream, so every insert lands before the next step's
+    reads.
     """
 
     def __init__(self, wl: W.Workload, caches: PagedCaches, device="cuda"):
         self.steps = [DecodeStep(wl, caches, device=device), DecodeStep(wl, caches, device=device)]
+        for st in self.steps:
+            st.capture()
         self.compute = torch.cuda.Stream(device=device)
         self.h2d = torch.cuda.Stream(device=device)
         self.d2h = torch.cuda.Stream(device=device)
@@ -170,20 +237,24 @@ class PipelinedSteps:
         self.out_done = [ev(), ev()]
         self.n = 0
 
-    def submit(self, host: dict):
-        """Enqueue one step on the pinned host inputs `host`; returns (pinned output
-        tensor, event recorded when it holds this step's result)."""
+    def pack_inputs(self, host: dict) -> torch.Tensor:
+        return self.steps[0].pack_inputs(host)
+
+    def submit(self, packed: torch.Tensor):
+        """Enqueue one step on a packed pinned input buffer (pack_inputs); returns
+        (pinned output tensor, event recorded when it holds this step's result)."""
         b = self.n & 1
         st = self.steps[b]
         with torch.cuda.stream(self.h2d):
             if self.n >= 2:
                 self.h2d.wait_event(self.compute_done[b])  # step n-2 is done with buffers b
-            st.load_inputs(host, non_blocking=True)
+            st.load_packed(packed, non_blocking=True)
             self.inputs_ready[b].record(self.h2d)
         self.compute.wait_event(self.inputs_ready[b])
         if self.n >= 2:
             self.compute.wait_event(self.out_done[b])  # step n-2's output has been read back
-        st.run(stream=self.compute)
+        with torch.cuda.stream(self.compute):
+            st.replay()
         self.compute_done[b].record(self.compute)
         with torch.cuda.stream(self.d2h):
             self.d2h.wait_event(self.compute_done[b])

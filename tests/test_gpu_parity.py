@@ -299,14 +299,15 @@ def test_topk_segment_filter_paths():
             assert np.array_equal(out.cpu().numpy(), want), f"k={k} ld={ld}"
 
 
-def test_pipelined_steps_match_a_plain_step():
-    # The overlapped serving loop gives, step after step, the plain step's output.
-    wl = W.make(1)
+@pytest.mark.parametrize("wid", [1, 4])
+def test_pipelined_steps_match_a_plain_step(wid):
+    # The overlapped serving loop (packed inputs, one CUDA-graph launch a step)
+    # gives, step after step, the plain step's output.
+    wl = W.make(wid)
     caches, step, host = _gpu_step(wl)
     want = step.out.cpu().numpy()
-    pin = {k: torch.from_numpy(np.ascontiguousarray(
-        v.view(np.int16) if v.dtype == np.uint16 else v)).pin_memory() for k, v in host.items()}
     pipe = PipelinedSteps(wl, caches, device=DEV)
+    pin = pipe.pack_inputs(host)
     for _ in range(5):
         h_out, done = pipe.submit(pin)
         done.synchronize()
