@@ -10,7 +10,7 @@
 // of more than kCand scores go through a candidate filter first:
 // topk_threshold_kernel -- one 512-thread CTA per such row: an evenly spaced
 //   sample of 2048 keys of the row and, as threshold, the sample key at a rank
-//   that leaves about 1.3 k candidates plus a margin (radix select).
+//   a few binomial standard deviations past the k-th (radix select).
 // topk_filter_kernel -- persistent CTAs over 16384-score segments of those
 //   rows: the segment's keys >= threshold are compacted in index order (warp
 //   scans, block scan over warps) and appended to the row's candidate list in
@@ -72,6 +72,8 @@ struct FilterSmem {
   int tmp[32];
   int warp_base[kTopkWarps];
   int chunk_pref[kTopkThreads];
+  long long rown[kTopkThreads];  // row lengths when every row has its own thread
+  uint32_t rthr[kTopkThreads];   // and their thresholds
   int base;
 };
 
@@ -93,8 +95,13 @@ __host__ __device__ inline int64_t align16(int64_t x) { return (x + 15) / 16 * 1
 __device__ __forceinline__ bool use_filter(int64_t n, int64_t ld, int k) {
   return n > kCand && n <= ld && k < n && k <= kCand;
 }
+// Threshold rank in the sample: m = k * 2048 / n sample keys are expected at or
+// above the k-th largest score; taking rank m + 4 sqrt(m) + 8 leaves fewer than k
+// candidates only with a probability below ~1e-5 (binomial tail), and such a row
+// falls back to the exact paths.
 __device__ __forceinline__ int sample_rank(int64_t n, int k) {
-  return min(kSample - 1, (int)(1.3 * (double)k * kSample / (double)n) + 32);
+  const double m = (double)k * kSample / (double)n;
+  return min(kSample - 1, (int)(m + 4.0 * sqrt(m)) + 8);
 }
 __device__ __forceinline__ int64_t row_len(const int32_t* seq_lens, int64_t t, int Q) {
   return (int64_t)seq_lens[t / Q] - Q + (t % Q) + 1;
@@ -334,14 +341,24 @@ topk_filter_kernel(const float* __restrict__ scores, int64_t ld,
   __shared__ FilterSmem s;
   pdl_launch_dependents();
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // With at most one row per thread, every row's length (and below, threshold) is
+  // kept in shared memory, so an item is mapped to (row, segment) without loads.
+  const bool small = T <= kTopkThreads;
   const int64_t per = (T + kTopkThreads - 1) / kTopkThreads;
   const int64_t r0 = min(T, (int64_t)tid * per), r1 = min(T, r0 + per);
   int cnt = 0;
-  for (int64_t t = r0; t < r1; ++t) cnt += row_segments(seq_lens, t, Q, ld, k);
+  if (small) {
+    const int64_t n = tid < T ? row_len(seq_lens, tid, Q) : 0;
+    cnt = (tid < T && use_filter(n, ld, k)) ? (int)((n + kSeg - 1) / kSeg) : 0;
+    s.rown[tid] = n;
+  } else {
+    for (int64_t t = r0; t < r1; ++t) cnt += row_segments(seq_lens, t, Q, ld, k);
+  }
   int items;
   s.chunk_pref[tid] = block_exclusive_scan(cnt, s.tmp, items);
-  __syncthreads();
   pdl_wait();  // scores, thresholds and counts are touched from here on
+  if (small && cnt > 0) s.rthr[tid] = ws.thr[tid];
+  __syncthreads();
 
   for (int item = blockIdx.x; item < items; item += gridDim.x) {
     int lo = 0, hi = kTopkThreads - 1;  // last chunk whose prefix is <= item
@@ -351,18 +368,25 @@ topk_filter_kernel(const float* __restrict__ scores, int64_t ld,
     }
     int64_t t = (int64_t)lo * per;
     int sg = item - s.chunk_pref[lo];
-    for (;;) {
-      const int ns = row_segments(seq_lens, t, Q, ld, k);
-      if (sg < ns) break;
-      sg -= ns;
-      ++t;
+    int64_t n;
+    uint32_t thr;
+    if (small) {
+      n = s.rown[lo];
+      thr = s.rthr[lo];
+    } else {
+      for (;;) {
+        const int ns = row_segments(seq_lens, t, Q, ld, k);
+        if (sg < ns) break;
+        sg -= ns;
+        ++t;
+      }
+      n = row_len(seq_lens, t, Q);
+      thr = ws.thr[t];
     }
-    const int64_t n = row_len(seq_lens, t, Q);
     const int64_t s0 = (int64_t)sg * kSeg, s1 = min(n, s0 + kSeg);
     const float* row = scores + t * ld;
 
-    // the segment's keys, all loads in flight, and the row's threshold
-    const uint32_t thr = ws.thr[t];
+    // the segment's keys, all loads in flight
     uint32_t key[kSegIters][4];
     int m[kSegIters];
     const int64_t w0 = s0 + (int64_t)warp * (kSegIters * 128) + 4 * lane;
