@@ -28,8 +28,8 @@
 //      into f16 hi + lo parts so P V keeps ~22 bits; O += P V with mma.sync, V
 //      fragments built by zipping the nibbles of two entries so one cvt yields
 //      an (entry, entry) pair, times the V multipliers.
-//   4. The 8 warps' (max, sum, O) are merged in shared memory, in the MMA
-//      fragment order (bank-conflict free), and the split writes its
+//   4. The 8 warps' (max, sum, O) are merged in shared memory, one float4 per
+//      lane and MMA n-tile (bank-conflict free), and the split writes its
 //      unnormalised [head][dim] output plus its running max (log2 units) and
 //      sum per head.
 // merge kernel -- one CTA per decode token combines the splits.
@@ -430,27 +430,37 @@ decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __rest
   float fv[4];
 #pragma unroll
   for (int b = 0; b < 4; ++b) fv[b] = ldexpf(1.f, (int)((refV >> (8 * b)) & 0xFFu) - 127);
-  // element (j, c) of lane l lives at red[warp][(4 j + c) * 32 + l]
-  float* red = reinterpret_cast<float*>(&s.tile[0][0][0]);
+  // elements (j, 0..3) of lane l live in one float4 at red4[warp][j * 32 + l]
+  float4* red4 = reinterpret_cast<float4*>(&s.tile[0][0][0]);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float f = fv[(2 * tig + 8 * (j >> 3)) >> 2];
-#pragma unroll
-    for (int c = 0; c < 4; ++c)
-      red[warp * kFrag + (4 * j + c) * 32 + lane] = o[j][c] * fw[c >> 1] * f;
+    const float f0 = fw[0] * f, f1 = fw[1] * f;
+    red4[warp * (kFrag / 4) + j * 32 + lane] =
+        make_float4(o[j][0] * f0, o[j][1] * f0, o[j][2] * f1, o[j][3] * f1);
   }
   __syncthreads();
-  // fragment element e -> (head, dim): lane = e % 32 (g = lane/4, tig = lane%4),
-  // c = (e/32) % 4, j = e / 128; head = g + 8 (c/2); dim = 8 (2 tig + c%2 + 8 (j/8)) + j%8
+  // float4 x = j * 32 + lane -> element c: head = g + 8 (c/2) (g = lane/4),
+  // dim = 8 (2 tig + c%2 + 8 (j/8)) + j%8 (tig = lane%4)
   const int64_t split = t * S + sp;
-  for (int e = tid; e < kFrag; e += kDecThreads) {
-    float acc = 0.f;
+  for (int x = tid; x < kFrag / 4; x += kDecThreads) {
+    float4 acc = red4[x];
 #pragma unroll
-    for (int w = 0; w < kDecWarps; ++w) acc += red[w * kFrag + e];
-    const int ln = e & 31, c = (e >> 5) & 3, j = e >> 7;
-    const int head = (ln >> 2) + 8 * (c >> 1);
-    const int dim = 8 * (2 * (ln & 3) + (c & 1) + 8 * (j >> 3)) + (j & 7);
-    ws_o[split * kFrag + head * kHeadDim + dim] = acc;
+    for (int w = 1; w < kDecWarps; ++w) {
+      const float4 y = red4[w * (kFrag / 4) + x];
+      acc.x += y.x;
+      acc.y += y.y;
+      acc.z += y.z;
+      acc.w += y.w;
+    }
+    const int ln = x & 31, j = x >> 5;
+    const int h0 = ln >> 2;
+    const int d0 = 8 * (2 * (ln & 3) + 8 * (j >> 3)) + (j & 7);
+    float* dst = ws_o + split * kFrag;
+    dst[h0 * kHeadDim + d0] = acc.x;
+    dst[h0 * kHeadDim + d0 + 8] = acc.y;
+    dst[(h0 + 8) * kHeadDim + d0] = acc.z;
+    dst[(h0 + 8) * kHeadDim + d0 + 8] = acc.w;
   }
   if (tid < kHeads) {
     float Mh = -INFINITY;
