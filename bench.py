@@ -157,6 +157,26 @@ def cpu_oracle_sample(wl, budget_s: float = 15.0):
     return done_tok / spent, detail, spent
 
 
+# --------------------------------------------------------------------------- ranks
+
+def max_over_ranks(x: float, world: int, device="cpu") -> float:
+    """The largest of the ranks' values (each rank's timed region; the job ends with
+    the slowest rank).  A no-op for one rank."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(tokens_per_rank_step: int, world: int, steps: int, total_ms: float) -> float:
+    """Whole-job decode tokens/s: every rank runs its own batch (replicas), so the
+    job processes world x tokens per step, in the slowest rank's time."""
+    return tokens_per_rank_step * world * steps / (total_ms / 1e3)
+
+
 # --------------------------------------------------------------------------- GPU arm
 
 def run_gpu(args):
@@ -239,13 +259,9 @@ def run_gpu(args):
     torch.cuda.synchronize()
     m.mx4_check_status()
     kern_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in per[n]) for n in names}
-    total_ms = sum(step_ms)
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
     ms_per_step = total_ms / args.steps
-    value = wl.T * world * args.steps / (total_ms / 1e3)
+    value = job_value(wl.T, world, args.steps, total_ms)
 
     # ---- end to end through the public API: host inputs -> device -> step -> host
     # output for every step, with the transfers of neighbouring steps overlapped
@@ -267,12 +283,8 @@ def run_gpu(args):
     pipe.h2d.wait_event(done)
     e1.record(pipe.h2d)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e_value = wl.T * world * args.steps / (e2e_ms / 1e3)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e_value = job_value(wl.T, world, args.steps, e2e_ms)
     m.mx4_check_status()
 
     peak, peak_kind = _peaks()
