@@ -76,6 +76,8 @@ def _load():
         lib.orc_index_score.argtypes = [P, i64, i32, P, i64, i64, P, i64, P, P, P, i64]
         lib.orc_topk_select.restype = i32
         lib.orc_topk_select.argtypes = [P, i64, P, i64, i32, i32, P]
+        lib.orc_norm_rope.restype = i32
+        lib.orc_norm_rope.argtypes = [P, i64, P, P, i64, P, ctypes.c_double, i32, P]
         lib.orc_sparse_paged_decode.restype = i32
         lib.orc_sparse_paged_decode.argtypes = [P, i64, i32, i32, i32, P, P, i64, i64, i64,
                                                 P, i64, P, P, i32, ctypes.c_double, P]
@@ -191,6 +193,22 @@ def mx4_insert(k, v, idx_k, slot_mapping, k_pages, v_pages, idx_pages):
                             _ptr(k_pages), _ptr(v_pages), kv_ps, kv_hs, _ptr(idx_pages),
                             idx_ps, P)
     _check(rc, "mx4_insert")
+
+
+def norm_rope(x, g, cos_sin, positions, eps, rope=True):
+    """RMS-norm with weight g, then (rope) the rotary turn of dims (i, i+64) by
+    cos_sin[pos]: float64 [n, 128] from fp32 rows x [n, 128]."""
+    lib = _load()
+    x = _c(x, np.float32).reshape(-1, 128)
+    n = x.shape[0]
+    g = _c(g, np.float32)
+    cos_sin = _c(cos_sin, np.float32)
+    positions = _c(np.broadcast_to(np.asarray(positions, np.int64), (n,)), np.int64)
+    out = np.empty((n, 128), np.float64)
+    rc = lib.orc_norm_rope(_ptr(x), n, _ptr(g), _ptr(cos_sin), cos_sin.shape[0], _ptr(positions),
+                           ctypes.c_double(eps), int(bool(rope)), _ptr(out))
+    _check(rc, "norm_rope")
+    return out
 
 
 def index_score(iq_bits, q_per_seq, idx_pages, block_table, seq_lens, ld, want_mag=False):

@@ -24,6 +24,9 @@
  *   [heads]  "vllm.models.minimax_m3.amd.mono.weights" -- _build_cp_qkv (one
  *            rank's rows q(2048) | k(128) | v(128) | index_q(128) | index_k(128):
  *            16 query heads, one KV head, one index head, head_dim 128).
+ *   [layer]  "vllm.models.minimax_m3.amd.mono.weights" -- SparseMoeLayer (the norm
+ *            weights g_q, g_k, g_iq, g_ik and the rotary table cos_sin a layer's
+ *            kernels read).
  *   [OCP]    OCP Microscaling Formats (MX) v1.0 -- the FP4 E2M1 element type
  *            (1 sign, 2 exponent bits with bias 1, 1 mantissa bit, no inf/NaN),
  *            the E8M0 scale type (2^(byte-127), 0xFF = NaN) and the conversion of
@@ -45,6 +48,12 @@
  *   R8  top-k ties go to the lower token index; the selected indices are
  *       returned in ascending order, padded with -1;
  *   R9  attention is softmax(scale * q.K) V over the selected tokens only.
+ *   R10 the writer in front of the insert ([layer] SparseMoeLayer: g_q, g_k,
+ *       g_iq, g_ik, cos_sin; no formula printed): each q, k, index-q and
+ *       index-k head row is RMS-normed over its 128 dims (mean of squares plus
+ *       eps, times the weight g) and then rotated: dims i and i+64 (i < 64) are
+ *       a pair turned by the angle whose cosine and sine are cos_sin[pos][i]
+ *       and cos_sin[pos][64+i]; V is neither normed nor rotated.
  */
 #include <math.h>
 #include <stddef.h>
@@ -451,4 +460,37 @@ int orc_sparse_paged_decode(const uint16_t *qh, int64_t B, int q, int H, int Hkv
 done:
     free(lg);
     return rc;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The writer's norm and rotary embedding, R10 ([layer] SparseMoeLayer):
+ *   z_j = x_j * g_j / sqrt(mean_j x_j^2 + eps)
+ *   y_i = z_i c_i - z_{i+64} s_i,  y_{i+64} = z_{i+64} c_i + z_i s_i   (i < 64)
+ * with c_i = cos_sin[pos][i], s_i = cos_sin[pos][64 + i]; rope = 0 skips the
+ * rotation.  x: n rows of 128 fp32; out: n rows of 128 float64.  A position
+ * outside [0, max_pos) is refused.                                            */
+int orc_norm_rope(const float *x, int64_t n, const float *g, const float *cos_sin,
+                  int64_t max_pos, const int64_t *pos, double eps, int rope, double *out)
+{
+    for (int64_t r = 0; r < n; ++r) {
+        const float *xr = x + r * ORC_ROW_ELEMS;
+        double *yr = out + r * ORC_ROW_ELEMS;
+        double ss = 0.0;
+        for (int j = 0; j < ORC_ROW_ELEMS; ++j) ss += (double)xr[j] * (double)xr[j];
+        const double inv = 1.0 / sqrt(ss / ORC_ROW_ELEMS + eps);
+        double z[ORC_ROW_ELEMS];
+        for (int j = 0; j < ORC_ROW_ELEMS; ++j) z[j] = (double)xr[j] * inv * (double)g[j];
+        if (!rope) {
+            memcpy(yr, z, sizeof z);
+            continue;
+        }
+        if (pos[r] < 0 || pos[r] >= max_pos) return ORC_ERR_BOUNDS;
+        const float *cs = cos_sin + pos[r] * ORC_ROW_ELEMS;
+        for (int i = 0; i < ORC_ROW_ELEMS / 2; ++i) {
+            const double c = cs[i], sn = cs[ORC_ROW_ELEMS / 2 + i];
+            yr[i] = z[i] * c - z[i + ORC_ROW_ELEMS / 2] * sn;
+            yr[i + ORC_ROW_ELEMS / 2] = z[i + ORC_ROW_ELEMS / 2] * c + z[i] * sn;
+        }
+    }
+    return ORC_OK;
 }

@@ -441,3 +441,67 @@ def test_decode_gqa_uses_kv_head_group():
     for h in range(4):
         V = np.stack([oracle.dequant_row(vp[0, h // 2], i) for i in range(L)])
         assert np.allclose(out[0, h], V.mean(axis=0), rtol=1e-14, atol=1e-15)
+
+
+# ----------------------------------------------------------------- norm + rotary (R10)
+
+def _cos_sin(angles):
+    """One rotary row per angle vector (64 angles): [cos(64) | sin(64)], fp32."""
+    a = np.asarray(angles, np.float64).reshape(-1, 64)
+    return np.concatenate([np.cos(a), np.sin(a)], axis=1).astype(np.float32)
+
+
+def test_norm_rope_hand_row():
+    # x = (3, 4, 0, ...): mean of squares 25/128, so z = x * sqrt(128) / 5; no turn
+    x = np.zeros((1, 128), np.float32)
+    x[0, 0], x[0, 1] = 3, 4
+    y = oracle.norm_rope(x, np.ones(128, np.float32), _cos_sin(np.zeros(64)), [0], 0.0)
+    want = np.zeros(128)
+    want[0], want[1] = 3 * math.sqrt(128) / 5, 4 * math.sqrt(128) / 5
+    assert np.allclose(y[0], want, rtol=0, atol=1e-12)
+
+
+def test_norm_rope_constant_row_gives_the_weight():
+    g = np.linspace(-2, 2, 128).astype(np.float32)
+    for c in (1e-3, 7.0, -5.0):
+        x = np.full((1, 128), c, np.float32)
+        y = oracle.norm_rope(x, g, _cos_sin(np.zeros(64)), [0], 0.0, rope=False)
+        assert np.allclose(y[0], np.sign(c) * g.astype(np.float64), rtol=1e-12, atol=0)
+
+
+def test_norm_rope_quarter_turn_direction():
+    # cos 0, sin 1: (z_i, z_{i+64}) -> (-z_{i+64}, z_i)
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((2, 128)).astype(np.float32)
+    g = rng.uniform(0.5, 1.5, 128).astype(np.float32)
+    cs = np.zeros((1, 128), np.float32)
+    cs[0, 64:] = 1.0
+    z = oracle.norm_rope(x, g, cs, [0, 0], 1e-6, rope=False)
+    y = oracle.norm_rope(x, g, cs, [0, 0], 1e-6)
+    assert np.array_equal(y[:, :64], -z[:, 64:]) and np.array_equal(y[:, 64:], z[:, :64])
+
+
+def test_norm_rope_turn_keeps_pair_norms_and_position_picks_the_row():
+    rng = np.random.default_rng(4)
+    x = rng.standard_normal((5, 128)).astype(np.float32)
+    g = np.ones(128, np.float32)
+    ang = rng.uniform(-math.pi, math.pi, (7, 64))
+    cs = _cos_sin(ang)
+    pos = np.array([0, 3, 6, 3, 1])
+    z = oracle.norm_rope(x, g, cs, pos, 0.0, rope=False)
+    y = oracle.norm_rope(x, g, cs, pos, 0.0)
+    assert np.allclose(y[:, :64] ** 2 + y[:, 64:] ** 2, z[:, :64] ** 2 + z[:, 64:] ** 2,
+                       rtol=1e-6, atol=1e-12)
+    c, s = cs[pos, :64].astype(np.float64), cs[pos, 64:].astype(np.float64)
+    assert np.allclose(y[:, 0], z[:, 0] * c[:, 0] - z[:, 64] * s[:, 0], rtol=1e-14, atol=0)
+    # unit weight, no eps: the normed row has mean square 1
+    assert np.allclose((z ** 2).mean(axis=1), 1.0, rtol=1e-12)
+
+
+def test_norm_rope_zero_row_and_bad_position():
+    x = np.zeros((1, 128), np.float32)
+    cs = _cos_sin(np.zeros((2, 64)))
+    y = oracle.norm_rope(x, np.ones(128, np.float32), cs, [1], 1e-6)
+    assert np.array_equal(y, np.zeros((1, 128)))
+    with pytest.raises(Exception):
+        oracle.norm_rope(x, np.ones(128, np.float32), cs, [2], 1e-6)
