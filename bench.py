@@ -287,6 +287,8 @@ def run_gpu(args):
     e2e_value = job_value(wl.T, world, args.steps, e2e_ms)
     m.mx4_check_status()
 
+    writer = time_writer(wl, dev, stream, flush_l2, min(args.steps, 200))
+
     peak, peak_kind = _peaks()
     score_s = kern_ms["index_score"] / 1e3
     achieved = ab["index_score"] / score_s / 1e9
@@ -318,6 +320,7 @@ def run_gpu(args):
                         "output back; the copies of neighbouring steps overlap the compute "
                         "(two buffer sets, three streams, one packed input copy and one CUDA-graph "
                         "launch a step); no L2 flush (a step moves more than the L2 holds)"},
+        "norm_rope_writer": writer,
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": ck,
         "wall_s_timed_region": round(wall, 3),
@@ -330,6 +333,60 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_writer(wl, dev, stream, flush_l2, steps):
+    """The norm + rotary writer (mx4_norm_rope_insert) on the step's T new tokens,
+    next to the plain mx4_insert of the same K/V/index-K rows; both on a scratch
+    pool, event-timed on the launching stream after an L2 flush.  Positions are the
+    decode tokens' own; the rotary table covers them."""
+    import torch
+
+    import mxfp4_sparse_paged_gb300 as m
+    T, H, Hkv = wl.T, W.Q_HEADS, W.KV_HEADS
+    pos = wl.positions()
+    x = {n: torch.from_numpy(a).to(dev) for n, a in W.writer_inputs(T, H, Hkv, wl.spec.seed).items()}
+    cs = torch.from_numpy(W.rope_table(int(pos.max()) + 1)).to(dev)
+    P = (T + W.PAGE_TOKENS - 1) // W.PAGE_TOKENS
+    kp = torch.full((P, Hkv, W.PAGE_BYTES), W.POISON, dtype=torch.uint8, device=dev)
+    vp = torch.full_like(kp, W.POISON)
+    ip = torch.full((P, W.PAGE_BYTES), W.POISON, dtype=torch.uint8, device=dev)
+    slots = torch.arange(T, dtype=torch.int64, device=dev)
+    posd = torch.from_numpy(pos).to(dev)
+    q_out = torch.empty((T, H, W.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+    iq_out = torch.empty((T, W.HEAD_DIM), dtype=torch.bfloat16, device=dev)
+
+    def writer():
+        m.mx4_norm_rope_insert(x["q"], x["iq"], x["k"], x["v"], x["idx_k"], posd, cs, x["g_q"],
+                               x["g_k"], x["g_iq"], x["g_ik"], 1e-6, slots, kp, vp, ip, q_out,
+                               iq_out, stream=stream)
+
+    def plain():
+        m.mx4_insert(x["k"], x["v"], x["idx_k"], slots, kp, vp, ip, stream=stream)
+
+    us = {}
+    for name, fn in (("mx4_norm_rope_insert", writer), ("mx4_insert", plain)):
+        for _ in range(3):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(steps)]
+        for i in range(steps):
+            flush_l2(i & 0xFF)
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        us[name] = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    m.mx4_check_status()
+    row = W.PAGE_BYTES // W.PAGE_TOKENS
+    # fp32 rows in, one rotary-table row and position and slot per token, bf16 q and
+    # index-q out, K/V/index-K page rows out
+    nbytes = T * ((H + 2 * Hkv + 2) * W.HEAD_DIM * 4 + W.HEAD_DIM * 4 + 16 +
+                  (H + 1) * W.HEAD_DIM * 2 + (2 * Hkv + 1) * row)
+    return {"kernel": "mx4_norm_rope_insert", "tokens": T, "us": round(us["mx4_norm_rope_insert"], 2),
+            "plain_mx4_insert_us": round(us["mx4_insert"], 2), "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(nbytes / us["mx4_norm_rope_insert"] / 1e3, 1),
+            "timing": "mean of CUDA-event pairs on the launching stream, L2 flushed before each"}
 
 
 def _ncu_traffic(name):

@@ -102,6 +102,41 @@ int mx4_insert(const float *k, const float *v, const float *idx_k, int64_t T, in
                int64_t idx_page_stride, int64_t num_pages, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * mx4_norm_rope_insert -- the writer in front of mx4_insert: norm and rotary
+ * embedding of the new token's heads, then the MXFP4 insert ("vllm.models.
+ * minimax_m3.amd.mono.weights", SparseMoeLayer: g_q, g_k, g_iq, g_ik, cos_sin;
+ * the formula is not printed -- the plainest reading is taken).
+ *
+ * For token t at position pos = positions[t], every q head, the index-q head,
+ * every K head and the index-K head row x (128 fp32) becomes
+ *     z = x * g / sqrt(mean(x^2) + eps),
+ *     y[i] = z[i] c[i] - z[i+64] s[i],  y[i+64] = z[i+64] c[i] + z[i] s[i]  (i < 64)
+ * with c[i] = cos_sin[pos*128 + i], s[i] = cos_sin[pos*128 + 64 + i] and g the
+ * head kind's weight.  q and index-q are written as bf16 (round to nearest
+ * even) to q_out and iq_out.  K and index-K are quantised like mx4_insert into
+ * their page rows, and so is V, unchanged.  Computed in fp32.
+ *
+ *   q            fp32 [T, H, 128];  iq fp32 [T, 128]
+ *   k, v         fp32 [T, Hkv, 128]; idx_k fp32 [T, 128]   (all contiguous)
+ *   positions    int64 [T]; cos_sin fp32 [max_pos, 128]
+ *   g_q, g_k, g_iq, g_ik  fp32 [128]; eps >= 0
+ *   slot_mapping, pages   as mx4_insert
+ *   q_out        bf16 [T, H, 128]; iq_out bf16 [T, 128]  (outputs)
+ * fp32 arrays 16-byte aligned, q_out / iq_out 8-byte aligned.  A position
+ * outside [0, max_pos) skips every row of that token and sets
+ * MX4_STATUS_BAD_INDEX; slots behave as in mx4_insert.  1 <= H <= 64,
+ * 1 <= Hkv <= 8.
+ * ------------------------------------------------------------------------- */
+int mx4_norm_rope_insert(const float *q, const float *iq, const float *k, const float *v,
+                         const float *idx_k, int64_t T, int H, int Hkv, const int64_t *positions,
+                         const float *cos_sin, int64_t max_pos, const float *g_q,
+                         const float *g_k, const float *g_iq, const float *g_ik, float eps,
+                         const int64_t *slot_mapping, uint8_t *k_pages, uint8_t *v_pages,
+                         int64_t kv_page_stride, int64_t kv_head_stride, uint8_t *idx_pages,
+                         int64_t idx_page_stride, int64_t num_pages, uint16_t *q_out,
+                         uint16_t *iq_out, void *stream);
+
+/* ---------------------------------------------------------------------------
  * index_score -- the index scorer (the scorers that read [pages, 128, 64] /
  * [pages, 128, 4] index-key views, "mxfp4_pages" / mxfp4_page_views).
  *

@@ -18,7 +18,7 @@ import threading
 
 import torch
 
-__all__ = ["mx4_insert", "index_score", "topk_select", "sparse_paged_decode",
+__all__ = ["mx4_insert", "mx4_norm_rope_insert", "index_score", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
            "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
            "mx4_last_error", "mx4_page_bytes", "library_path", "Mx4Error", "PAGE_BYTES",
@@ -66,6 +66,10 @@ def _load():
         lib.mx4_page_bytes.argtypes = []
         lib.mx4_insert.restype = i32
         lib.mx4_insert.argtypes = [P, P, P, i64, i32, P, P, P, i64, i64, P, i64, i64, P]
+        lib.mx4_norm_rope_insert.restype = i32
+        lib.mx4_norm_rope_insert.argtypes = [P, P, P, P, P, i64, i32, i32, P, P, i64, P, P, P, P,
+                                             ctypes.c_float, P, P, P, i64, i64, P, i64, i64, P,
+                                             P, P]
         lib.index_score.restype = i32
         lib.index_score.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, P]
         lib.topk_select.restype = i32
@@ -104,6 +108,8 @@ def _check(rc: int):
 
 
 def _need(t, dtype, name, contiguous=True):
+    if t.device.type != "cuda":
+        raise ValueError(f"{name}: must be a CUDA tensor, got one on {t.device}")
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if contiguous and not t.is_contiguous():
@@ -142,6 +148,46 @@ def mx4_insert(k, v, idx_k, slot_mapping, k_pages, v_pages, idx_pages, stream=No
                               _ptr(k_pages), _ptr(v_pages), k_pages.stride(0), k_pages.stride(1),
                               _ptr(idx_pages), idx_pages.stride(0), int(k_pages.shape[0]),
                               _stream(stream)))
+
+
+def mx4_norm_rope_insert(q, iq, k, v, idx_k, positions, cos_sin, g_q, g_k, g_iq, g_ik, eps,
+                         slot_mapping, k_pages, v_pages, idx_pages, q_out, iq_out, stream=None):
+    """RMS-norm (weights g_*) and rotary turn (cos_sin [max_pos, 128] = [cos | sin],
+    row positions[t]) of the new tokens' q [T,H,128] and index-q [T,128] heads
+    -> bf16 q_out, iq_out; of their K and index-K heads -> MXFP4 page rows, with V
+    inserted unchanged (all fp32 inputs)."""
+    for t, name in ((q, "q"), (iq, "iq"), (k, "k"), (v, "v"), (idx_k, "idx_k"),
+                    (cos_sin, "cos_sin"), (g_q, "g_q"), (g_k, "g_k"), (g_iq, "g_iq"),
+                    (g_ik, "g_ik")):
+        _need(t, torch.float32, name)
+    _need(positions, torch.int64, "positions")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _need(q_out, torch.bfloat16, "q_out")
+    _need(iq_out, torch.bfloat16, "iq_out")
+    _pages(k_pages, "k_pages", 3)
+    _pages(v_pages, "v_pages", 3)
+    _pages(idx_pages, "idx_pages", 2)
+    if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    if q.dim() != 3 or k.dim() != 3:
+        raise ValueError("q must be [T, H, 128] and k [T, Hkv, 128]")
+    T, H, Hkv = int(q.shape[0]), int(q.shape[1]), int(k.shape[1])
+    want = {"q": (q, (T, H, 128)), "iq": (iq, (T, 128)), "k": (k, (T, Hkv, 128)),
+            "v": (v, (T, Hkv, 128)), "idx_k": (idx_k, (T, 128)), "positions": (positions, (T,)),
+            "slot_mapping": (slot_mapping, (T,)), "q_out": (q_out, (T, H, 128)),
+            "iq_out": (iq_out, (T, 128)), "g_q": (g_q, (128,)), "g_k": (g_k, (128,)),
+            "g_iq": (g_iq, (128,)), "g_ik": (g_ik, (128,))}
+    for name, (t, shape) in want.items():
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
+    if cos_sin.dim() != 2 or cos_sin.shape[1] != 128:
+        raise ValueError("cos_sin must be [max_pos, 128] (cosines | sines)")
+    _check(_load().mx4_norm_rope_insert(
+        _ptr(q), _ptr(iq), _ptr(k), _ptr(v), _ptr(idx_k), T, H, Hkv, _ptr(positions),
+        _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(g_q), _ptr(g_k), _ptr(g_iq), _ptr(g_ik),
+        float(eps), _ptr(slot_mapping), _ptr(k_pages), _ptr(v_pages), k_pages.stride(0),
+        k_pages.stride(1), _ptr(idx_pages), idx_pages.stride(0), int(k_pages.shape[0]),
+        _ptr(q_out), _ptr(iq_out), _stream(stream)))
 
 
 def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=None):

@@ -22,6 +22,12 @@ cudaError_t launch_index_score(const uint16_t*, int, const uint8_t*, int64_t, in
 cudaError_t launch_topk(const float*, int64_t, const int32_t*, int64_t, int, int, int32_t*,
                         void*, uint32_t*, int, cudaStream_t);
 size_t topk_workspace_bytes(int64_t, int, int64_t);
+cudaError_t launch_norm_rope_insert(const float*, const float*, const float*, const float*,
+                                    const float*, int64_t, int, int, const int64_t*, const float*,
+                                    int64_t, const float*, const float*, const float*,
+                                    const float*, float, const int64_t*, uint8_t*, uint8_t*,
+                                    int64_t, int64_t, uint8_t*, int64_t, int64_t, uint16_t*,
+                                    uint16_t*, uint32_t*, cudaStream_t);
 cudaError_t launch_decode(const uint16_t*, int64_t, int, const uint8_t*, const uint8_t*, int64_t,
                           int64_t, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
                           float, float*, void*, uint32_t*, cudaStream_t);
@@ -124,6 +130,49 @@ int mx4_insert(const float* k, const float* v, const float* idx_k, int64_t T, in
                                         idx_page_stride, num_pages, d->status,
                                         static_cast<cudaStream_t>(stream)),
                      "mx4_insert");
+}
+
+int mx4_norm_rope_insert(const float* q, const float* iq, const float* k, const float* v,
+                         const float* idx_k, int64_t T, int H, int Hkv, const int64_t* positions,
+                         const float* cos_sin, int64_t max_pos, const float* g_q,
+                         const float* g_k, const float* g_iq, const float* g_ik, float eps,
+                         const int64_t* slot_mapping, uint8_t* k_pages, uint8_t* v_pages,
+                         int64_t kv_page_stride, int64_t kv_head_stride, uint8_t* idx_pages,
+                         int64_t idx_page_stride, int64_t num_pages, uint16_t* q_out,
+                         uint16_t* iq_out, void* stream) {
+  if (T < 0) return fail(MX4_ERR_INVALID, "mx4_norm_rope_insert: T = %lld < 0", (long long)T);
+  if (H < 1 || H > 64 || Hkv < 1 || Hkv > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "mx4_norm_rope_insert: H = %d, Hkv = %d (1..64, 1..8)", H,
+                Hkv);
+  if (!(eps >= 0.f) || !(eps < INFINITY))
+    return fail(MX4_ERR_INVALID, "mx4_norm_rope_insert: eps must be finite and >= 0");
+  if (T == 0) return ok();
+  if (!q || !iq || !k || !v || !idx_k || !positions || !cos_sin || !g_q || !g_k || !g_iq ||
+      !g_ik || !slot_mapping || !k_pages || !v_pages || !idx_pages || !q_out || !iq_out)
+    return fail(MX4_ERR_INVALID, "mx4_norm_rope_insert: NULL pointer");
+  if (max_pos < 1) return fail(MX4_ERR_INVALID, "mx4_norm_rope_insert: max_pos < 1");
+  if (!aligned(q, 16) || !aligned(iq, 16) || !aligned(k, 16) || !aligned(v, 16) ||
+      !aligned(idx_k, 16) || !aligned(cos_sin, 16) || !aligned(g_q, 16) || !aligned(g_k, 16) ||
+      !aligned(g_iq, 16) || !aligned(g_ik, 16) || !aligned(q_out, 8) || !aligned(iq_out, 8))
+    return fail(MX4_ERR_INVALID, "mx4_norm_rope_insert: misaligned array");
+  if (!aligned(k_pages, 16) || !aligned(v_pages, 16) || !aligned(idx_pages, 16) ||
+      kv_page_stride % 16 || kv_head_stride % 16 || idx_page_stride % 16)
+    return fail(MX4_ERR_INVALID,
+                "mx4_norm_rope_insert: pages must be 16-byte aligned with 16-byte strides");
+  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || idx_page_stride < mx4::kPageBytes ||
+      (Hkv > 1 && kv_head_stride < mx4::kPageBytes))
+    return fail(MX4_ERR_INVALID, "mx4_norm_rope_insert: num_pages < 1 or a stride below 8704");
+  if (T * (H + 2 + 2 * Hkv) > (int64_t)8 * 0x7FFFFFFF)
+    return fail(MX4_ERR_UNSUPPORTED, "mx4_norm_rope_insert: T too large");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(
+      mx4::launch_norm_rope_insert(q, iq, k, v, idx_k, T, H, Hkv, positions, cos_sin, max_pos,
+                                   g_q, g_k, g_iq, g_ik, eps, slot_mapping, k_pages, v_pages,
+                                   kv_page_stride, kv_head_stride, idx_pages, idx_page_stride,
+                                   num_pages, q_out, iq_out, d->status,
+                                   static_cast<cudaStream_t>(stream)),
+      "mx4_norm_rope_insert");
 }
 
 int index_score(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx_pages,

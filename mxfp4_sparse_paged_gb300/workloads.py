@@ -33,7 +33,7 @@ K_ROWS, V_ROWS, IDX_ROWS = 0, 1, 2
 _CHUNK = 4096  # tokens per independently seeded chunk of rows
 
 # purposes of the seeded streams
-_P_ROWS, _P_QUERY, _P_LENS, _P_PERM, _P_OUTLIER = 1, 2, 3, 4, 5
+_P_ROWS, _P_QUERY, _P_LENS, _P_PERM, _P_OUTLIER, _P_WRITER = 1, 2, 3, 4, 5, 6
 
 
 @dataclass(frozen=True)
@@ -225,3 +225,30 @@ def algorithmic_bytes(wl: Workload) -> dict:
         "mx4_insert": int(3 * row * ins),
         "selected_tokens": int(sel.sum()),
     }
+
+
+def rope_table(max_pos: int, base: float = 10000.0) -> np.ndarray:
+    """Rotary table fp32 [max_pos, 128]: column i < 64 is cos(p * base^(-i/64)) at
+    row p, column 64 + i the matching sine.  It is an input of the writer like any
+    other (the usual rotary frequencies; any table is a valid one)."""
+    inv = base ** (-np.arange(HEAD_DIM // 2, dtype=np.float64) / (HEAD_DIM // 2))
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+def writer_inputs(T: int, H: int, Hkv: int, seed: int) -> dict:
+    """Pre-norm fp32 rows of T new tokens for the norm + rotary writer: q [T, H, 128],
+    iq [T, 128], k and v [T, Hkv, 128], idx_k [T, 128] (N(0,1) rows, each row
+    times 2^u with u uniform in [-8, 8)), and the four norm weights g_q, g_k, g_iq,
+    g_ik [128] drawn 1 + 0.2 N(0,1)."""
+    g = _rng(seed, _P_WRITER)
+
+    def rows(*shape):
+        x = g.standard_normal(shape + (HEAD_DIM,))
+        return (x * np.exp2(g.uniform(-8, 8, shape + (1,)))).astype(np.float32)
+
+    out = {"q": rows(T, H), "iq": rows(T), "k": rows(T, Hkv), "v": rows(T, Hkv),
+           "idx_k": rows(T)}
+    for n in ("g_q", "g_k", "g_iq", "g_ik"):
+        out[n] = (1.0 + 0.2 * g.standard_normal(HEAD_DIM)).astype(np.float32)
+    return out

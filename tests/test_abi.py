@@ -101,3 +101,22 @@ def test_workspace_sizes(lib):
     assert m.topk_select_workspace(3, 2048, 20000) == 2 * 16 + 48 + 2 * 3 * 8192 * 4
     assert m.topk_select_workspace(64, 2048, 8192) == 0      # no row exceeds the capacity
     assert m.topk_select_workspace(64, 9000, 131072) == 0    # k above the capacity
+
+
+def test_bindings_refuse_host_tensors_before_any_call():
+    # A host pointer handed to a kernel would be read on the device: the binding
+    # refuses it first (no library call, no GPU needed).
+    import torch
+    import mxfp4_sparse_paged_gb300 as m
+    r = torch.zeros((2, 1, 128))
+    pages = torch.zeros((1, 1, 8704), dtype=torch.uint8)
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m.mx4_insert(r, r, r[:, 0], torch.zeros(2, dtype=torch.int64), pages, pages.clone(),
+                     pages[:, 0])
+    with pytest.raises(ValueError, match="CUDA tensor"):
+        m.mx4_norm_rope_insert(torch.zeros((2, 16, 128)), r[:, 0], r, r, r[:, 0],
+                               torch.zeros(2, dtype=torch.int64), torch.zeros((4, 128)),
+                               *(torch.ones(128) for _ in range(4)), 1e-6,
+                               torch.zeros(2, dtype=torch.int64), pages, pages.clone(),
+                               pages[:, 0], torch.zeros((2, 16, 128), dtype=torch.bfloat16),
+                               torch.zeros((2, 128), dtype=torch.bfloat16))

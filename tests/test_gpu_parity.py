@@ -406,3 +406,151 @@ def test_empty_batch_is_a_no_op():
     m.mx4_insert(r, r, r[:, 0], torch.empty(0, dtype=torch.int64, device=DEV), kv, kv.clone(),
                  pages)
     m.mx4_check_status()
+
+
+# ----------------------------------------------------------------- norm + rotary writer
+#
+# The writer's fp32 arithmetic (sum of squares, IEEE square root and divide, the
+# turn) lands within 2e-6 (|z_i| + |z_partner|) of the float64 definition, z the
+# normed row before the turn.  Page bytes must equal the exact quantiser's bytes
+# for fl32(float64 row), or else be what it gives some row inside that band (a
+# value within the band of an E2M1 rounding midpoint or of a power-of-two block
+# maximum); bf16 outputs must lie between the roundings of the band's ends.
+
+_E2M1_MAG = np.array([0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0])
+
+
+def _signed_codes(data):
+    codes = np.empty(128, np.int64)
+    codes[0::2], codes[1::2] = data & 15, data >> 4
+    return np.where(codes & 8, -1.0, 1.0) * _E2M1_MAG[codes & 7]
+
+
+def _quantised_value(x, E):
+    """Signed E2M1 value the exact quantiser gives each x (float64) at block exponent E."""
+    a = np.minimum(np.abs(x) * 2.0 ** -E, 6.0)
+    mag = np.array([oracle.e2m1_value(oracle.round_magnitude(v)) for v in a])
+    return np.sign(x) * mag
+
+
+def _row_in_band(data, scale, y, tol):
+    lo, hi = y - tol, y + tol
+    got = _signed_codes(data)
+    for b in range(4):
+        sl = slice(32 * b, 32 * b + 32)
+        l, h = lo[sl], hi[sl]
+        amin = np.where((l <= 0) & (h >= 0), 0.0, np.minimum(np.abs(l), np.abs(h))).max()
+        amax = np.maximum(np.abs(l), np.abs(h)).max()
+        E = int(scale[b]) - 127
+        if not oracle.block_exponent(amin) <= E <= oracle.block_exponent(amax):
+            return False
+        if not (np.all(_quantised_value(l, E) <= got[sl]) and
+                np.all(got[sl] <= _quantised_value(h, E))):
+            return False
+    return True
+
+
+def _check_quantised(got, want, slots, y, tol, what):
+    """got/want: [P, 8704] pages; row i of y/tol goes to slots[i] (skipped if < 0)."""
+    n_diff = 0
+    gm, wm = got.copy(), want.copy()
+    for i, s in enumerate(slots):
+        if s < 0:
+            continue
+        pg, r = divmod(int(s), 128)
+        d, sc = slice(64 * r, 64 * r + 64), slice(8192 + 4 * r, 8196 + 4 * r)
+        if not (np.array_equal(got[pg, d], want[pg, d]) and
+                np.array_equal(got[pg, sc], want[pg, sc])):
+            n_diff += 1
+            assert _row_in_band(got[pg, d], got[pg, sc], y[i], tol[i]), f"{what} of token {i}"
+        for a in (gm, wm):
+            a[pg, d], a[pg, sc] = 0, 0
+    assert np.array_equal(gm, wm), f"{what}: rows outside the slots were touched"
+    return n_diff
+
+
+def _check_bf16(got, y, tol, what):
+    g = got.float().numpy().reshape(y.shape).astype(np.float64)
+    lo = torch.from_numpy(y - tol).to(torch.bfloat16).double().numpy()
+    hi = torch.from_numpy(y + tol).to(torch.bfloat16).double().numpy()
+    assert np.all((lo <= g) & (g <= hi)), f"{what}: bf16 outside the band"
+    exact = torch.from_numpy(y.astype(np.float32)).to(torch.bfloat16).double().numpy()
+    assert np.mean(g == exact) >= 0.99, f"{what}: too many band-edge roundings"
+
+
+def _norm_rope_band(x, g, cs, pos, eps):
+    y = oracle.norm_rope(x.reshape(-1, 128), g, cs, pos, eps)
+    z = oracle.norm_rope(x.reshape(-1, 128), g, cs, pos, eps, rope=False)
+    return y, 2e-6 * (np.abs(z) + np.abs(np.roll(z, 64, axis=1)))
+
+
+def _writer_gpu(x, pos, cs, eps, slots, P, H, Hkv):
+    d = {n: torch.from_numpy(a).to(DEV) for n, a in x.items()}
+    T = pos.shape[0]
+    kp = torch.full((P, Hkv, 8704), 0xFF, dtype=torch.uint8, device=DEV)
+    vp = torch.full_like(kp, 0xFF)
+    ip = torch.full((P, 8704), 0xFF, dtype=torch.uint8, device=DEV)
+    q_out = torch.zeros((T, H, 128), dtype=torch.bfloat16, device=DEV)
+    iq_out = torch.zeros((T, 128), dtype=torch.bfloat16, device=DEV)
+    m.mx4_norm_rope_insert(d["q"], d["iq"], d["k"], d["v"], d["idx_k"],
+                           torch.from_numpy(pos).to(DEV), torch.from_numpy(cs).to(DEV), d["g_q"],
+                           d["g_k"], d["g_iq"], d["g_ik"], eps, torch.from_numpy(slots).to(DEV),
+                           kp, vp, ip, q_out, iq_out)
+    return kp, vp, ip, q_out, iq_out
+
+
+@pytest.mark.parametrize("H,Hkv", [(16, 1), (4, 2)])
+def test_norm_rope_insert_against_oracle(H, Hkv):
+    T, P, max_pos = 300, 4, 4096
+    x = W.writer_inputs(T, H, Hkv, seed=31 + H)
+    rng = np.random.default_rng(32 + Hkv)
+    pos = rng.integers(0, max_pos, T).astype(np.int64)
+    pos[0], pos[1] = 0, max_pos - 1          # identity turn; last table row
+    for n in ("q", "iq", "k", "idx_k"):
+        x[n][2] = 0.0                        # a zero row stays zero (eps > 0)
+    cs = W.rope_table(max_pos)
+    eps = float(np.float32(1e-6))
+    slots = rng.permutation(P * 128)[:T].astype(np.int64)
+    slots[5] = slots[17] = -1                # tokens that are not cached
+    yq, tq = _norm_rope_band(x["q"], x["g_q"], cs, np.repeat(pos, H), eps)
+    yiq, tiq = _norm_rope_band(x["iq"], x["g_iq"], cs, pos, eps)
+    yk, tk = _norm_rope_band(x["k"], x["g_k"], cs, np.repeat(pos, Hkv), eps)
+    yik, tik = _norm_rope_band(x["idx_k"], x["g_ik"], cs, pos, eps)
+    kp_o = np.full((P, Hkv, 8704), 0xFF, np.uint8)
+    vp_o = kp_o.copy()
+    ip_o = np.full((P, 8704), 0xFF, np.uint8)
+    oracle.mx4_insert(yk.astype(np.float32).reshape(T, Hkv, 128), x["v"],
+                      yik.astype(np.float32), slots, kp_o, vp_o, ip_o)
+
+    kp, vp, ip, q_out, iq_out = _writer_gpu(x, pos, cs, eps, slots, P, H, Hkv)
+    m.mx4_check_status()
+    assert np.array_equal(vp.cpu().numpy(), vp_o)            # V goes in unchanged
+    _check_bf16(q_out.cpu(), yq, tq, "q")
+    _check_bf16(iq_out.cpu(), yiq, tiq, "index-q")
+    assert not q_out[2].any() and not iq_out[2].any()
+    kpn, ipn = kp.cpu().numpy(), ip.cpu().numpy()
+    yk, tk = yk.reshape(T, Hkv, 128), tk.reshape(T, Hkv, 128)
+    nd = sum(_check_quantised(kpn[:, h], kp_o[:, h], slots, yk[:, h], tk[:, h], f"K head {h}")
+             for h in range(Hkv))
+    nd += _check_quantised(ipn, ip_o, slots, yik, tik, "index-K")
+    assert nd <= 0.02 * T * (Hkv + 1)
+
+
+def test_norm_rope_insert_bad_position_is_flagged_and_skipped():
+    H, Hkv, P, max_pos = 16, 1, 1, 64
+    x = W.writer_inputs(4, H, Hkv, seed=3)
+    cs = W.rope_table(max_pos)
+    pos = np.array([0, 63, 64, -1], np.int64)
+    slots = np.arange(4, dtype=np.int64)
+    kp, vp, ip, q_out, iq_out = _writer_gpu(x, pos, cs, 1e-6, slots, P, H, Hkv)
+    with pytest.raises(m.Mx4Error) as ei:
+        m.mx4_check_status()
+    assert ei.value.bits & 0x8
+    vp_o = np.full((P, Hkv, 8704), 0xFF, np.uint8)
+    oracle.mx4_insert(None, x["v"][:2], None, slots[:2], vp_o.copy(), vp_o, None)
+    assert np.array_equal(vp.cpu().numpy(), vp_o)           # tokens 2, 3 left alone
+    assert q_out[:2].any() and not q_out[2:].any() and not iq_out[2:].any()
+    # no tokens: nothing to do, nothing flagged
+    e = {n: a[:0] if a.ndim > 1 else a for n, a in x.items()}
+    _writer_gpu(e, pos[:0], cs, 1e-6, slots[:0], P, H, Hkv)
+    m.mx4_check_status()
