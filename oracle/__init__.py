@@ -8,7 +8,7 @@ The arithmetic lives in ``mx4_oracle.c`` (plain C, float64); this module only
 compiles it with gcc and marshals numpy arrays through ctypes.  Every function
 below mirrors one C function; their docstrings restate what it computes and
 the source it follows (see the C file's header for the page citations and the
-readings R1..R9 taken where the pages are silent).
+readings R1..R14 taken where the pages are silent).
 """
 from __future__ import annotations
 

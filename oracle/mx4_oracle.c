@@ -40,15 +40,15 @@
  *   R3  the exponent is clamped to [-127, 127];
  *   R4  the element code keeps the sign of x even when the magnitude rounds to
  *       zero (x < 0 -> code 0x8);
- *   R5  a negative slot means "do not insert this token";
- *   R6  token j (0-based) of a sequence with q decode tokens sits at position
+ *   R6  a negative slot means "do not insert this token";
+ *   R7  token j (0-based) of a sequence with q decode tokens sits at position
  *       seq_len - q + j and sees cached tokens 0 .. that position;
- *   R7  the index score is the plain dot product of the index-q head with the
+ *   R8  the index score is the plain dot product of the index-q head with the
  *       dequantised index key (no weight, no activation, no scale);
- *   R8  top-k ties go to the lower token index; the selected indices are
+ *   R9  top-k ties go to the lower token index; the selected indices are
  *       returned in ascending order, padded with -1;
- *   R9  attention is softmax(scale * q.K) V over the selected tokens only.
- *   R10 the writer in front of the insert ([layer] SparseMoeLayer: g_q, g_k,
+ *   R10 attention is softmax(scale * q.K) V over the selected tokens only.
+ *   R14 the writer in front of the insert ([layer] SparseMoeLayer: g_q, g_k,
  *       g_iq, g_ik, cos_sin; no formula printed): each q, k, index-q and
  *       index-k head row is RMS-normed over its 128 dims (mean of squares plus
  *       eps, times the weight g) and then rotated: dims i and i+64 (i < 64) are
@@ -226,7 +226,7 @@ int orc_mx4_insert(const float *k, const float *v, const float *idx_k, int64_t T
     for (t = 0; t < T; ++t) {
         int64_t s = slot_mapping[t], page;
         int row;
-        if (s < 0) continue;                                  /* R5 */
+        if (s < 0) continue;                                  /* R6 */
         page = s / ORC_PAGE_TOKENS;
         row = (int)(s % ORC_PAGE_TOKENS);
         if (page >= num_pages) return ORC_ERR_BOUNDS;
@@ -275,7 +275,7 @@ static double bf16_to_double(uint16_t bits)
 }
 
 /* ------------------------------------------------------------------------- */
-/* a2: index scores, readings R6, R7                                          */
+/* a2: index scores, readings R7, R8                                          */
 /* ------------------------------------------------------------------------- */
 
 /* For decode token t = s*q + j (position p = seq_len[s] - q + j):
@@ -325,7 +325,7 @@ int orc_index_score(const uint16_t *iq, int64_t B, int q, const uint8_t *idx_pag
 }
 
 /* ------------------------------------------------------------------------- */
-/* a3: top-k selection, reading R8                                            */
+/* a3: top-k selection, reading R9                                            */
 /* ------------------------------------------------------------------------- */
 
 /* One candidate of the selection: its score and its token index. */
@@ -334,7 +334,7 @@ struct orc_cand {
     int64_t index;
 };
 
-/* Order for qsort: larger score first, then lower index (R8).  The order is
+/* Order for qsort: larger score first, then lower index (R9).  The order is
  * total, so the result does not depend on the sort's stability. */
 static int cand_order(const void *pa, const void *pb)
 {
@@ -386,7 +386,7 @@ int orc_topk_select(const double *scores, int64_t ld, const int32_t *seq_lens, i
 }
 
 /* ------------------------------------------------------------------------- */
-/* a4: GQA attention over the selected tokens, reading R9                     */
+/* a4: GQA attention over the selected tokens, reading R10                    */
 /* ------------------------------------------------------------------------- */
 
 /* For decode token t of sequence s and query head h (KV head h / (H/Hkv)):
@@ -463,7 +463,7 @@ done:
 }
 
 /* ------------------------------------------------------------------------- */
-/* The writer's norm and rotary embedding, R10 ([layer] SparseMoeLayer):
+/* The writer's norm and rotary embedding, R14 ([layer] SparseMoeLayer):
  *   z_j = x_j * g_j / sqrt(mean_j x_j^2 + eps)
  *   y_i = z_i c_i - z_{i+64} s_i,  y_{i+64} = z_{i+64} c_i + z_i s_i   (i < 64)
  * with c_i = cos_sin[pos][i], s_i = cos_sin[pos][64 + i]; rope = 0 skips the
