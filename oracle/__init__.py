@@ -8,7 +8,7 @@ The arithmetic lives in ``mx4_oracle.c`` (plain C, float64); this module only
 compiles it with gcc and marshals numpy arrays through ctypes.  Every function
 below mirrors one C function; their docstrings restate what it computes and
 the source it follows (see the C file's header for the page citations and the
-readings R1..R14 taken where the pages are silent).
+readings R1..R16 taken where the pages are silent).
 """
 from __future__ import annotations
 
@@ -81,6 +81,15 @@ def _load():
         lib.orc_sparse_paged_decode.restype = i32
         lib.orc_sparse_paged_decode.argtypes = [P, i64, i32, i32, i32, P, P, i64, i64, i64,
                                                 P, i64, P, P, i32, ctypes.c_double, P]
+        lib.orc_e4m3_value.restype = ctypes.c_double
+        lib.orc_e4m3_value.argtypes = [i32]
+        lib.orc_e4m3_encode.restype = i32
+        lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.orc_fp8_index_insert.restype = i32
+        lib.orc_fp8_index_insert.argtypes = [P, i64, P, ctypes.c_float, P, i64, i64]
+        lib.orc_index_score_fp8.restype = i32
+        lib.orc_index_score_fp8.argtypes = [P, i64, i32, P, i64, i64, P, i64, P, ctypes.c_float,
+                                            P, P, i64]
         lib.orc_page_bytes.restype = i32
         _lib = lib
         return lib
@@ -267,3 +276,55 @@ def sparse_paged_decode(q_bits, q_per_seq, k_pages, v_pages, block_table, seq_le
                                      topk.shape[1], float(scale), _ptr(out))
     _check(rc, "sparse_paged_decode")
     return out
+
+
+# --------------------------------------------------------------------------
+# the fp8 index cache variant
+# --------------------------------------------------------------------------
+
+FP8_ROW_BYTES = 128
+FP8_PAGE_BYTES = PAGE_TOKENS * FP8_ROW_BYTES
+
+
+def e4m3_value(code: int) -> float:
+    """Value of an FP8 E4M3 code (OCP); NaN for S.1111.111."""
+    return _load().orc_e4m3_value(int(code))
+
+
+def e4m3_encode(y: float) -> int:
+    """E4M3 code of the fp32 value y: nearest, ties to even, saturating at 448."""
+    return _load().orc_e4m3_encode(float(y))
+
+
+def fp8_index_insert(idx_k, slot_mapping, scale, pages):
+    """Insert index-K rows (fp32 [T, 128]) into fp8 pages (uint8 [P, 16384]), in
+    place: code E4M3(fl32(x / scale)) per element."""
+    idx_k = _c(idx_k, np.float32).reshape(-1, ROW_ELEMS)
+    slot_mapping = _c(slot_mapping, np.int64)
+    assert pages.dtype == np.uint8 and pages.flags.c_contiguous
+    assert pages.shape[1] == FP8_PAGE_BYTES
+    rc = _load().orc_fp8_index_insert(_ptr(idx_k), idx_k.shape[0], _ptr(slot_mapping),
+                                      ctypes.c_float(scale), _ptr(pages), pages.strides[0],
+                                      pages.shape[0])
+    _check(rc, "fp8_index_insert")
+
+
+def index_score_fp8(iq_bits, q_per_seq, pages, block_table, seq_lens, scale, ld,
+                    want_mag=False):
+    """Index scores over the fp8 cache, float64 [T, ld] (and sum of |terms| if
+    want_mag).  iq_bits: bf16 bit patterns, uint16 [T, 128]."""
+    lib = _load()
+    iq_bits = _c(iq_bits, np.uint16)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    B = seq_lens.shape[0]
+    T = iq_bits.shape[0]
+    assert T == B * q_per_seq
+    scores = np.empty((T, ld), np.float64)
+    mag = np.empty((T, ld), np.float64) if want_mag else None
+    rc = lib.orc_index_score_fp8(_ptr(iq_bits), B, int(q_per_seq), _ptr(pages), pages.strides[0],
+                                 pages.shape[0], _ptr(block_table), block_table.shape[1],
+                                 _ptr(seq_lens), ctypes.c_float(scale), _ptr(scores), _ptr(mag),
+                                 ld)
+    _check(rc, "index_score_fp8")
+    return (scores, mag) if want_mag else scores

@@ -27,12 +27,18 @@
  *   [layer]  "vllm.models.minimax_m3.amd.mono.weights" -- SparseMoeLayer (the norm
  *            weights g_q, g_k, g_iq, g_ik and the rotary table cos_sin a layer's
  *            kernels read).
+ *   [fp8]    "vllm.models.minimax_m3.amd.mono.weights" -- SparseMoeLayer (index_cache
+ *            [blocks, block, head_dim] fp8, shared block ids) and
+ *            "vllm.models.minimax_m3.amd.mono.dispatch" -- _config_refusal (the
+ *            index cache dtype must be fp8): the other revision's index-K cache.
  *   [OCP]    OCP Microscaling Formats (MX) v1.0 -- the FP4 E2M1 element type
  *            (1 sign, 2 exponent bits with bias 1, 1 mantissa bit, no inf/NaN),
  *            the E8M0 scale type (2^(byte-127), 0xFF = NaN) and the conversion of
  *            a 32-element block: shared exponent floor(log2(amax)) - emax_elem
  *            with emax_elem = 2 for E2M1, elements rounded to nearest, ties to
- *            even, saturating at the largest normal.
+ *            even, saturating at the largest normal; and the FP8 E4M3 element
+ *            type (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
+ *            inf, S.1111.111 = NaN, largest normal 448).
  *
  * Readings taken where the pages are silent (each also listed in the design doc):
  *   R1  scale b of a row covers the contiguous elements 32b .. 32b+31;
@@ -54,6 +60,13 @@
  *       eps, times the weight g) and then rotated: dims i and i+64 (i < 64) are
  *       a pair turned by the angle whose cosine and sine are cos_sin[pos][i]
  *       and cos_sin[pos][64+i]; V is neither normed nor rotated.
+ *   R15 the fp8 of the [fp8] index cache is OCP E4M3 (the MX element type of
+ *       the same pages' MXFP8 weights), one byte per element, a token row 128 B
+ *       and a page of 128 rows 16384 B;
+ *   R16 that layout has no room for scales, so one fp32 scale S > 0 per cache
+ *       is an argument: the stored code is E4M3(fl32(x / S)), rounded to
+ *       nearest, ties to even, saturating at 448; the element reads back as
+ *       E4M3 value times S.
  */
 #include <math.h>
 #include <stddef.h>
@@ -490,6 +503,130 @@ int orc_norm_rope(const float *x, int64_t n, const float *g, const float *cos_si
             const double c = cs[i], sn = cs[ORC_ROW_ELEMS / 2 + i];
             yr[i] = z[i] * c - z[i + ORC_ROW_ELEMS / 2] * sn;
             yr[i + ORC_ROW_ELEMS / 2] = z[i + ORC_ROW_ELEMS / 2] * c + z[i] * sn;
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* The fp8 index cache variant  [fp8], [OCP], readings R15, R16               */
+/* ------------------------------------------------------------------------- */
+
+/* Value of an E4M3 code: bit 7 sign, bits 6..3 exponent (bias 7), bits 2..0
+ * mantissa.  Exponent field 0 is subnormal: m/8 * 2^(1-7).  Otherwise
+ * (1 + m/8) * 2^(e-7); S.1111.111 is NaN and there is no infinity. */
+double orc_e4m3_value(int code)
+{
+    int sign = (code >> 7) & 1;
+    int e = (code >> 3) & 15;
+    int m = code & 7;
+    double mag;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9);
+    else
+        mag = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/* Round a non-negative double to the nearest integer, ties to the even one. */
+static double round_half_even(double a)
+{
+    double f = floor(a), r = a - f;
+    if (r > 0.5 || (r == 0.5 && fmod(f, 2.0) != 0.0)) f += 1.0;
+    return f;
+}
+
+/* E4M3 code of a finite y (R16): nearest value, ties to the even mantissa,
+ * magnitudes above 448 saturate to 448; the sign bit is kept for values that
+ * round to zero.  Subnormals step by 2^-9; normals with exponent e (2^e <=
+ * |y| < 2^(e+1), -6 <= e <= 8) step by 2^(e-3). */
+int orc_e4m3_encode(float y)
+{
+    int sign = signbit(y) ? 0x80 : 0;
+    double a = fabs((double)y);
+    int e, code;
+    if (a > 448.0) return sign | 0x7E;
+    if (a < ldexp(1.0, -6)) {
+        code = (int)round_half_even(ldexp(a, 9));            /* 0 .. 8; 8 is 2^-6 */
+    } else {
+        double mant;
+        int m;
+        (void)frexp(a, &e);
+        e -= 1;                                               /* 2^e <= a < 2^(e+1) */
+        mant = ldexp(a, -e);                                  /* [1, 2), exact */
+        m = (int)round_half_even((mant - 1.0) * 8.0);        /* 0 .. 8 */
+        if (m == 8) { m = 0; e += 1; }
+        code = ((e + 7) << 3) | m;                            /* <= 0x7E as a <= 448 */
+    }
+    return sign | code;
+}
+
+/* Insert the index-K rows of new tokens into the fp8 cache: for each t with
+ * slot s = slot_mapping[t] >= 0, byte d of row s%128 of page s/128 is
+ * E4M3(fl32(idx_k[t][d] / scale)).  The quotient is rounded to fp32 first,
+ * as an fp32 implementation divides (the precision the code is decided in).
+ * Pages are addressed as base + page*page_stride, rows 128 B apart. */
+int orc_fp8_index_insert(const float *idx_k, int64_t T, const int64_t *slot_mapping,
+                         float scale, uint8_t *pages, int64_t page_stride, int64_t num_pages)
+{
+    int64_t t;
+    int d;
+    if (!(scale > 0.0f) || !isfinite(scale)) return ORC_ERR_INVALID;
+    for (t = 0; t < T; ++t) {
+        int64_t s = slot_mapping[t], page;
+        uint8_t *row;
+        if (s < 0) continue;                                  /* R6 */
+        page = s / ORC_PAGE_TOKENS;
+        if (page >= num_pages) return ORC_ERR_BOUNDS;
+        row = pages + page * page_stride + (s % ORC_PAGE_TOKENS) * ORC_ROW_ELEMS;
+        for (d = 0; d < ORC_ROW_ELEMS; ++d) {
+            float x = idx_k[t * ORC_ROW_ELEMS + d];
+            float y;
+            if (!isfinite(x)) return ORC_ERR_INVALID;
+            y = x / scale;
+            row[d] = (uint8_t)orc_e4m3_encode(y);
+        }
+    }
+    return ORC_OK;
+}
+
+/* Index scores over the fp8 cache: as orc_index_score, with the key element
+ * read back as E4M3 value times scale (R16). */
+int orc_index_score_fp8(const uint16_t *iq, int64_t B, int q, const uint8_t *pages,
+                        int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                        int64_t bt_width, const int32_t *seq_lens, float scale,
+                        double *scores, double *mag, int64_t ld)
+{
+    int64_t s, i;
+    int j, d;
+    for (s = 0; s < B; ++s) {
+        int64_t L = seq_lens[s];
+        if (L < q || L > ld || L > bt_width * ORC_PAGE_TOKENS) return ORC_ERR_BOUNDS;
+        for (j = 0; j < q; ++j) {
+            int64_t t = s * q + j;
+            int64_t p = L - q + j;
+            const uint16_t *qt = iq + t * ORC_ROW_ELEMS;
+            for (i = 0; i < ld; ++i) {
+                double acc = 0.0, acc_abs = 0.0;
+                int64_t pg;
+                const uint8_t *row;
+                if (i > p) {
+                    scores[t * ld + i] = -INFINITY;
+                    if (mag) mag[t * ld + i] = 0.0;
+                    continue;
+                }
+                pg = page_of(block_table, bt_width, s, i, num_pages);
+                if (pg < 0) return ORC_ERR_BOUNDS;
+                row = pages + pg * page_stride + (i % ORC_PAGE_TOKENS) * ORC_ROW_ELEMS;
+                for (d = 0; d < ORC_ROW_ELEMS; ++d) {
+                    double term = bf16_to_double(qt[d]) * (orc_e4m3_value(row[d]) * scale);
+                    acc += term;
+                    acc_abs += fabs(term);
+                }
+                scores[t * ld + i] = acc;
+                if (mag) mag[t * ld + i] = acc_abs;
+            }
         }
     }
     return ORC_OK;

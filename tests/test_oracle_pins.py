@@ -505,3 +505,131 @@ def test_norm_rope_zero_row_and_bad_position():
     assert np.array_equal(y, np.zeros((1, 128)))
     with pytest.raises(Exception):
         oracle.norm_rope(x, np.ones(128, np.float32), cs, [2], 1e-6)
+
+
+# ---------------------------------------------------------------- fp8 index cache (E4M3)
+
+def test_e4m3_hand_values():
+    # OCP E4M3: bias 7, subnormals m/8 * 2^-6, S.1111.111 NaN, largest normal 448
+    hand = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6,
+            0x0F: 1.875 * 2.0 ** -6, 0x38: 1.0, 0x39: 1.125, 0x3F: 1.875, 0x40: 2.0,
+            0x77: 240.0, 0x78: 256.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0}
+    for code, v in hand.items():
+        assert oracle.e4m3_value(code) == v, hex(code)
+    assert math.copysign(1.0, oracle.e4m3_value(0x80)) == -1.0
+    assert math.isnan(oracle.e4m3_value(0x7F)) and math.isnan(oracle.e4m3_value(0xFF))
+
+
+def test_e4m3_values_match_torch_float8():
+    # A library decode of the same format: all 256 codes.
+    lib = torch.arange(256, dtype=torch.uint8).view(torch.float8_e4m3fn).double().numpy()
+    mine = np.array([oracle.e4m3_value(c) for c in range(256)])
+    assert np.array_equal(np.isnan(lib), np.isnan(mine))
+    ok = ~np.isnan(lib)
+    assert np.array_equal(lib[ok], mine[ok])
+    assert np.array_equal(np.signbit(lib[ok]), np.signbit(mine[ok]))
+
+
+def test_e4m3_encode_ties_and_saturation():
+    hand = [(1.0625, 0x38), (1.1875, 0x3A), (2.0 ** -10, 0x00), (3 * 2.0 ** -10, 0x02),
+            (2.0 ** -6 * (1 + 1 / 16), 0x08), (15 * 2.0 ** -10, 0x08), (448.0, 0x7E),
+            (449.0, 0x7E), (464.0, 0x7E), (1e30, 0x7E), (-1e30, 0xFE),
+            (float(np.finfo(np.float32).max), 0x7E), (-0.0, 0x80), (-(2.0 ** -12), 0x80),
+            (0.0, 0x00), (0.1, 0x1D), (-3.3, 0xC5)]
+    for y, code in hand:
+        assert oracle.e4m3_encode(y) == code, (y, hex(code), hex(oracle.e4m3_encode(y)))
+    # every finite code round-trips
+    for c in range(256):
+        if (c & 0x7F) != 0x7F:
+            assert oracle.e4m3_encode(oracle.e4m3_value(c)) == c, hex(c)
+
+
+def test_e4m3_encode_matches_torch_float8_in_range():
+    # torch rounds to nearest even but does not saturate: compare below 464.
+    rng = np.random.default_rng(8)
+    x = (rng.standard_normal(20000) * np.exp2(rng.uniform(-14, 9, 20000))).astype(np.float32)
+    finite = np.array([oracle.e4m3_value(c) for c in range(256) if (c & 0x7F) != 0x7F])
+    mids = (np.sort(finite)[1:] + np.sort(finite)[:-1]) / 2
+    x = np.concatenate([x, mids.astype(np.float32),
+                        np.nextafter(mids.astype(np.float32), np.float32(np.inf)),
+                        np.nextafter(mids.astype(np.float32), np.float32(-np.inf))])
+    x = x[np.abs(x) < 464]
+    lib = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    mine = np.array([oracle.e4m3_encode(v) for v in x], np.uint8)
+    # torch may drop the sign of a value that rounds to zero: compare magnitudes there
+    z = (lib & 0x7F) == 0
+    assert np.array_equal(mine[~z], lib[~z])
+    assert np.all((mine[z] & 0x7F) == 0)
+
+
+def _fp8_fill(P, bt, lens, rows, scale):
+    pages = np.full((P, oracle.FP8_PAGE_BYTES), 0xFF, np.uint8)
+    for s, L in enumerate(lens):
+        slots = np.array([bt[s, i // 128] * 128 + i % 128 for i in range(L)], np.int64)
+        oracle.fp8_index_insert(rows[s], slots, scale, pages)
+    return pages
+
+
+def test_fp8_insert_layout_scale_and_slots():
+    pages = np.full((2, oracle.FP8_PAGE_BYTES), 0xFF, np.uint8)
+    x = np.zeros((3, 128), np.float32)
+    x[0, 0], x[0, 5], x[0, 127] = 3.0, -0.5, 896.0
+    x[1, 1] = 1.0
+    oracle.fp8_index_insert(x, np.array([130, -1, 127]), 2.0, pages)
+    row = pages[1, 2 * 128:3 * 128]                       # slot 130: page 1, row 2
+    assert row[0] == 0x3C and row[5] == 0xA8 and row[127] == 0x7E   # 1.5, -0.25, 448
+    assert np.all(np.delete(row, [0, 5, 127]) == 0)
+    assert np.all(pages[0, 127 * 128:] == 0)              # slot 127: the zero row x[2]
+    untouched = np.ones_like(pages, bool)
+    untouched[1, 256:384] = False
+    untouched[0, 127 * 128:] = False
+    assert np.all(pages[untouched] == 0xFF)              # slot -1 wrote nothing
+    with pytest.raises(ValueError):
+        oracle.fp8_index_insert(x[:1], np.array([256]), 1.0, pages)
+    with pytest.raises(ValueError):
+        oracle.fp8_index_insert(x[:1], np.array([0]), 0.0, pages)
+
+
+def test_fp8_index_score_exact_small_case_and_causal_bound():
+    # Keys decoded by torch's float8 type, queries small integers, scale a power of
+    # two: the exact score is a rational number computed here with Fractions.
+    rng = np.random.default_rng(23)
+    lens = [130, 9]
+    bt = np.array([[2, 0], [1, -1]], np.int32)
+    scale = 0.25
+    rows = [(rng.standard_normal((L, 128)) * 4).astype(np.float32) for L in lens]
+    pages = _fp8_fill(3, bt, lens, rows, scale)
+    q = 2
+    iqf = rng.integers(-3, 4, (4, 128)).astype(np.float32)
+    ld = 140
+    sc = oracle.index_score_fp8(W.to_bf16_bits(iqf), q, pages, bt, np.array(lens, np.int32),
+                                scale, ld)
+    dec = torch.from_numpy(pages).view(torch.float8_e4m3fn).double().numpy()
+    for s in range(2):
+        for j in range(q):
+            t = s * q + j
+            p = lens[s] - q + j
+            for i in range(ld):
+                if i > p:
+                    assert sc[t, i] == -np.inf
+                    continue
+                pg = bt[s, i // 128]
+                key = dec[pg, (i % 128) * 128:(i % 128 + 1) * 128]
+                exact = sum(Fraction(int(iqf[t, d])) * Fraction(float(key[d])) * Fraction(scale)
+                            for d in range(128))
+                assert sc[t, i] == float(exact)
+
+
+def test_fp8_index_score_unit_query_reads_one_element_times_scale():
+    rng = np.random.default_rng(3)
+    rows = [(rng.standard_normal((200, 128)) * 100).astype(np.float32)]
+    bt = np.array([[1, 0]], np.int32)
+    pages = _fp8_fill(2, bt, [200], rows, 8.0)
+    dec = torch.from_numpy(pages).view(torch.float8_e4m3fn).double().numpy()
+    for d in (0, 3, 64, 127):
+        iqf = np.zeros((1, 128), np.float32)
+        iqf[0, d] = 1.0
+        sc = oracle.index_score_fp8(W.to_bf16_bits(iqf), 1, pages, bt, np.array([200], np.int32),
+                                    8.0, 200)
+        want = [dec[bt[0, i // 128], (i % 128) * 128 + d] * 8.0 for i in range(200)]
+        assert np.array_equal(sc[0], want)
