@@ -40,6 +40,7 @@ from mxfp4_sparse_paged_gb300 import workloads as W  # noqa: E402
 
 METRIC = "sparse MXFP4 paged-decode tokens/s"
 UNIT = "tokens/s"
+FP8_INDEX_SCALE = 0.25  # per-cache scale of the fp8 index-K variant: |row| / 0.25 stays below 448
 
 
 def _peaks():
@@ -199,7 +200,9 @@ def run_gpu(args):
             dist.barrier()
 
     wl = W.make(args.workload)
-    caches = PagedCaches(wl.num_pages, device=dev)
+    # The fill also writes the fp8 index-K cache variant from the same rows; the timed
+    # step reads only the MXFP4 pools.
+    caches = PagedCaches(wl.num_pages, device=dev, fp8_index_scale=FP8_INDEX_SCALE)
     caches.fill(wl)
     step = DecodeStep(wl, caches, device=dev)
     host = step_inputs_host(wl)
@@ -288,6 +291,7 @@ def run_gpu(args):
     m.mx4_check_status()
 
     writer = time_writer(wl, dev, stream, flush_l2, min(args.steps, 200))
+    fp8 = time_fp8_scorer(wl, caches, step, stream, flush_l2, min(args.steps, 200))
 
     peak, peak_kind = _peaks()
     score_s = kern_ms["index_score"] / 1e3
@@ -321,6 +325,9 @@ def run_gpu(args):
                         "(two buffer sets, three streams, one packed input copy and one CUDA-graph "
                         "launch a step); no L2 flush (a step moves more than the L2 holds)"},
         "norm_rope_writer": writer,
+        "fp8_index_variant": dict(fp8, mxfp4_index_score_us=round(kern_ms["index_score"] * 1e3, 2),
+                                  peak_gbs=peak,
+                                  frac=round(fp8["achieved_gbs"] / peak, 4)),
         "gpu_launches": step.launches_per_step() * args.steps,
         "clocks": ck,
         "wall_s_timed_region": round(wall, 3),
@@ -333,6 +340,41 @@ def run_gpu(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def time_fp8_scorer(wl, caches, step, stream, flush_l2, steps):
+    """index_score_fp8 over the fp8 (E4M3) index-K cache, filled from the same rows as
+    the MXFP4 one, with the step's index-q, block table and lengths: event-timed per
+    launch on the launching stream after an L2 flush.  Algorithmic bytes: one 128-byte
+    key row per cached token."""
+    import torch
+
+    import mxfp4_sparse_paged_gb300 as m
+    if step.slots.numel():  # the decode tokens' own rows, as the step inserts them
+        m.fp8_index_insert(step.idx_new, step.slots, caches.fp8_index_scale, caches.fp8_idx_pages,
+                           stream=stream)
+
+    def score():
+        m.index_score_fp8(step.iq, wl.q, caches.fp8_idx_pages, step.block_table, step.seq_lens,
+                          caches.fp8_index_scale, step.scores, stream=stream)
+
+    for _ in range(3):
+        flush_l2(1)
+        score()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(i & 0xFF)
+        evs[i][0].record(stream)
+        score()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    m.mx4_check_status()
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    nbytes = int(W.HEAD_DIM * wl.seq_lens.astype(np.int64).sum())
+    return {"kernel": "index_score_fp8", "scale": caches.fp8_index_scale, "us": round(us, 2),
+            "algorithmic_bytes": nbytes, "achieved_gbs": round(nbytes / us / 1e3, 1),
+            "timing": "mean of CUDA-event pairs on the launching stream, L2 flushed before each"}
 
 
 def time_writer(wl, dev, stream, flush_l2, steps):

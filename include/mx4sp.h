@@ -66,6 +66,7 @@ typedef enum {
 #define MX4_PAGE_TOKENS 128
 #define MX4_HEAD_DIM 128
 #define MX4_PAGE_BYTES 8704
+#define MX4_FP8_PAGE_BYTES 16384 /* fp8 index-K cache page: 128 rows x 128 E4M3 bytes */
 
 /* Reason for the last non-OK return on this thread ("" if none). */
 const char *mx4_last_error(void);
@@ -242,6 +243,42 @@ int sparse_paged_decode_noalloc(const uint16_t *q, int64_t T, int q_per_seq, int
                                 int64_t bt_width, const int32_t *seq_lens,
                                 const int32_t *topk_idx, int k, float scale, float *out,
                                 void *stream);
+
+/* ---------------------------------------------------------------------------
+ * The fp8 index-K cache variant ("vllm.models.minimax_m3.amd.mono.weights",
+ * SparseMoeLayer.index_cache: [blocks, block, head_dim] fp8 with the block ids
+ * of the K/V cache; "vllm.models.minimax_m3.amd.mono.dispatch",
+ * _config_refusal: the index cache dtype is fp8).  A page holds 128 token rows
+ * of 128 OCP E4M3 bytes (MX4_FP8_PAGE_BYTES), row r at byte r*128.  The layout
+ * has no scale bytes: one fp32 scale S > 0 per cache is an argument.
+ *
+ * fp8_index_insert -- for each new token t with slot s = slot_mapping[t] >= 0,
+ * byte d of row s%128 of page s/128 becomes E4M3(fl32(idx_k[t][d] / S)):
+ * the IEEE fp32 quotient rounded to the nearest E4M3 value, ties to even,
+ * magnitudes past 448 saturating to 448, the sign kept for a quotient that
+ * rounds to zero.  Negative slots are skipped; a slot past the pool skips the
+ * token (MX4_STATUS_BAD_SLOT); a non-finite input is written as the conversion
+ * gives it and sets MX4_STATUS_BAD_VALUE.
+ *
+ *   idx_k         fp32 [T, 128], contiguous, 16-byte aligned
+ *   slot_mapping  int64 [T]
+ *   pages         uint8 [num_pages, 16384] at byte stride page_stride
+ *                 (a multiple of 16, at least 16384), written in place
+ *
+ * index_score_fp8 -- index_score over the fp8 cache: for decode token
+ * t = s*q + j at position p = seq_lens[s] - q + j,
+ *     scores[t*ld_scores + i] = S * sum_d iq[t][d] * E4M3value(row i)[d]
+ * for 0 <= i <= p, computed in fp32, -inf for p < i < seq_lens[s], entries at
+ * i >= seq_lens[s] not written.  Arguments, limits and status bits as
+ * index_score, with pages [num_pages, 16384] at page_stride.  An E4M3 NaN byte
+ * (0x7F, 0xFF: the poison of a never-written row) gives a NaN score.
+ * ------------------------------------------------------------------------- */
+int fp8_index_insert(const float *idx_k, int64_t T, const int64_t *slot_mapping, float scale,
+                     uint8_t *pages, int64_t page_stride, int64_t num_pages, void *stream);
+int index_score_fp8(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t *pages,
+                    int64_t page_stride, int64_t num_pages, const int32_t *block_table,
+                    int64_t B, int64_t bt_width, const int32_t *seq_lens, float scale,
+                    float *scores, int64_t ld_scores, void *stream);
 
 /* ---------------------------------------------------------------------------
  * mx4_check_status -- synchronise `stream`, return MX4_OK if no kernel of this

@@ -18,13 +18,14 @@ import threading
 
 import torch
 
-__all__ = ["mx4_insert", "mx4_norm_rope_insert", "index_score", "topk_select", "sparse_paged_decode",
+__all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
            "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
            "mx4_last_error", "mx4_page_bytes", "library_path", "Mx4Error", "PAGE_BYTES",
            "PAGE_TOKENS", "HEAD_DIM"]
 
 PAGE_BYTES = 8704
+FP8_PAGE_BYTES = 16384
 PAGE_TOKENS = 128
 HEAD_DIM = 128
 NOALLOC_SCRATCH_BYTES = 32 << 20
@@ -70,6 +71,11 @@ def _load():
         lib.mx4_norm_rope_insert.argtypes = [P, P, P, P, P, i64, i32, i32, P, P, i64, P, P, P, P,
                                              ctypes.c_float, P, P, P, i64, i64, P, i64, i64, P,
                                              P, P]
+        lib.fp8_index_insert.restype = i32
+        lib.fp8_index_insert.argtypes = [P, i64, P, ctypes.c_float, P, i64, i64, P]
+        lib.index_score_fp8.restype = i32
+        lib.index_score_fp8.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, ctypes.c_float,
+                                        P, i64, P]
         lib.index_score.restype = i32
         lib.index_score.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, P]
         lib.topk_select.restype = i32
@@ -188,6 +194,46 @@ def mx4_norm_rope_insert(q, iq, k, v, idx_k, positions, cos_sin, g_q, g_k, g_iq,
         float(eps), _ptr(slot_mapping), _ptr(k_pages), _ptr(v_pages), k_pages.stride(0),
         k_pages.stride(1), _ptr(idx_pages), idx_pages.stride(0), int(k_pages.shape[0]),
         _ptr(q_out), _ptr(iq_out), _stream(stream)))
+
+
+def _fp8_pages(t, name):
+    _need(t, torch.uint8, name, contiguous=False)
+    if t.dim() != 2 or t.shape[1] != FP8_PAGE_BYTES or t.stride(1) != 1:
+        raise ValueError(f"{name}: uint8 pages need shape [P, {FP8_PAGE_BYTES}] with a "
+                         f"contiguous byte axis, got {tuple(t.shape)} strides {t.stride()}")
+
+
+def fp8_index_insert(idx_k, slot_mapping, scale, pages, stream=None):
+    """Quantise new tokens' index-K rows (fp32 [T, 128]) into the fp8 (E4M3) index
+    cache pages [P, 16384] through slot_mapping (int64 [T]), code E4M3(x / scale)."""
+    _need(idx_k, torch.float32, "idx_k")
+    _need(slot_mapping, torch.int64, "slot_mapping")
+    _fp8_pages(pages, "pages")
+    if idx_k.dim() != 2 or idx_k.shape[1] != 128 or tuple(slot_mapping.shape) != (idx_k.shape[0],):
+        raise ValueError("idx_k must be [T, 128] and slot_mapping [T]")
+    _check(_load().fp8_index_insert(_ptr(idx_k), int(idx_k.shape[0]), _ptr(slot_mapping),
+                                    float(scale), _ptr(pages), pages.stride(0),
+                                    int(pages.shape[0]), _stream(stream)))
+
+
+def index_score_fp8(iq, q_per_seq, pages, block_table, seq_lens, scale, scores, stream=None):
+    """index_score over the fp8 index cache: scale * iq . E4M3 row, fp32 [T, ld]."""
+    _need(iq, torch.bfloat16, "iq")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(scores, torch.float32, "scores", contiguous=False)
+    _fp8_pages(pages, "pages")
+    if scores.stride(1) != 1:
+        raise ValueError("scores: the token axis must be contiguous")
+    B = int(seq_lens.shape[0])
+    if iq.dim() != 2 or iq.shape[1] != 128 or iq.shape[0] != B * q_per_seq:
+        raise ValueError("iq must be [B * q_per_seq, 128]")
+    if block_table.dim() != 2 or block_table.shape[0] != B or scores.shape[0] != iq.shape[0]:
+        raise ValueError("block_table must be [B, width] and scores [T, ld]")
+    _check(_load().index_score_fp8(_ptr(iq), int(iq.shape[0]), int(q_per_seq), _ptr(pages),
+                                   pages.stride(0), int(pages.shape[0]), _ptr(block_table), B,
+                                   int(block_table.shape[1]), _ptr(seq_lens), float(scale),
+                                   _ptr(scores), scores.stride(0), _stream(stream)))
 
 
 def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=None):

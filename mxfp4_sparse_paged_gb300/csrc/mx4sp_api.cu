@@ -32,6 +32,11 @@ cudaError_t launch_decode(const uint16_t*, int64_t, int, const uint8_t*, const u
                           int64_t, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
                           float, float*, void*, uint32_t*, cudaStream_t);
 size_t decode_workspace_bytes(int64_t, int);
+cudaError_t launch_fp8_index_insert(const float*, int64_t, const int64_t*, float, uint8_t*,
+                                    int64_t, int64_t, uint32_t*, cudaStream_t);
+cudaError_t launch_index_score_fp8(const uint16_t*, int, const uint8_t*, int64_t, int64_t,
+                                   const int32_t*, int, int64_t, const int32_t*, float, float*,
+                                   int64_t, uint32_t*, int, cudaStream_t);
 }  // namespace mx4
 
 // Device status word: kernels OR MX4_STATUS_* bits into it when they skip bad
@@ -198,6 +203,58 @@ int index_score(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx
                                              scores, ld_scores, d->status, d->num_sms,
                                              static_cast<cudaStream_t>(stream)),
                      "index_score");
+}
+
+int fp8_index_insert(const float* idx_k, int64_t T, const int64_t* slot_mapping, float scale,
+                     uint8_t* pages, int64_t page_stride, int64_t num_pages, void* stream) {
+  if (T < 0) return fail(MX4_ERR_INVALID, "fp8_index_insert: T = %lld < 0", (long long)T);
+  if (!(scale > 0.f) || !(scale < INFINITY))
+    return fail(MX4_ERR_INVALID, "fp8_index_insert: scale must be finite and > 0");
+  if (T == 0) return ok();
+  if (!idx_k || !slot_mapping || !pages)
+    return fail(MX4_ERR_INVALID, "fp8_index_insert: NULL pointer");
+  if (!aligned(idx_k, 16) || !aligned(pages, 16) || page_stride % 16)
+    return fail(MX4_ERR_INVALID, "fp8_index_insert: misaligned rows, pages or page stride");
+  if (num_pages < 1 || page_stride < MX4_FP8_PAGE_BYTES)
+    return fail(MX4_ERR_INVALID, "fp8_index_insert: num_pages < 1 or a stride below 16384");
+  if (T > (int64_t)8 * 0x7FFFFFFF)
+    return fail(MX4_ERR_UNSUPPORTED, "fp8_index_insert: T too large");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(mx4::launch_fp8_index_insert(idx_k, T, slot_mapping, scale, pages,
+                                                  page_stride, num_pages, d->status,
+                                                  static_cast<cudaStream_t>(stream)),
+                     "fp8_index_insert");
+}
+
+int index_score_fp8(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* pages,
+                    int64_t page_stride, int64_t num_pages, const int32_t* block_table,
+                    int64_t B, int64_t bt_width, const int32_t* seq_lens, float scale,
+                    float* scores, int64_t ld_scores, void* stream) {
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "index_score_fp8: q_per_seq = %d (supported 1..8)",
+                q_per_seq);
+  if (B < 0 || B > 65535)
+    return fail(MX4_ERR_UNSUPPORTED, "index_score_fp8: B = %lld", (long long)B);
+  if (T != B * q_per_seq)
+    return fail(MX4_ERR_INVALID, "index_score_fp8: T = %lld != B * q_per_seq", (long long)T);
+  if (!(scale > 0.f) || !(scale < INFINITY))
+    return fail(MX4_ERR_INVALID, "index_score_fp8: scale must be finite and > 0");
+  if (B == 0) return ok();
+  if (!iq || !pages || !block_table || !seq_lens || !scores)
+    return fail(MX4_ERR_INVALID, "index_score_fp8: NULL pointer");
+  if (!aligned(iq, 16) || !aligned(pages, 16) || page_stride % 16 || !aligned(scores, 4))
+    return fail(MX4_ERR_INVALID, "index_score_fp8: misaligned iq, pages or page stride");
+  if (num_pages < 1 || page_stride < MX4_FP8_PAGE_BYTES || bt_width < 1 || ld_scores < 1)
+    return fail(MX4_ERR_INVALID,
+                "index_score_fp8: num_pages, page stride, bt_width or ld invalid");
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(mx4::launch_index_score_fp8(iq, q_per_seq, pages, page_stride, num_pages,
+                                                 block_table, (int)B, bt_width, seq_lens, scale,
+                                                 scores, ld_scores, d->status, d->num_sms,
+                                                 static_cast<cudaStream_t>(stream)),
+                     "index_score_fp8");
 }
 
 size_t topk_select_workspace(int64_t T, int k, int64_t ld_scores) {

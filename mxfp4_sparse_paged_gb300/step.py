@@ -4,7 +4,8 @@
 index-K [pages, 8704]) in device memory, poisoned with 0xFF so a read of a
 never-written row shows up as NaN, and fills them from a workload with
 mx4_insert through the shared page-128 slot mapping ("vllm.models.minimax_m3.
-amd.mono.dispatch", _slots_shared).
+amd.mono.dispatch", _slots_shared).  Optionally it also holds the fp8 index-K
+cache [pages, 16384] of the other revision, filled from the same rows.
 
 `DecodeStep` holds the per-step buffers and workspaces and issues, on one
 stream, the hot path of a decode step: [mx4_insert of the new tokens] ->
@@ -18,25 +19,38 @@ import math
 import numpy as np
 import torch
 
-from . import (index_score, mx4_insert, sparse_paged_decode, sparse_paged_decode_workspace,
-               topk_select, topk_select_workspace)
+from . import (FP8_PAGE_BYTES, fp8_index_insert, index_score, mx4_insert, sparse_paged_decode,
+               sparse_paged_decode_workspace, topk_select, topk_select_workspace)
 from . import workloads as W
 
 
 class PagedCaches:
-    def __init__(self, num_pages: int, device="cuda", kv_heads: int = 1):
+    """Resident page pools: MXFP4 K, V and index-K, and optionally the fp8 (E4M3)
+    index-K cache variant with its per-cache scale, filled from the same rows."""
+
+    def __init__(self, num_pages: int, device="cuda", kv_heads: int = 1,
+                 fp8_index_scale: float | None = None):
         self.num_pages = num_pages
         self.k_pages = torch.full((num_pages, kv_heads, W.PAGE_BYTES), W.POISON, dtype=torch.uint8,
                                   device=device)
         self.v_pages = torch.full_like(self.k_pages, W.POISON)
         self.idx_pages = torch.full((num_pages, W.PAGE_BYTES), W.POISON, dtype=torch.uint8,
                                     device=device)
+        self.fp8_index_scale = fp8_index_scale
+        self.fp8_idx_pages = None
+        if fp8_index_scale is not None:
+            self.fp8_idx_pages = torch.full((num_pages, FP8_PAGE_BYTES), W.POISON,
+                                            dtype=torch.uint8, device=device)
 
     def nbytes(self) -> int:
-        return 3 * self.num_pages * W.PAGE_BYTES
+        fp8 = 0 if self.fp8_idx_pages is None else self.num_pages * FP8_PAGE_BYTES
+        return 3 * self.num_pages * W.PAGE_BYTES + fp8
 
-    def insert_rows(self, k, v, idx_k, slots, stream=None):
+    def insert_rows(self, k, v, idx_k, slots, stream=None, fp8=True):
+        """Insert into the MXFP4 pools and (fp8=True, if present) the fp8 index cache."""
         mx4_insert(k, v, idx_k, slots, self.k_pages, self.v_pages, self.idx_pages, stream=stream)
+        if fp8 and self.fp8_idx_pages is not None:
+            fp8_index_insert(idx_k, slots, self.fp8_index_scale, self.fp8_idx_pages, stream=stream)
 
     def fill(self, wl: W.Workload, chunk: int = 32768, sequences=None):
         """Insert tokens 0 .. prefilled(s)-1 of every (or the given) sequence."""
@@ -194,7 +208,7 @@ class DecodeStep:
 
         if self.slots.numel():
             timed("mx4_insert", lambda: c.insert_rows(self.k_new, self.v_new, self.idx_new,
-                                                      self.slots, stream=stream))
+                                                      self.slots, stream=stream, fp8=False))
         timed("index_score", lambda: index_score(self.iq, wl.q, c.idx_pages, self.block_table,
                                                  self.seq_lens, self.scores, stream=stream))
         timed("topk_select", lambda: topk_select(self.scores, self.seq_lens, wl.q, wl.k,

@@ -554,3 +554,141 @@ def test_norm_rope_insert_bad_position_is_flagged_and_skipped():
     e = {n: a[:0] if a.ndim > 1 else a for n, a in x.items()}
     _writer_gpu(e, pos[:0], cs, 1e-6, slots[:0], P, H, Hkv)
     m.mx4_check_status()
+
+
+# ----------------------------------------------------------------- fp8 index cache variant
+
+FP8_PAGE = 16384
+
+
+def _bf16_dev(bits):
+    return torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(DEV)
+
+
+def _fp8_insert_both(rows, slots, scale, P):
+    want = np.full((P, FP8_PAGE), 0xFF, np.uint8)
+    oracle.fp8_index_insert(rows, slots, scale, want)
+    got = torch.full((P, FP8_PAGE), 0xFF, dtype=torch.uint8, device=DEV)
+    m.fp8_index_insert(torch.from_numpy(rows).to(DEV), torch.from_numpy(slots).to(DEV), scale, got)
+    m.mx4_check_status()
+    return got, want
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.37, 2.0 ** -20])
+def test_fp8_index_insert_bit_exact(scale):
+    # Quotients on every E4M3 rounding midpoint and just off it, zeros of both
+    # signs, subnormal and smallest-normal inputs, the saturation edge, and rows
+    # across 30 binades; scattered slots with two skipped tokens.
+    f32 = np.finfo(np.float32)
+    finite = np.array([oracle.e4m3_value(c) for c in range(128) if c != 0x7F])
+    mids = ((finite[1:] + finite[:-1]) / 2).astype(np.float32)
+    vals = np.concatenate([mids, np.nextafter(mids, np.float32(np.inf)),
+                           np.nextafter(mids, np.float32(0)), finite.astype(np.float32)])
+    vals = np.concatenate([vals, -vals])
+    nrow = (len(vals) + 127) // 128
+    rows = np.zeros((nrow + 70, 128), np.float32)
+    rows.reshape(-1)[:len(vals)] = vals * np.float32(scale)
+    r = nrow
+    rows[r + 1] = -0.0
+    rows[r + 2, :6] = np.array([448, 449, 464, 465, 1e30, -1e30]) * scale
+    rows[r + 2, 6] = -f32.max
+    rows[r + 3] = f32.tiny
+    rows[r + 4] = np.float32(2.0 ** -149)
+    rows[r + 5, :4] = np.array([2.0 ** -10, -2.0 ** -10, 2.0 ** -12, -2.0 ** -12]) * scale
+    rng = np.random.default_rng(17)
+    k = rows.shape[0] - (r + 6)
+    rows[r + 6:] = (rng.standard_normal((k, 128)) * np.exp2(rng.uniform(-12, 10, (k, 1))) *
+                    scale).astype(np.float32)
+    n = rows.shape[0]
+    P = (n + 127) // 128 + 1
+    slots = rng.permutation(P * 128)[:n].astype(np.int64)
+    slots[3] = slots[40] = -1
+    got, want = _fp8_insert_both(rows, slots, scale, P)
+    assert np.array_equal(got.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("q", [1, 3])
+def test_index_score_fp8_ragged_and_topk_chain(q):
+    rng = np.random.default_rng(40 + q)
+    lens = np.array([q, 127, 128, 129, 700, 1500, 2049, 4100], np.int32)
+    B = len(lens)
+    npg = (lens + 127) // 128
+    P = int(npg.sum()) + 2
+    perm = rng.permutation(P).astype(np.int32)
+    bt = np.full((B, int(npg.max())), -1, np.int32)
+    o = 0
+    for s in range(B):
+        bt[s, :npg[s]] = perm[o:o + npg[s]]
+        o += npg[s]
+    scale = 0.37
+    rows = [(rng.standard_normal((int(L), 128)) * 3).astype(np.float32) for L in lens]
+    rows[5][::97] *= 40                                   # a few outlier rows
+    slots = np.concatenate([bt[s, np.arange(L) // 128].astype(np.int64) * 128 + np.arange(L) % 128
+                            for s, L in enumerate(lens)])
+    got_pages, want_pages = _fp8_insert_both(np.concatenate(rows), slots, scale, P)
+    assert np.array_equal(got_pages.cpu().numpy(), want_pages)
+    iq_bits = W.to_bf16_bits(rng.standard_normal((B * q, 128)).astype(np.float32))
+    ld = int(lens.max()) + 5
+    want, mag = oracle.index_score_fp8(iq_bits, q, want_pages, bt, lens, scale, ld, want_mag=True)
+    d_bt, d_lens = torch.from_numpy(bt).to(DEV), torch.from_numpy(lens).to(DEV)
+    sc = torch.full((B * q, ld), 7.0, dtype=torch.float32, device=DEV)
+    m.index_score_fp8(_bf16_dev(iq_bits), q, got_pages, d_bt, d_lens, scale, sc)
+    m.mx4_check_status()
+    g = sc.cpu().numpy()
+    L_tok = np.repeat(lens, q)
+    check_scores(g, want, mag, L_tok)
+    assert np.all(g[:, -5:][np.repeat(lens, q) < ld - 5] == 7.0)   # nothing past seq_len
+    # the selection from these scores, against the oracle's selection from its own
+    k = 256
+    sel = oracle.topk_select(want, lens, q, k)
+    out = torch.empty((B * q, k), dtype=torch.int32, device=DEV)
+    ws = torch.empty(max(m.topk_select_workspace(B * q, k, ld), 16), dtype=torch.uint8, device=DEV)
+    m.topk_select(sc, d_lens, q, k, out, ws)
+    m.mx4_check_status()
+    n_tok = np.array([int(lens[t // q]) - q + t % q + 1 for t in range(B * q)])
+    check_topk(out.cpu().numpy(), sel, want, n_tok)
+    # a poisoned key row (0xFF bytes: E4M3 NaN) gives a non-finite score on both sides
+    pg, row = int(bt[4, 0]), 10
+    want_pages[pg, row * 128:(row + 1) * 128] = 0xFF
+    got_pages[pg, row * 128:(row + 1) * 128] = 0xFF
+    want, mag = oracle.index_score_fp8(iq_bits, q, want_pages, bt, lens, scale, ld, want_mag=True)
+    m.index_score_fp8(_bf16_dev(iq_bits), q, got_pages, d_bt, d_lens, scale, sc)
+    m.mx4_check_status()
+    g = sc.cpu().numpy()
+    check_scores(g, want, mag, L_tok)
+    assert not np.isfinite(g[4 * q:5 * q, row]).any()
+
+
+def test_index_score_fp8_full_size_sampled():
+    # The b256 lognormal workload (2.98 M cached tokens) in the launch configuration
+    # the benchmark times: the whole batch scored from the fp8 cache, sampled
+    # sequences checked against the oracle's own fp8 pages.
+    wl = W.make(4)
+    scale = 0.25
+    caches = PagedCaches(wl.num_pages, device=DEV, fp8_index_scale=scale)
+    caches.fill(wl)
+    step = DecodeStep(wl, caches, device=DEV)
+    host = step_inputs_host(wl)
+    step.load_inputs(host)
+    step.run()
+    m.fp8_index_insert(step.idx_new, step.slots, scale, caches.fp8_idx_pages)  # decode tokens
+    m.index_score_fp8(step.iq, wl.q, caches.fp8_idx_pages, step.block_table, step.seq_lens,
+                      scale, step.scores)
+    m.mx4_check_status()
+    L = wl.seq_lens
+    short = int(np.nonzero(L < 2048)[0][0])
+    seqs = sorted({short, int(np.argmax(L)), int(np.argmin(L)), 7, 131})
+    pages = np.full((wl.num_pages, FP8_PAGE), 0xFF, np.uint8)
+    for s in seqs:
+        n = wl.prefilled(s)
+        for a in range(0, n, 65536):
+            b = min(n, a + 65536)
+            oracle.fp8_index_insert(wl.rows(s, W.IDX_ROWS, a, b), wl.slots(s, np.arange(a, b)),
+                                    scale, pages)
+    tok = np.concatenate([np.arange(s * wl.q, (s + 1) * wl.q) for s in seqs])
+    oracle.fp8_index_insert(host["idx_k"][tok], host["slots"][tok], scale, pages)
+    lens = wl.seq_lens[seqs]
+    want, mag = oracle.index_score_fp8(host["iq"][tok], wl.q, pages, wl.block_table[seqs], lens,
+                                       scale, int(wl.max_len), want_mag=True)
+    g = step.scores.cpu().numpy()[tok]
+    check_scores(g, want, mag, np.repeat(lens, wl.q))
