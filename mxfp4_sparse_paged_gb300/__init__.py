@@ -105,7 +105,14 @@ def _stream(stream):
 
 
 def _ptr(t):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    # Every tensor handed to the library passes here: a host tensor would be read
+    # on the device, so it is refused before the call.
+    if t is None:
+        return None
+    if t.device.type != "cuda":
+        raise ValueError(f"every tensor argument must be a CUDA tensor, got a {t.device} tensor "
+                         f"of shape {tuple(t.shape)}")
+    return ctypes.c_void_p(t.data_ptr())
 
 
 def _check(rc: int):
@@ -114,12 +121,22 @@ def _check(rc: int):
 
 
 def _need(t, dtype, name, contiguous=True):
-    if t.device.type != "cuda":
-        raise ValueError(f"{name}: must be a CUDA tensor, got one on {t.device}")
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
     if contiguous and not t.is_contiguous():
         raise ValueError(f"{name}: must be contiguous")
+
+
+def _dims(t, name, *sizes):
+    """t must have len(sizes) dims; a size of None matches any extent."""
+    if t.dim() != len(sizes) or any(w is not None and int(e) != w for e, w in zip(t.shape, sizes)):
+        want = ", ".join("*" if w is None else str(w) for w in sizes)
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected [{want}]")
+
+
+def _rows_at_least(t, n, name):
+    if int(t.shape[0]) < n:
+        raise ValueError(f"{name} has {int(t.shape[0])} rows, needs at least {n}")
 
 
 def _pages(t, name, ndim):
@@ -149,7 +166,13 @@ def mx4_insert(k, v, idx_k, slot_mapping, k_pages, v_pages, idx_pages, stream=No
     _pages(idx_pages, "idx_pages", 2)
     if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
         raise ValueError("k_pages and v_pages must have the same shape and strides")
+    _dims(k, "k", None, None, HEAD_DIM)
     T, Hkv = int(k.shape[0]), int(k.shape[1])
+    _dims(v, "v", T, Hkv, HEAD_DIM)
+    _dims(idx_k, "idx_k", T, HEAD_DIM)
+    _dims(slot_mapping, "slot_mapping", T)
+    if int(k_pages.shape[1]) != Hkv:
+        raise ValueError(f"k_pages has {int(k_pages.shape[1])} KV heads, k has {Hkv}")
     _check(_load().mx4_insert(_ptr(k), _ptr(v), _ptr(idx_k), T, Hkv, _ptr(slot_mapping),
                               _ptr(k_pages), _ptr(v_pages), k_pages.stride(0), k_pages.stride(1),
                               _ptr(idx_pages), idx_pages.stride(0), int(k_pages.shape[0]),
@@ -188,6 +211,8 @@ def mx4_norm_rope_insert(q, iq, k, v, idx_k, positions, cos_sin, g_q, g_k, g_iq,
             raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {shape}")
     if cos_sin.dim() != 2 or cos_sin.shape[1] != 128:
         raise ValueError("cos_sin must be [max_pos, 128] (cosines | sines)")
+    if int(k_pages.shape[1]) != Hkv:
+        raise ValueError(f"k_pages has {int(k_pages.shape[1])} KV heads, k has {Hkv}")
     _check(_load().mx4_norm_rope_insert(
         _ptr(q), _ptr(iq), _ptr(k), _ptr(v), _ptr(idx_k), T, H, Hkv, _ptr(positions),
         _ptr(cos_sin), int(cos_sin.shape[0]), _ptr(g_q), _ptr(g_k), _ptr(g_iq), _ptr(g_ik),
@@ -209,8 +234,8 @@ def fp8_index_insert(idx_k, slot_mapping, scale, pages, stream=None):
     _need(idx_k, torch.float32, "idx_k")
     _need(slot_mapping, torch.int64, "slot_mapping")
     _fp8_pages(pages, "pages")
-    if idx_k.dim() != 2 or idx_k.shape[1] != 128 or tuple(slot_mapping.shape) != (idx_k.shape[0],):
-        raise ValueError("idx_k must be [T, 128] and slot_mapping [T]")
+    _dims(idx_k, "idx_k", None, HEAD_DIM)
+    _dims(slot_mapping, "slot_mapping", int(idx_k.shape[0]))
     _check(_load().fp8_index_insert(_ptr(idx_k), int(idx_k.shape[0]), _ptr(slot_mapping),
                                     float(scale), _ptr(pages), pages.stride(0),
                                     int(pages.shape[0]), _stream(stream)))
@@ -221,15 +246,15 @@ def index_score_fp8(iq, q_per_seq, pages, block_table, seq_lens, scale, scores, 
     _need(iq, torch.bfloat16, "iq")
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
-    _need(scores, torch.float32, "scores", contiguous=False)
+    _need(scores, torch.float32, "scores")
     _fp8_pages(pages, "pages")
-    if scores.stride(1) != 1:
-        raise ValueError("scores: the token axis must be contiguous")
+    _dims(seq_lens, "seq_lens", None)
     B = int(seq_lens.shape[0])
-    if iq.dim() != 2 or iq.shape[1] != 128 or iq.shape[0] != B * q_per_seq:
-        raise ValueError("iq must be [B * q_per_seq, 128]")
-    if block_table.dim() != 2 or block_table.shape[0] != B or scores.shape[0] != iq.shape[0]:
-        raise ValueError("block_table must be [B, width] and scores [T, ld]")
+    _dims(iq, "iq", B * int(q_per_seq), HEAD_DIM)
+    _dims(block_table, "block_table", None, None)
+    _rows_at_least(block_table, B, "block_table")
+    _dims(scores, "scores", None, None)
+    _rows_at_least(scores, B * int(q_per_seq), "scores")
     _check(_load().index_score_fp8(_ptr(iq), int(iq.shape[0]), int(q_per_seq), _ptr(pages),
                                    pages.stride(0), int(pages.shape[0]), _ptr(block_table), B,
                                    int(block_table.shape[1]), _ptr(seq_lens), float(scale),
@@ -241,11 +266,15 @@ def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=
     _need(iq, torch.bfloat16, "iq")
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
-    _need(scores, torch.float32, "scores", contiguous=False)
+    _need(scores, torch.float32, "scores")
     _pages(idx_pages, "idx_pages", 2)
-    if scores.stride(1) != 1:
-        raise ValueError("scores: rows must be contiguous")
+    _dims(seq_lens, "seq_lens", None)
     B = int(seq_lens.shape[0])
+    _dims(iq, "iq", B * int(q_per_seq), HEAD_DIM)
+    _dims(block_table, "block_table", None, None)
+    _rows_at_least(block_table, B, "block_table")
+    _dims(scores, "scores", None, None)
+    _rows_at_least(scores, B * int(q_per_seq), "scores")
     _check(_load().index_score(_ptr(iq), int(iq.shape[0]), int(q_per_seq), _ptr(idx_pages),
                                idx_pages.stride(0), int(idx_pages.shape[0]), _ptr(block_table), B,
                                int(block_table.shape[1]), _ptr(seq_lens), _ptr(scores),
@@ -258,11 +287,15 @@ def topk_select_workspace(T, k, ld_scores) -> int:
 
 def topk_select(scores, seq_lens, q_per_seq, k, topk_idx, ws=None, stream=None):
     """topk_idx[t] = the min(k, n) best indices (ties -> lower index), ascending, -1 padded."""
-    _need(scores, torch.float32, "scores", contiguous=False)
+    _need(scores, torch.float32, "scores")
     _need(seq_lens, torch.int32, "seq_lens")
     _need(topk_idx, torch.int32, "topk_idx")
-    if scores.stride(1) != 1:
-        raise ValueError("scores: rows must be contiguous")
+    _dims(seq_lens, "seq_lens", None)
+    T = int(seq_lens.shape[0]) * int(q_per_seq)
+    _dims(scores, "scores", None, None)
+    _rows_at_least(scores, T, "scores")
+    _dims(topk_idx, "topk_idx", None, int(k))
+    _rows_at_least(topk_idx, T, "topk_idx")
     ws_bytes = 0 if ws is None else ws.numel() * ws.element_size()
     _check(_load().topk_select(_ptr(scores), scores.stride(0), _ptr(seq_lens),
                                int(seq_lens.shape[0]), int(q_per_seq), int(k), _ptr(topk_idx),
@@ -285,7 +318,16 @@ def sparse_paged_decode(q, q_per_seq, k_pages, v_pages, block_table, seq_lens, t
     _pages(v_pages, "v_pages", 3)
     if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
         raise ValueError("k_pages and v_pages must have the same shape and strides")
+    _dims(q, "q", None, None, HEAD_DIM)
     T, H = int(q.shape[0]), int(q.shape[1])
+    _dims(seq_lens, "seq_lens", None)
+    B = int(seq_lens.shape[0])
+    if T != B * int(q_per_seq):
+        raise ValueError(f"q has {T} tokens, seq_lens gives {B} x {int(q_per_seq)}")
+    _dims(out, "out", T, H, HEAD_DIM)
+    _dims(topk_idx, "topk_idx", T, None)
+    _dims(block_table, "block_table", None, None)
+    _rows_at_least(block_table, B, "block_table")
     ws_bytes = ws.numel() * ws.element_size()
     _check(_load().sparse_paged_decode(
         _ptr(q), T, int(q_per_seq), H, int(k_pages.shape[1]), _ptr(k_pages), _ptr(v_pages),
@@ -309,7 +351,16 @@ def sparse_paged_decode_noalloc(q, q_per_seq, k_pages, v_pages, block_table, seq
     _pages(v_pages, "v_pages", 3)
     if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
         raise ValueError("k_pages and v_pages must have the same shape and strides")
+    _dims(q, "q", None, None, HEAD_DIM)
     T, H = int(q.shape[0]), int(q.shape[1])
+    _dims(seq_lens, "seq_lens", None)
+    B = int(seq_lens.shape[0])
+    if T != B * int(q_per_seq):
+        raise ValueError(f"q has {T} tokens, seq_lens gives {B} x {int(q_per_seq)}")
+    _dims(out, "out", T, H, HEAD_DIM)
+    _dims(topk_idx, "topk_idx", T, None)
+    _dims(block_table, "block_table", None, None)
+    _rows_at_least(block_table, B, "block_table")
     _check(_load().sparse_paged_decode_noalloc(
         _ptr(q), T, int(q_per_seq), H, int(k_pages.shape[1]), _ptr(k_pages), _ptr(v_pages),
         k_pages.stride(0), k_pages.stride(1), int(k_pages.shape[0]), _ptr(block_table),

@@ -120,3 +120,68 @@ def test_bindings_refuse_host_tensors_before_any_call():
                                torch.zeros(2, dtype=torch.int64), pages, pages.clone(),
                                pages[:, 0], torch.zeros((2, 16, 128), dtype=torch.bfloat16),
                                torch.zeros((2, 128), dtype=torch.bfloat16))
+
+
+def _cpu_args():
+    import torch
+    T, H, B, k, ld = 4, 16, 4, 8, 300
+    f32, bf, i32, i64, u8 = torch.float32, torch.bfloat16, torch.int32, torch.int64, torch.uint8
+    return {
+        "k": torch.zeros((T, 1, 128)), "v": torch.zeros((T, 1, 128)),
+        "idx_k": torch.zeros((T, 128)), "slots": torch.zeros(T, dtype=i64),
+        "kp": torch.zeros((3, 1, 8704), dtype=u8), "vp": torch.zeros((3, 1, 8704), dtype=u8),
+        "ip": torch.zeros((3, 8704), dtype=u8), "fp8": torch.zeros((3, 16384), dtype=u8),
+        "iq": torch.zeros((T, 128), dtype=bf), "q": torch.zeros((T, H, 128), dtype=bf),
+        "bt": torch.zeros((B, 3), dtype=i32), "sl": torch.ones(B, dtype=i32),
+        "scores": torch.zeros((T, ld), dtype=f32), "idx": torch.zeros((T, k), dtype=i32),
+        "out": torch.zeros((T, H, 128), dtype=f32), "ws": torch.zeros(64, dtype=u8),
+    }
+
+
+def _calls(a, m):
+    return {
+        "mx4_insert": lambda: m.mx4_insert(a["k"], a["v"], a["idx_k"], a["slots"], a["kp"],
+                                           a["vp"], a["ip"]),
+        "index_score": lambda: m.index_score(a["iq"], 1, a["ip"], a["bt"], a["sl"], a["scores"]),
+        "index_score_fp8": lambda: m.index_score_fp8(a["iq"], 1, a["fp8"], a["bt"], a["sl"], 0.5,
+                                                     a["scores"]),
+        "fp8_index_insert": lambda: m.fp8_index_insert(a["idx_k"], a["slots"], 1.0, a["fp8"]),
+        "topk_select": lambda: m.topk_select(a["scores"], a["sl"], 1, a["idx"].shape[1], a["idx"],
+                                             a["ws"]),
+        "sparse_paged_decode": lambda: m.sparse_paged_decode(a["q"], 1, a["kp"], a["vp"], a["bt"],
+                                                             a["sl"], a["idx"], 0.1, a["out"],
+                                                             a["ws"]),
+        "sparse_paged_decode_noalloc": lambda: m.sparse_paged_decode_noalloc(
+            a["q"], 1, a["kp"], a["vp"], a["bt"], a["sl"], a["idx"], 0.1, a["out"]),
+    }
+
+
+def test_bindings_with_consistent_host_tensors_stop_at_the_device_check(lib):
+    import mxfp4_sparse_paged_gb300 as m
+    for name, call in _calls(_cpu_args(), m).items():
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
+
+
+@pytest.mark.parametrize("bad", [
+    ("mx4_insert", "v", (4, 2, 128)), ("mx4_insert", "idx_k", (3, 128)),
+    ("mx4_insert", "slots", (5,)), ("mx4_insert", "k", (4, 2, 128)),
+    ("index_score", "iq", (3, 128)), ("index_score", "bt", (3, 3)),
+    ("index_score", "scores", (3, 300)), ("index_score_fp8", "bt", (2, 3)),
+    ("index_score_fp8", "iq", (4, 64)), ("fp8_index_insert", "slots", (3,)),
+    ("topk_select", "scores", (2, 300)), ("topk_select", "idx", (3, 8)),
+    ("sparse_paged_decode", "out", (4, 8, 128)), ("sparse_paged_decode", "idx", (3, 8)),
+    ("sparse_paged_decode", "bt", (3, 3)), ("sparse_paged_decode", "q", (5, 16, 128)),
+    ("sparse_paged_decode_noalloc", "out", (4, 16, 64)),
+])
+def test_bindings_refuse_inconsistent_shapes(lib, bad):
+    # A table shorter than the batch, an output with too few rows or a K/V head count
+    # the pages do not have would let a kernel read or write past the buffer.
+    import torch
+    import mxfp4_sparse_paged_gb300 as m
+    call, key, shape = bad
+    a = _cpu_args()
+    a[key] = torch.zeros(shape, dtype=a[key].dtype)
+    with pytest.raises(ValueError) as ei:
+        _calls(a, m)[call]()
+    assert "CUDA tensor" not in str(ei.value), str(ei.value)
