@@ -8,7 +8,7 @@ The arithmetic lives in ``mx4_oracle.c`` (plain C, float64); this module only
 compiles it with gcc and marshals numpy arrays through ctypes.  Every function
 below mirrors one C function; their docstrings restate what it computes and
 the source it follows (see the C file's header for the page citations and the
-readings R1..R16 taken where the pages are silent).
+readings R1..R17 taken where the pages are silent).
 """
 from __future__ import annotations
 
@@ -90,6 +90,12 @@ def _load():
         lib.orc_index_score_fp8.restype = i32
         lib.orc_index_score_fp8.argtypes = [P, i64, i32, P, i64, i64, P, i64, P, ctypes.c_float,
                                             P, P, i64]
+        lib.orc_mxfp8_block_exponent.restype = i32
+        lib.orc_mxfp8_block_exponent.argtypes = [ctypes.c_double]
+        lib.orc_mxfp8_quantize_block.restype = i32
+        lib.orc_mxfp8_quantize_block.argtypes = [P, P, P]
+        lib.orc_index_score_mxq.restype = i32
+        lib.orc_index_score_mxq.argtypes = [P, i64, i32, P, i64, i64, P, i64, P, P, P, i64]
         lib.orc_page_bytes.restype = i32
         _lib = lib
         return lib
@@ -327,4 +333,41 @@ def index_score_fp8(iq_bits, q_per_seq, pages, block_table, seq_lens, scale, ld,
                                  _ptr(seq_lens), ctypes.c_float(scale), _ptr(scores), _ptr(mag),
                                  ld)
     _check(rc, "index_score_fp8")
+    return (scores, mag) if want_mag else scores
+
+
+# --------------------------------------------------------------------------
+# block-scaled score mode: the index-q row in MXFP8
+# --------------------------------------------------------------------------
+
+def mxfp8_block_exponent(amax: float) -> int:
+    """Shared exponent of an MXFP8 (E4M3) block: floor(log2(amax)) - 8, clamped."""
+    return _load().orc_mxfp8_block_exponent(float(amax))
+
+
+def mxfp8_quantize_block(x):
+    """32 fp32 values -> (E4M3 codes uint8[32], E8M0 scale byte)."""
+    x = _c(x, np.float32)
+    assert x.shape == (32,)
+    codes = np.zeros(32, np.uint8)
+    sb = np.zeros(1, np.uint8)
+    _check(_load().orc_mxfp8_quantize_block(_ptr(x), _ptr(codes), _ptr(sb)), "mxfp8_quantize_block")
+    return codes, int(sb[0])
+
+
+def index_score_mxq(iq_bits, q_per_seq, idx_pages, block_table, seq_lens, ld, want_mag=False):
+    """Index scores with each index-q row first converted to MXFP8, float64 [T, ld]."""
+    lib = _load()
+    iq_bits = _c(iq_bits, np.uint16)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    B = seq_lens.shape[0]
+    T = iq_bits.shape[0]
+    assert T == B * q_per_seq
+    scores = np.empty((T, ld), np.float64)
+    mag = np.empty((T, ld), np.float64) if want_mag else None
+    rc = lib.orc_index_score_mxq(_ptr(iq_bits), B, int(q_per_seq), _ptr(idx_pages),
+                                 idx_pages.strides[0], idx_pages.shape[0], _ptr(block_table),
+                                 block_table.shape[1], _ptr(seq_lens), _ptr(scores), _ptr(mag), ld)
+    _check(rc, "index_score_mxq")
     return (scores, mag) if want_mag else scores

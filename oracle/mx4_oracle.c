@@ -67,6 +67,12 @@
  *       is an argument: the stored code is E4M3(fl32(x / S)), rounded to
  *       nearest, ties to even, saturating at 448; the element reads back as
  *       E4M3 value times S.
+ *   R17 the block-scaled score mode (an MX operand format for the query, as a
+ *       block-scaled tensor-core product needs): the bf16 index-q row is
+ *       converted to MXFP8 per [OCP] -- per 32-element block, shared exponent
+ *       floor(log2(amax)) - 8 (8 = the largest E4M3 exponent), clamped to
+ *       [-127, 127], -127 for amax == 0; elements x * 2^-E to E4M3, nearest,
+ *       ties to even, saturating at 448 -- and dotted with the dequantised key.
  */
 #include <math.h>
 #include <stddef.h>
@@ -621,6 +627,93 @@ int orc_index_score_fp8(const uint16_t *iq, int64_t B, int q, const uint8_t *pag
                 row = pages + pg * page_stride + (i % ORC_PAGE_TOKENS) * ORC_ROW_ELEMS;
                 for (d = 0; d < ORC_ROW_ELEMS; ++d) {
                     double term = bf16_to_double(qt[d]) * (orc_e4m3_value(row[d]) * scale);
+                    acc += term;
+                    acc_abs += fabs(term);
+                }
+                scores[t * ld + i] = acc;
+                if (mag) mag[t * ld + i] = acc_abs;
+            }
+        }
+    }
+    return ORC_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Block-scaled score mode: the index-q row in MXFP8  [OCP], reading R17     */
+/* ------------------------------------------------------------------------- */
+
+/* Shared exponent of an MXFP8 (E4M3) block with largest magnitude amax:
+ * floor(log2(amax)) - 8, clamped to [-127, 127]; -127 for amax == 0. */
+int orc_mxfp8_block_exponent(double amax)
+{
+    int e, E;
+    if (amax == 0.0) return -127;
+    (void)frexp(amax, &e);
+    E = (e - 1) - 8;
+    if (E < -127) E = -127;
+    if (E > 127) E = 127;
+    return E;
+}
+
+/* Quantise x[0..31] (finite) to 32 E4M3 codes and one E8M0 scale byte. */
+int orc_mxfp8_quantize_block(const float *x, uint8_t *codes, uint8_t *scale_byte)
+{
+    double amax = 0.0;
+    int i, E;
+    for (i = 0; i < ORC_BLOCK; ++i) {
+        if (!isfinite(x[i])) return ORC_ERR_INVALID;
+        if (fabs((double)x[i]) > amax) amax = fabs((double)x[i]);
+    }
+    E = orc_mxfp8_block_exponent(amax);
+    *scale_byte = (uint8_t)(E + 127);
+    for (i = 0; i < ORC_BLOCK; ++i) {
+        /* exact: a power-of-two scaling of an fp32 value, below 512 in magnitude;
+         * parts below the smallest fp32 subnormal would round to code 0 anyway */
+        codes[i] = (uint8_t)orc_e4m3_encode((float)ldexp((double)x[i], -E));
+    }
+    return ORC_OK;
+}
+
+/* Index scores with the index-q row in MXFP8 (R17): as orc_index_score, with
+ * iq[t] replaced by its MXFP8 value sum_b E4M3(code_j) * 2^(scale_b - 127). */
+int orc_index_score_mxq(const uint16_t *iq, int64_t B, int q, const uint8_t *idx_pages,
+                        int64_t idx_page_stride, int64_t num_pages, const int32_t *block_table,
+                        int64_t bt_width, const int32_t *seq_lens, double *scores, double *mag,
+                        int64_t ld)
+{
+    int64_t s, i;
+    int j, d, b;
+    for (s = 0; s < B; ++s) {
+        int64_t L = seq_lens[s];
+        if (L < q || L > ld || L > bt_width * ORC_PAGE_TOKENS) return ORC_ERR_BOUNDS;
+        for (j = 0; j < q; ++j) {
+            int64_t t = s * q + j;
+            int64_t p = L - q + j;
+            float x[ORC_ROW_ELEMS];
+            double qv[ORC_ROW_ELEMS];
+            uint8_t codes[ORC_BLOCK], sb;
+            for (d = 0; d < ORC_ROW_ELEMS; ++d)
+                x[d] = (float)bf16_to_double(iq[t * ORC_ROW_ELEMS + d]);
+            for (b = 0; b < ORC_ROW_ELEMS / ORC_BLOCK; ++b) {
+                int rc = orc_mxfp8_quantize_block(x + b * ORC_BLOCK, codes, &sb);
+                if (rc) return rc;
+                for (d = 0; d < ORC_BLOCK; ++d)
+                    qv[b * ORC_BLOCK + d] = orc_e4m3_value(codes[d]) * orc_e8m0_value(sb);
+            }
+            for (i = 0; i < ld; ++i) {
+                double acc = 0.0, acc_abs = 0.0;
+                int64_t pg;
+                const uint8_t *page;
+                if (i > p) {
+                    scores[t * ld + i] = -INFINITY;
+                    if (mag) mag[t * ld + i] = 0.0;
+                    continue;
+                }
+                pg = page_of(block_table, bt_width, s, i, num_pages);
+                if (pg < 0) return ORC_ERR_BOUNDS;
+                page = idx_pages + pg * idx_page_stride;
+                for (d = 0; d < ORC_ROW_ELEMS; ++d) {
+                    double term = qv[d] * orc_dequant_element(page, (int)(i % ORC_PAGE_TOKENS), d);
                     acc += term;
                     acc_abs += fabs(term);
                 }

@@ -633,3 +633,87 @@ def test_fp8_index_score_unit_query_reads_one_element_times_scale():
                                     8.0, 200)
         want = [dec[bt[0, i // 128], (i % 128) * 128 + d] * 8.0 for i in range(200)]
         assert np.array_equal(sc[0], want)
+
+
+# ---------------------------------------------------------------- block-scaled score mode (MXFP8 query)
+
+def test_mxfp8_hand_worked_block():
+    # amax 1 -> E = 0 - 8 = -8 (byte 0x77); y = x * 2^8: 256 -> 0x78, 76.8 -> 80 -> 0x6A,
+    # -5.12 -> -5 -> 0xCA; zeros stay zero
+    x = np.zeros(32, np.float32)
+    x[:3] = [1.0, 0.3, -0.02]
+    codes, sb = oracle.mxfp8_quantize_block(x)
+    assert sb == 0x77
+    assert list(codes[:3]) == [0x78, 0x6A, 0xCA] and not codes[3:].any()
+    codes, sb = oracle.mxfp8_quantize_block(np.zeros(32, np.float32))
+    assert sb == 0 and not codes.any()
+
+
+def test_mxfp8_block_exponent_and_saturation_edge():
+    assert oracle.mxfp8_block_exponent(1.0) == -8
+    assert oracle.mxfp8_block_exponent(2.0) == -7
+    assert oracle.mxfp8_block_exponent(float(np.nextafter(np.float32(2), np.float32(0)))) == -8
+    assert oracle.mxfp8_block_exponent(2.0 ** -130) == -127
+    assert oracle.mxfp8_block_exponent(float(np.finfo(np.float32).max)) == 127 - 8
+    # an amax just below 2^(E+9) scales to just below 512: it saturates to 448
+    x = np.zeros(32, np.float32)
+    x[0] = np.nextafter(np.float32(2), np.float32(0))
+    x[1] = -x[0]
+    codes, sb = oracle.mxfp8_quantize_block(x)
+    assert sb == 127 - 8 and codes[0] == 0x7E and codes[1] == 0xFE
+
+
+def test_mxfp8_elements_match_torch_float8_at_the_block_exponent():
+    # With E fixed by the block maximum, an element's code is the library's E4M3
+    # conversion of x * 2^-E wherever that stays below 464 (torch does not saturate).
+    rng = np.random.default_rng(12)
+    for trial in range(200):
+        x = (rng.standard_normal(32) * 2.0 ** rng.integers(-30, 30)).astype(np.float32)
+        x[rng.integers(32)] *= rng.choice([1.0, 0.0, 1e-8])
+        codes, sb = oracle.mxfp8_quantize_block(x)
+        E = sb - 127
+        assert E == oracle.mxfp8_block_exponent(float(np.abs(x).max()))
+        y = x.astype(np.float64) * 2.0 ** -E
+        assert np.abs(y).max() < 512
+        ok = np.abs(y) < 464
+        lib = torch.from_numpy(y[ok].astype(np.float32)).to(torch.float8_e4m3fn)
+        lib = lib.view(torch.uint8).numpy()
+        z = (lib & 0x7F) == 0
+        assert np.array_equal(codes[ok][~z], lib[~z])
+        assert np.all((codes[ok][z] & 0x7F) == 0)
+        assert np.all(codes[~ok] & 0x7F == 0x7E)
+
+
+def test_index_score_mxq_exact_against_rationals_and_error_bound():
+    # Keys of exactly representable MXFP4 values; the query's MXFP8 values come from
+    # torch's E4M3 decode of the oracle's codes times 2^E; the score is their exact
+    # rational dot.  And the difference to the bf16-query score stays within
+    # sum_j |k_j| * (E4M3 half-step of q_j at its block exponent).
+    rng = np.random.default_rng(31)
+    lens = [200, 5]
+    bt = np.array([[1, 2], [0, -1]], np.int32)
+    rows = [_grid_rows(rng, L) for L in lens]
+    ip = _fill(3, bt, lens, rows)
+    q = 1
+    iqf = (rng.standard_normal((2, 128)) * np.exp2(rng.integers(-6, 6, (2, 128)))).astype(np.float32)
+    iq = W.to_bf16_bits(iqf)
+    iqv = torch.from_numpy(iq.view(np.int16)).view(torch.bfloat16).double().numpy()
+    sc = oracle.index_score_mxq(iq, q, ip, bt, np.array(lens, np.int32), 200)
+    ref = oracle.index_score(iq, q, ip, bt, np.array(lens, np.int32), 200)
+    for t in range(2):
+        qhat, half = np.zeros(128), np.zeros(128)
+        for b in range(4):
+            codes, sb = oracle.mxfp8_quantize_block(iqv[t, 32 * b:32 * b + 32].astype(np.float32))
+            dec = torch.from_numpy(codes).view(torch.float8_e4m3fn).double().numpy()
+            qhat[32 * b:32 * b + 32] = dec * 2.0 ** (sb - 127)
+            # half an E4M3 step at each element's binade (2^-10 below 2^-6), or the
+            # distance to 448 where the scaled element saturates; times 2^E
+            y = np.abs(iqv[t, 32 * b:32 * b + 32]) * 2.0 ** -(sb - 127)
+            e = np.floor(np.log2(np.maximum(y, 2.0 ** -6)))
+            half[32 * b:32 * b + 32] = np.maximum(2.0 ** (e - 4), y - 448.0) * 2.0 ** (sb - 127)
+        for i in range(lens[t]):
+            key = rows[t][i].astype(np.float64)
+            exact = sum(Fraction(float(qhat[d])) * Fraction(float(key[d])) for d in range(128))
+            assert sc[t, i] == float(exact)
+            assert abs(sc[t, i] - ref[t, i]) <= float(np.abs(key) @ half) * (1 + 1e-12)
+        assert np.all(sc[t, lens[t]:] == -np.inf)
