@@ -49,7 +49,7 @@ extern "C" {
 typedef enum {
     MX4_OK = 0,
     MX4_ERR_INVALID = -1,     /* a NULL pointer, a negative size, a misaligned buffer */
-    MX4_ERR_UNSUPPORTED = -2, /* a geometry this build does not implement */
+    MX4_ERR_UNSUPPORTED = -2, /* a geometry this library does not implement */
     MX4_ERR_WORKSPACE = -3,   /* workspace too small */
     MX4_ERR_CUDA = -4,        /* a CUDA runtime error (launch or copy) */
     MX4_ERR_BOUNDS = -5       /* reported by mx4_check_status: a kernel skipped bad data */
@@ -204,7 +204,7 @@ size_t topk_select_workspace(int64_t T, int k, int64_t ld_scores);
  *   topk_idx  int32 [T, k], ascending indices then -1 padding
  *   out       fp32 [T, H, 128] (output)
  *   ws        workspace of sparse_paged_decode_workspace(T, k) bytes
- * H == 16 and Hkv == 1 in this build (else MX4_ERR_UNSUPPORTED).  An index
+ * H == 16 and Hkv == 1 in this library (else MX4_ERR_UNSUPPORTED).  An index
  * outside [0, p] or a bad page id skips that token and sets
  * MX4_STATUS_BAD_INDEX / MX4_STATUS_BAD_PAGE.  A token with no selected index
  * gets a zero output.

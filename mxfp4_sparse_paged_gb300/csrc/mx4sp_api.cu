@@ -302,7 +302,7 @@ int sparse_paged_decode(const uint16_t* q, int64_t T, int q_per_seq, int H, int 
                         size_t ws_bytes, void* stream) {
   if (H != 16 || Hkv != 1)
     return fail(MX4_ERR_UNSUPPORTED,
-                "sparse_paged_decode: H = %d, Hkv = %d (this build: 16 query heads, 1 KV head)",
+                "sparse_paged_decode: H = %d, Hkv = %d (supported: 16 query heads, 1 KV head)",
                 H, Hkv);
   if (q_per_seq < 1 || q_per_seq > 8)
     return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode: q_per_seq = %d", q_per_seq);

@@ -40,7 +40,7 @@
  *            type (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, no
  *            inf, S.1111.111 = NaN, largest normal 448).
  *
- * Readings taken where the pages are silent (each also listed in the design doc):
+ * Readings taken where the pages are silent:
  *   R1  scale b of a row covers the contiguous elements 32b .. 32b+31;
  *   R2  amax == 0 gives shared exponent -127 (scale byte 0x00);
  *   R3  the exponent is clamped to [-127, 127];
