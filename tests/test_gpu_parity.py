@@ -232,6 +232,30 @@ def test_insert_dense_sweep_of_scaled_values():
         assert np.array_equal(got, want)
 
 
+def test_insert_every_pattern_near_each_rounding_threshold():
+    # Both encoders are monotone step functions of |y| (the kernel counts threshold
+    # comparisons; the oracle takes the nearest grid value), so they agree everywhere
+    # once they agree on every fp32 pattern around each of the 7 midpoints and on a
+    # sweep in between (the test above).  Here: all patterns within 4096 ulps of each
+    # midpoint, both signs, next to an anchor of 4.0 so the block exponent is 0.
+    mids = np.array([0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0], np.float32)
+    u = mids.view(np.int32)
+    pats = (u[:, None] + np.arange(-4096, 4097, dtype=np.int32)[None, :]).reshape(-1)
+    vals = pats.view(np.float32)
+    vals = np.concatenate([vals, -vals])
+    nb = (len(vals) + 30) // 31
+    blocks = np.zeros((nb, 32), np.float32)
+    blocks[:, 0] = 4.0
+    flat = np.zeros(nb * 31, np.float32)
+    flat[:len(vals)] = vals
+    blocks[:, 1:] = flat.reshape(nb, 31)
+    nrow = (nb + 3) // 4
+    rows = np.zeros((nrow * 4, 32), np.float32)
+    rows[:nb] = blocks
+    got, want = _insert_both(rows.reshape(nrow, 128))
+    assert np.array_equal(got, want)
+
+
 # ----------------------------------------------------------------- top-k exact
 
 def test_topk_bit_exact_on_shared_scores():
