@@ -62,3 +62,24 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
     args = argparse.Namespace(workload=0, steps=1, warmup=3, cpu_budget=1.0)
     assert bench.run_reference(args) is None
     assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_prints_one_contract_line(monkeypatch, capsys):
+    # --impl reference on the tiny workload: the oracle on the host's cores, one JSON
+    # line with the metric, a cpu_baseline naming the threads it used, and an e2e
+    # entry without transfers.
+    import json
+    import bench
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.delenv("RANK", raising=False)
+    args = argparse.Namespace(workload=0, steps=4, warmup=3, cpu_budget=1.0)
+    bench.run_reference(args)
+    out = capsys.readouterr().out.strip().splitlines()
+    assert len(out) == 1
+    line = json.loads(out[0])
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["unit"] == bench.UNIT and line["value"] > 0 and line["steps"] == 4
+    assert line["cpu_baseline"]["cores"] == bench.host_cores()
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["value"] == line["value"]
+    assert line["config"]["workload"] == "tiny-b1-ctx512"
