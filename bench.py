@@ -372,6 +372,13 @@ def run_gpu(args):
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": ab["index_score"],
                      "traffic": traffic},
+        "roofline_decode": {
+            "bound": "hbm", "kernel": "sparse_paged_decode (split + merge kernels)",
+            "achieved": round(ab["sparse_paged_decode"] / dec_s / 1e9, 1), "peak": peak,
+            "unit": "GB/s", "frac": round(ab["sparse_paged_decode"] / dec_s / 1e9 / peak, 4),
+            "algorithmic_bytes_per_launch": ab["sparse_paged_decode"],
+            "traffic": _ncu_traffic(wl.spec.name, "decode_split_traffic.json"),
+            "traffic_kernel": "decode_split_kernel"},
         "hot_path_hbm": {"kernels": "index_score + sparse_paged_decode",
                          "algorithmic_bytes": hot_bytes, "achieved_gbs": round(hot_gbs, 1),
                          "frac": round(hot_gbs / peak, 4)},
@@ -495,12 +502,12 @@ def time_writer(wl, dev, stream, flush_l2, steps):
             "timing": "mean of CUDA-event pairs on the launching stream, L2 flushed before each"}
 
 
-def _ncu_traffic(name):
-    """dram bytes (read + write) per index_score launch from the committed ncu
-    record for this workload, or None when there is none or the kernel's sources
-    changed since the counters were taken."""
+def _ncu_traffic(name, record="index_score_traffic.json"):
+    """dram bytes (read + write) per launch of a kernel from its committed ncu record
+    for this workload, or None when there is none or the kernel's sources changed
+    since the counters were taken."""
     import hashlib
-    p = os.path.join(ROOT, "profiles", "index_score_traffic.json")
+    p = os.path.join(ROOT, "profiles", record)
     try:
         with open(p) as f:
             rec = json.load(f)[name]
