@@ -717,3 +717,19 @@ def test_index_score_mxq_exact_against_rationals_and_error_bound():
             assert sc[t, i] == float(exact)
             assert abs(sc[t, i] - ref[t, i]) <= float(np.abs(key) @ half) * (1 + 1e-12)
         assert np.all(sc[t, lens[t]:] == -np.inf)
+
+
+def test_encoders_are_monotone_step_functions():
+    # The e2m1 rounding and the E4M3 encoder never decrease as |y| grows, and change
+    # value only at the grid midpoints: over dense sorted inputs the decoded value is
+    # non-decreasing and every step of it straddles a midpoint.
+    y = np.linspace(0.0, 7.999, 20001)
+    mag = np.array([oracle.e2m1_value(oracle.round_magnitude(v)) for v in y])
+    assert np.all(np.diff(mag) >= 0)
+    grid = np.array([0, .5, 1, 1.5, 2, 3, 4, 6])
+    mids = (grid[1:] + grid[:-1]) / 2
+    for i in np.nonzero(np.diff(mag))[0]:
+        assert np.any((y[i] <= mids) & (mids <= y[i + 1])), (y[i], y[i + 1])
+    z = np.linspace(-500.0, 500.0, 40001).astype(np.float32)
+    val = np.array([oracle.e4m3_value(oracle.e4m3_encode(v)) for v in z])
+    assert np.all(np.diff(val) >= 0)
