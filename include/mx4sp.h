@@ -125,8 +125,10 @@ int mx4_insert(const float *k, const float *v, const float *idx_k, int64_t T, in
  *   q_out        bf16 [T, H, 128]; iq_out bf16 [T, 128]  (outputs)
  * fp32 arrays 16-byte aligned, q_out / iq_out 8-byte aligned.  A position
  * outside [0, max_pos) skips every row of that token and sets
- * MX4_STATUS_BAD_INDEX; slots behave as in mx4_insert.  1 <= H <= 64,
- * 1 <= Hkv <= 8.
+ * MX4_STATUS_BAD_INDEX.  Slots behave as in mx4_insert; a negative slot skips
+ * only the token's page rows (its q_out and iq_out rows are still written).
+ * Non-finite values set MX4_STATUS_BAD_VALUE when they reach a page row.
+ * 1 <= H <= 64, 1 <= Hkv <= 8.
  * ------------------------------------------------------------------------- */
 int mx4_norm_rope_insert(const float *q, const float *iq, const float *k, const float *v,
                          const float *idx_k, int64_t T, int H, int Hkv, const int64_t *positions,
