@@ -7,9 +7,17 @@ Inputs are resident in HBM when the timed region starts; the L2 is flushed
 (a 256 MiB write, then a read of it so the write-back of its dirty lines
 falls outside the step) between timed steps, outside the per-step CUDA events.
 
-Default workload: 256 sequences, lognormal contexts (median 8192, capped at
-131072), one decode token each inserted in the step, top-2048 -- the only
-workload whose step runs all four kernels.  `--workload 0..4` picks another.
+By default all five workloads are measured, each with its own block in the
+JSON line (step time, tokens/s, per-kernel times, the scorer's, the decode's
+and the hot path's HBM fractions, the end-to-end rate through the C entry point
+mx4_decode_step with host buffers, clocks).  The headline -- `value`, `roofline`,
+`e2e`, the extra legs and the CPU baselines -- is workload 4: 256 sequences,
+lognormal contexts (median 8192, capped at 131072), one decode token each
+inserted in the step, top-2048, the only workload whose step runs all four
+kernels and the largest.  `--workload N` measures one workload only.
+
+Clocks are sampled with nvidia-smi over a soak of about one second of the same
+step right before the K timed steps and over the timed steps themselves.
 
 Under torchrun (N > 1) every rank runs an independent replica of the same
 workload (the path shards by sequence with no exchange step): weak scaling,
@@ -240,12 +248,172 @@ def job_value(tokens_per_rank_step: int, world: int, steps: int, total_ms: float
 
 # --------------------------------------------------------------------------- GPU arm
 
+def _flusher(dev):
+    import torch
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def flush_l2(v):
+        # Write a buffer twice the L2 size, then read it back: the read evicts the
+        # written lines, so their write-back lands here rather than in the step.
+        flush.fill_(v)
+        flush.view(torch.int64).sum()
+    return flush_l2
+
+
+def _event_ms(pairs):
+    return [a.elapsed_time(b) for a, b in pairs]
+
+
+def _roof(name, nbytes, ms, peak, traffic=None, extra=None):
+    gbs = nbytes / (ms / 1e3) / 1e9
+    d = {"bound": "hbm", "kernel": name, "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+         "frac": round(gbs / peak, 4), "algorithmic_bytes_per_launch": int(nbytes),
+         "traffic": traffic}
+    if traffic:
+        d["traffic_over_algorithmic"] = round(traffic / nbytes, 3)
+        d["dram_gbs_at_traffic"] = round(traffic / (ms / 1e3) / 1e9, 1)
+    if extra:
+        d.update(extra)
+    return d
+
+
+def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=False):
+    """Time one workload's decode step on this GPU: warm-up, a clock-sampled soak of
+    about args.soak seconds of the same step, the timed steps (one event pair each,
+    L2 flushed between them), a per-kernel event pass, and the step end to end
+    through the C entry point mx4_decode_step with host buffers.  Returns the
+    workload's block of the JSON line (and the live objects for the headline's
+    extra legs)."""
+    import torch
+
+    import mxfp4_sparse_paged_gb300 as m
+    from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, step_inputs_host
+
+    wl = W.make(wid)
+    caches = PagedCaches(wl.num_pages, device=dev,
+                         fp8_index_scale=FP8_INDEX_SCALE if headline else None)
+    caches.fill(wl)
+    step = DecodeStep(wl, caches, device=dev)
+    host = step_inputs_host(wl)
+    torch.cuda.synchronize()
+    ab = W.algorithmic_bytes(wl)
+    names = (["mx4_insert"] if wl.spec.insert_in_step else []) + \
+        ["index_score", "topk_select", "sparse_paged_decode"]
+    # The in-step insert rewrites the decode tokens' rows with the same values, so
+    # every timed step does identical work.
+    step.load_inputs(host)
+    for _ in range(args.warmup):
+        flush_l2(1)
+        step.run(stream=stream)
+    m.mx4_check_status()
+    if not args.eager:
+        step.capture()  # the step's kernels as one CUDA graph (same launches, same order)
+        for _ in range(3):
+            flush_l2(1)
+            step.replay()
+
+    def one_step():
+        if args.eager:
+            step.run(stream=stream)
+        else:
+            step.replay()
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+    st = [(ev(), ev()) for _ in range(args.steps)]
+    # clocks: sampled over a soak of the same step right before the timed steps and
+    # over the timed steps (a timed region of K steps is far shorter than a sample)
+    clocks = Clocks(int(dev.index or 0))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    soak_steps = 0
+    while time.perf_counter() - t0 < args.soak:
+        for _ in range(50):
+            flush_l2(1)
+            one_step()
+        soak_steps += 50
+        torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush_l2(i & 0xFF)
+        st[i][0].record(stream)
+        one_step()
+        st[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    wall = time.perf_counter() - wall0
+    ck = clocks.stop()
+    m.mx4_check_status()
+    step_ms = _event_ms(st)
+    # Per-kernel times: the same steps again with an event pair around each entry
+    # point.  Events between kernels serialise them (no kernel starts under the
+    # previous one), so this pass is kept out of the step timing above.
+    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names}
+    for i in range(args.steps):
+        flush_l2(i & 0xFF)
+        step.run(stream=stream, events={n: per[n][i] for n in names})
+    torch.cuda.synchronize()
+    m.mx4_check_status()
+    kern_ms = {n: statistics.mean(_event_ms(per[n])) for n in names}
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_value(wl.T, world, args.steps, total_ms)
+
+    # ---- end to end through the C ABI with host buffers: every step copies its
+    # packed inputs from pinned host memory, runs the four stages and copies its
+    # output back (mx4_decode_step), one step after another on one stream.
+    pin = step.pack_inputs(host)
+    h_out = torch.empty(tuple(step.out.shape), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        step.run_host(pin, h_out, stream=stream)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = ev(), ev()
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.run_host(pin, h_out, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    m.mx4_check_status()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
+    e2e = {"value": round(job_value(wl.T, world, args.steps, e2e_ms), 1), "unit": UNIT,
+           "h2d_bytes_per_step": int(pin.numel()),
+           "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()),
+           "mode": "through the C entry point mx4_decode_step: each step copies its packed "
+                   "inputs from pinned host memory, runs insert/score/top-k/decode and copies "
+                   "its output to pinned host memory, steps back to back on one stream; no L2 "
+                   "flush"}
+
+    peak, peak_kind = _peaks()
+    sc_ms, dec_ms = kern_ms["index_score"], kern_ms["sparse_paged_decode"]
+    hot = ab["index_score"] + ab["sparse_paged_decode"]
+    hot_gbs = hot / ((sc_ms + dec_ms) / 1e3) / 1e9
+    r_score = _roof("index_score", ab["index_score"], sc_ms, peak,
+                    _ncu_traffic(wl.spec.name, "index_score_traffic.json"))
+    r_dec = _roof("sparse_paged_decode (run kernel + merge kernel)", ab["sparse_paged_decode"],
+                  dec_ms, peak, _ncu_traffic(wl.spec.name, "decode_split_traffic.json"),
+                  {"traffic_kernel": "decode_split_kernel"})
+    block = {
+        "value": round(value, 1), "unit": UNIT, "ms_per_step": round(total_ms / args.steps, 4),
+        "decode_tokens": wl.T, "cached_tokens": int(wl.seq_lens.astype(np.int64).sum()),
+        "kernel_ms": {n: round(v, 5) for n, v in kern_ms.items()},
+        "kernel_ms_timing": "a second pass with a CUDA-event pair around each entry point; "
+                            "the events serialise the kernels",
+        "roofline_index_score": r_score, "roofline_decode": r_dec,
+        "hot_path_hbm": {"kernels": "index_score + sparse_paged_decode",
+                         "algorithmic_bytes": int(hot), "achieved_gbs": round(hot_gbs, 1),
+                         "frac": round(hot_gbs / peak, 4),
+                         "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": e2e, "clocks": ck, "soak_steps": soak_steps,
+        "gpu_launches": step.launches_per_step() * args.steps,
+        "wall_s_timed_region": round(wall, 4),
+    }
+    return block, (wl, caches, step, host, kern_ms)
+
+
 def run_gpu(args):
     import torch
     import torch.distributed as dist
-
-    import mxfp4_sparse_paged_gb300 as m
-    from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, PipelinedSteps, step_inputs_host
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -259,145 +427,75 @@ def run_gpu(args):
         if world > 1:
             dist.barrier()
 
-    wl = W.make(args.workload)
-    # The fill also writes the fp8 index-K cache variant from the same rows; the timed
-    # step reads only the MXFP4 pools.
-    caches = PagedCaches(wl.num_pages, device=dev, fp8_index_scale=FP8_INDEX_SCALE)
-    caches.fill(wl)
-    step = DecodeStep(wl, caches, device=dev)
-    host = step_inputs_host(wl)
-    torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
-    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
-
-    def flush_l2(v):
-        # Write a buffer twice the L2 size, then read it back: the read evicts the
-        # written lines, so their write-back lands here rather than in the step.
-        flush.fill_(v)
-        flush.view(torch.int64).sum()
-    ab = W.algorithmic_bytes(wl)
-
-    # The in-step insert rewrites the decode tokens' rows with the same values, so
-    # every timed step does identical work.
-    names = (["mx4_insert"] if wl.spec.insert_in_step else []) + \
-        ["index_score", "topk_select", "sparse_paged_decode"]
-    step.load_inputs(host)
-    for _ in range(args.warmup):
-        flush_l2(1)
-        step.run(stream=stream)
-    m.mx4_check_status()
-
-    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
-    st = [(ev(), ev()) for _ in range(args.steps)]
-    if not args.eager:
-        step.capture()  # the step's kernels as one CUDA graph (same launches, same order)
-        for _ in range(3):
-            flush_l2(1)
-            step.replay()
-    clocks = Clocks(local)
-    barrier()
-    torch.cuda.synchronize()
-    wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush_l2(i & 0xFF)
-        st[i][0].record(stream)
-        if args.eager:
-            step.run(stream=stream)
+    flush_l2 = _flusher(dev)
+    head = args.workload if args.workload is not None else 4
+    order = [head] if args.workload is not None else [0, 1, 2, 3, 4]
+    blocks = {}
+    for wid in order:
+        blk, live = measure_workload(wid, args, dev, stream, flush_l2, world, barrier,
+                                     headline=(wid == head))
+        blocks[W.SPECS[wid].name] = blk
+        if wid == head:
+            head_blk, head_live = blk, live
         else:
-            step.replay()
-        st[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier()
-    wall = time.perf_counter() - wall0
-    ck = clocks.stop()
-    m.mx4_check_status()
-    step_ms = [a.elapsed_time(b) for a, b in st]
-    # Per-kernel times: the same steps again with an event pair around each entry
-    # point (events between kernels stop a kernel from starting early under the
-    # previous one, so they are kept out of the step timing above).
-    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names}
-    for i in range(args.steps):
-        flush_l2(i & 0xFF)
-        step.run(stream=stream, events={n: per[n][i] for n in names})
-    torch.cuda.synchronize()
-    m.mx4_check_status()
-    kern_ms = {n: statistics.mean(a.elapsed_time(b) for a, b in per[n]) for n in names}
-    total_ms = max_over_ranks(sum(step_ms), world, dev)
-    ms_per_step = total_ms / args.steps
-    value = job_value(wl.T, world, args.steps, total_ms)
+            del live
+            torch.cuda.empty_cache()
+    wl, caches, step, host, kern_ms = head_live
+    peak, _ = _peaks()
 
-    # ---- end to end through the public API: host inputs -> device -> step -> host
-    # output for every step, with the transfers of neighbouring steps overlapped
-    # (PipelinedSteps).  No flush here: each step streams the 204 MB index cache and
-    # writes and reads 134 MB of scores, more than the 129 MB L2.
+    # the headline's extra legs: the overlapped serving loop, the writer, the fp8 scorer
+    from mxfp4_sparse_paged_gb300.step import PipelinedSteps
     pipe = PipelinedSteps(wl, caches, device=dev)
     pin = pipe.pack_inputs(host)
-    h2d = pin.numel()
-    d2h = pipe.h_out[0].numel() * pipe.h_out[0].element_size()
     for _ in range(4):
         _, done = pipe.submit(pin)
     done.synchronize()
     barrier()
     torch.cuda.synchronize()
-    e0, e1 = ev(), ev()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(pipe.h2d)
     for _ in range(args.steps):
         _, done = pipe.submit(pin)
     pipe.h2d.wait_event(done)
     e1.record(pipe.h2d)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
-    e2e_value = job_value(wl.T, world, args.steps, e2e_ms)
-    m.mx4_check_status()
-
+    pipe_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     writer = time_writer(wl, dev, stream, flush_l2, min(args.steps, 200))
     fp8 = time_fp8_scorer(wl, caches, step, stream, flush_l2, min(args.steps, 200))
 
-    peak, peak_kind = _peaks()
-    score_s = kern_ms["index_score"] / 1e3
-    achieved = ab["index_score"] / score_s / 1e9
-    dec_s = kern_ms["sparse_paged_decode"] / 1e3
-    hot_bytes = ab["index_score"] + ab["sparse_paged_decode"]
-    hot_gbs = hot_bytes / (score_s + dec_s) / 1e9
-    traffic = _ncu_traffic(wl.spec.name)
+    # roofline of the step's dominant HBM-bound kernel (the one taking longer)
+    dominant = "roofline_decode" if kern_ms["sparse_paged_decode"] > kern_ms["index_score"] \
+        else "roofline_index_score"
     line = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "metric": METRIC, "value": head_blk["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head_blk["ms_per_step"],
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp32",
         "data": "synthetic (seeded N(0,1) K/V/index-K rows quantised to MXFP4 pages; "
                 "bf16 N(0,1) queries)",
         "config": _config(wl),
-        "roofline": {"bound": "hbm", "kernel": "index_score", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)",
-                     "algorithmic_bytes_per_launch": ab["index_score"],
-                     "traffic": traffic},
-        "roofline_decode": {
-            "bound": "hbm", "kernel": "sparse_paged_decode (split + merge kernels)",
-            "achieved": round(ab["sparse_paged_decode"] / dec_s / 1e9, 1), "peak": peak,
-            "unit": "GB/s", "frac": round(ab["sparse_paged_decode"] / dec_s / 1e9 / peak, 4),
-            "algorithmic_bytes_per_launch": ab["sparse_paged_decode"],
-            "traffic": _ncu_traffic(wl.spec.name, "decode_split_traffic.json"),
-            "traffic_kernel": "decode_split_kernel"},
-        "hot_path_hbm": {"kernels": "index_score + sparse_paged_decode",
-                         "algorithmic_bytes": hot_bytes, "achieved_gbs": round(hot_gbs, 1),
-                         "frac": round(hot_gbs / peak, 4)},
-        "kernel_ms": {n: round(v, 5) for n, v in kern_ms.items()},
+        "roofline": dict(head_blk[dominant], peak_source="measured (MEASURED_PEAKS.json hbm_gbs)"
+                         if _peaks()[1] == "measured" else "fallback"),
+        "roofline_index_score": head_blk["roofline_index_score"],
+        "roofline_decode": head_blk["roofline_decode"],
+        "hot_path_hbm": head_blk["hot_path_hbm"],
+        "kernel_ms": head_blk["kernel_ms"], "kernel_ms_timing": head_blk["kernel_ms_timing"],
         "step_launch": ("separate API calls" if args.eager else
                         "one CUDA-graph launch of the step's kernels (captured from the API calls)"),
-        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h),
-                "mode": "every step copies its inputs from pinned host memory and reads its "
-                        "output back; the copies of neighbouring steps overlap the compute "
-                        "(two buffer sets, three streams, one packed input copy and one CUDA-graph "
-                        "launch a step); no L2 flush (a step moves more than the L2 holds)"},
+        "e2e": head_blk["e2e"],
+        "e2e_pipelined": {"value": round(job_value(wl.T, world, args.steps, pipe_ms), 1),
+                          "unit": UNIT, "h2d_bytes_per_step": int(pin.numel()),
+                          "d2h_bytes_per_step": int(pipe.h_out[0].numel() * 4),
+                          "mode": "the Python serving loop (PipelinedSteps): packed inputs and "
+                                  "the output copied on their own streams, overlapping the "
+                                  "neighbouring steps' compute; one CUDA-graph launch a step"},
         "norm_rope_writer": writer,
         "fp8_index_variant": dict(fp8, mxfp4_index_score_us=round(kern_ms["index_score"] * 1e3, 2),
-                                  peak_gbs=peak,
-                                  frac=round(fp8["achieved_gbs"] / peak, 4)),
-        "gpu_launches": step.launches_per_step() * args.steps,
-        "clocks": ck,
-        "wall_s_timed_region": round(wall, 3),
+                                  peak_gbs=peak, frac=round(fp8["achieved_gbs"] / peak, 4)),
+        "gpu_launches": head_blk["gpu_launches"],
+        "clocks": head_blk["clocks"],
+        "wall_s_timed_region": head_blk["wall_s_timed_region"],
+        "workloads": blocks,
     }
     if rank == 0 and not args.no_cpu_baseline:
         cache = _OracleCache(wl)
@@ -571,7 +669,10 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", type=int, default=4, choices=range(5))
+    ap.add_argument("--workload", type=int, default=None, choices=range(5),
+                    help="one workload only (default: all five, the last, 4, as the headline)")
+    ap.add_argument("--soak", type=float, default=1.0,
+                    help="seconds of the same step run, clock-sampled, before the timed steps")
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the cpu_baseline legs of the GPU arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -581,6 +682,8 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     if args.impl == "reference":
+        if args.workload is None:
+            args.workload = 4
         run_reference(args)
     else:
         run_gpu(args)

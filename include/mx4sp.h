@@ -196,16 +196,19 @@ size_t topk_select_workspace(int64_t T, int k, int64_t ld_scores);
  *     out[t][h][:] = sum_i softmax(l)_i * dequant(V[s, i])[:]
  * over the indices i of topk_idx[t*k ...] that are >= 0 (negative entries are
  * skipped, so the -1 padding of topk_select is ignored).
- * Logits and the softmax are fp32; the selected list is cut into splits, each
- * split keeps a running max and sum (online softmax), and a merge kernel
- * combines the splits.
+ * Logits and the softmax are fp32.  The selected lists are cut into runs of
+ * entries, one run per warp of a persistent grid and token; each run keeps a
+ * running max and sum (online softmax) and writes its partial result to the
+ * workspace, and a merge kernel combines the runs of each token.
  *
  *   q         bf16 [T, H, 128], contiguous
  *   k_pages, v_pages  uint8 [num_pages, Hkv, 8704] at the given strides
  *   block_table int32 [B, bt_width]; seq_lens int32 [B]
  *   topk_idx  int32 [T, k], ascending indices then -1 padding
  *   out       fp32 [T, H, 128] (output)
- *   ws        workspace of sparse_paged_decode_workspace(T, k) bytes
+ *   ws        workspace of sparse_paged_decode_workspace(T, k) bytes, 16-byte
+ *             aligned; the size depends on the current device's SM count (the
+ *             grid has one CTA per SM), so query it with that device current
  * H == 16 and Hkv == 1 in this library (else MX4_ERR_UNSUPPORTED).  An index
  * outside [0, p] or a bad page id skips that token and sets
  * MX4_STATUS_BAD_INDEX / MX4_STATUS_BAD_PAGE.  A token with no selected index
@@ -221,13 +224,15 @@ size_t sparse_paged_decode_workspace(int64_t T, int k);
 
 /* ---------------------------------------------------------------------------
  * sparse_paged_decode_noalloc -- sparse_paged_decode without a caller
- * workspace.  The paper has no counterpart for it: it exists for callers that cannot
- * allocate device memory (a host framework that owns all device memory and
- * gives an extension only the operation's inputs and outputs, or a C or
- * foreign-language runtime with no device allocator).  Same arguments, result
- * and errors as sparse_paged_decode, minus ws/ws_bytes.
+ * workspace.  The pages this library follows ("vllm.models.minimax_m3.amd.ops.
+ * mxfp4_pages", "vllm.models.minimax_m3.amd.mono.dispatch") have no counterpart
+ * for it: it exists for callers that cannot allocate device memory (a host
+ * framework that owns all device memory and gives an extension only the
+ * operation's inputs and outputs, or a C or foreign-language runtime with no
+ * device allocator).  Same arguments, result and errors as
+ * sparse_paged_decode, minus ws/ws_bytes.
  *
- * The split workspace lives in a fixed array inside the library of
+ * The run workspace lives in a fixed array inside the library of
  * MX4_NOALLOC_SCRATCH_BYTES (32 MiB) of device memory, which every GPU that
  * loads the library holds until the process exits.  A call whose workspace
  * (sparse_paged_decode_workspace(T, k)) exceeds it returns MX4_ERR_WORKSPACE
@@ -235,7 +240,9 @@ size_t sparse_paged_decode_workspace(int64_t T, int k);
  * a device looks up the array's device address (cudaGetSymbolAddress) with
  * that device current: make it before any stream capture.  All calls on a
  * device share the array, so calls that overlap on the GPU race; nothing in it
- * needs clearing between calls.
+ * needs clearing between calls.  The looked-up address (like the device
+ * address of the status word every call uses) is kept for the life of the
+ * process: do not use the library across a cudaDeviceReset of that device.
  * ------------------------------------------------------------------------- */
 #define MX4_NOALLOC_SCRATCH_BYTES (32u << 20)
 int sparse_paged_decode_noalloc(const uint16_t *q, int64_t T, int q_per_seq, int H, int Hkv,
@@ -281,6 +288,47 @@ int index_score_fp8(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t 
                     int64_t page_stride, int64_t num_pages, const int32_t *block_table,
                     int64_t B, int64_t bt_width, const int32_t *seq_lens, float scale,
                     float *scores, int64_t ld_scores, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * mx4_decode_step -- one whole decode step from host memory to host memory:
+ * the step's inputs are copied from one packed host buffer to the device, the
+ * new tokens' K/V/index-K rows are inserted (mx4_insert), the index keys are
+ * scored (index_score), the top-k selected (topk_select), attention computed
+ * (sparse_paged_decode), and the output copied back to host memory.  This is
+ * the chain the scorer and pa_decode form over the same pages
+ * ("vllm.models.minimax_m3.amd.ops.mxfp4_pages", module description), with the
+ * insert through the shared slot mapping first ("vllm.models.minimax_m3.amd.
+ * mono.dispatch", _slots_shared).
+ *
+ *   h_inputs   HOST buffer of mx4_decode_step_input_bytes(T, n_new) bytes laid
+ *              out as mx4_decode_step_input_offsets gives: q bf16 [T, 16, 128],
+ *              iq bf16 [T, 128], k_new fp32 [n_new, 128], v_new fp32
+ *              [n_new, 128], idx_k_new fp32 [n_new, 128], slots int64 [n_new]
+ *              (n_new = 0: no insert).  Page-locked memory makes the copy
+ *              asynchronous; pageable memory works but the copy blocks the host.
+ *   d_staging  DEVICE buffer of at least the same size (the copy's target)
+ *   caches, tables, q_per_seq, k, scale: as the four calls above (H = 16,
+ *              Hkv = 1); T = B * q_per_seq
+ *   d_scores   fp32 [T, ld_scores]; d_topk_idx int32 [T, k]; d_out fp32
+ *              [T, 16, 128]; topk_ws / dec_ws the two workspaces (device)
+ *   h_out      HOST fp32 [T, 16, 128]: receives the step's attention output
+ * Everything is enqueued on `stream` and the call returns without waiting:
+ * h_out holds the result once the stream reaches this point (synchronise the
+ * stream or record an event).  Errors as the four calls; the first failing
+ * stage's status is returned and nothing after it is enqueued.
+ * ------------------------------------------------------------------------- */
+size_t mx4_decode_step_input_bytes(int64_t T, int64_t n_new);
+/* offsets[0..5] = byte offsets of q, iq, k_new, v_new, idx_k_new, slots in the
+ * packed input buffer (each a multiple of 256). */
+void mx4_decode_step_input_offsets(int64_t T, int64_t n_new, size_t offsets[6]);
+int mx4_decode_step(const void *h_inputs, int64_t n_new, void *d_staging, size_t staging_bytes,
+                    uint8_t *k_pages, uint8_t *v_pages, int64_t kv_page_stride,
+                    int64_t kv_head_stride, uint8_t *idx_pages, int64_t idx_page_stride,
+                    int64_t num_pages, const int32_t *block_table, int64_t B, int64_t bt_width,
+                    const int32_t *seq_lens, int q_per_seq, int k, float scale, float *d_scores,
+                    int64_t ld_scores, int32_t *d_topk_idx, void *topk_ws, size_t topk_ws_bytes,
+                    void *dec_ws, size_t dec_ws_bytes, float *d_out, float *h_out,
+                    void *stream);
 
 /* ---------------------------------------------------------------------------
  * mx4_check_status -- synchronise `stream`, return MX4_OK if no kernel of this

@@ -20,7 +20,8 @@ import torch
 
 __all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
-           "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES",
+           "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "mx4_decode_step",
+           "mx4_decode_step_input_layout",
            "mx4_last_error", "mx4_page_bytes", "library_path", "Mx4Error", "PAGE_BYTES",
            "PAGE_TOKENS", "HEAD_DIM"]
 
@@ -90,6 +91,14 @@ def _load():
         lib.sparse_paged_decode_noalloc.restype = i32
         lib.sparse_paged_decode_noalloc.argtypes = [P, i64, i32, i32, i32, P, P, i64, i64, i64, P,
                                                     i64, i64, P, P, i32, ctypes.c_float, P, P]
+        lib.mx4_decode_step_input_bytes.restype = sz
+        lib.mx4_decode_step_input_bytes.argtypes = [i64, i64]
+        lib.mx4_decode_step_input_offsets.restype = None
+        lib.mx4_decode_step_input_offsets.argtypes = [i64, i64, ctypes.POINTER(sz)]
+        lib.mx4_decode_step.restype = i32
+        lib.mx4_decode_step.argtypes = [P, i64, P, sz, P, P, i64, i64, P, i64, i64, P, i64, i64,
+                                        P, i32, i32, ctypes.c_float, P, i64, P, P, sz, P, sz, P,
+                                        P, P]
         lib.mx4_check_status.restype = i32
         lib.mx4_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         _lib = lib
@@ -338,7 +347,7 @@ def sparse_paged_decode(q, q_per_seq, k_pages, v_pages, block_table, seq_lens, t
 
 def sparse_paged_decode_noalloc(q, q_per_seq, k_pages, v_pages, block_table, seq_lens, topk_idx,
                                 scale, out, stream=None):
-    """sparse_paged_decode for callers that cannot allocate device memory: the split
+    """sparse_paged_decode for callers that cannot allocate device memory: the run
     workspace is the library's own fixed NOALLOC_SCRATCH_BYTES array, so no
     workspace argument is taken and nothing is allocated.  Calls on one device
     share that array and must not overlap on the GPU."""
@@ -366,6 +375,64 @@ def sparse_paged_decode_noalloc(q, q_per_seq, k_pages, v_pages, block_table, seq
         k_pages.stride(0), k_pages.stride(1), int(k_pages.shape[0]), _ptr(block_table),
         int(seq_lens.shape[0]), int(block_table.shape[1]), _ptr(seq_lens), _ptr(topk_idx),
         int(topk_idx.shape[1]), float(scale), _ptr(out), _stream(stream)))
+
+
+def _host_ptr(t, name):
+    # The step's input and output buffers live in host memory (page-locked for an
+    # asynchronous copy); a device tensor here would be read as a host address.
+    if t.device.type != "cpu" or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous host (CPU) tensor")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def mx4_decode_step_input_layout(T, n_new):
+    """(offsets of q, iq, k_new, v_new, idx_k_new, slots in the packed input buffer,
+    its total bytes) for mx4_decode_step."""
+    off = (ctypes.c_size_t * 6)()
+    _load().mx4_decode_step_input_offsets(int(T), int(n_new), off)
+    return [int(x) for x in off], int(_load().mx4_decode_step_input_bytes(int(T), int(n_new)))
+
+
+def mx4_decode_step(h_inputs, n_new, d_staging, k_pages, v_pages, idx_pages, block_table,
+                    seq_lens, q_per_seq, k, scale, d_scores, d_topk_idx, topk_ws, dec_ws, d_out,
+                    h_out, stream=None):
+    """One decode step from host memory to host memory: copy the packed host inputs
+    (uint8 CPU tensor, layout mx4_decode_step_input_layout) to d_staging, insert the
+    n_new new tokens, score, select, attend, and copy the output (fp32 [T, 16, 128])
+    into the host tensor h_out.  Asynchronous on `stream`."""
+    _need(h_inputs, torch.uint8, "h_inputs")
+    _need(h_out, torch.float32, "h_out")
+    _need(d_staging, torch.uint8, "d_staging")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(d_scores, torch.float32, "d_scores")
+    _need(d_topk_idx, torch.int32, "d_topk_idx")
+    _need(d_out, torch.float32, "d_out")
+    _pages(k_pages, "k_pages", 3)
+    _pages(v_pages, "v_pages", 3)
+    _pages(idx_pages, "idx_pages", 2)
+    if k_pages.stride() != v_pages.stride() or k_pages.shape != v_pages.shape:
+        raise ValueError("k_pages and v_pages must have the same shape and strides")
+    B = int(seq_lens.shape[0])
+    T = B * int(q_per_seq)
+    _, nbytes = mx4_decode_step_input_layout(T, n_new)
+    if h_inputs.numel() < nbytes or d_staging.numel() < nbytes:
+        raise ValueError(f"input buffers need {nbytes} bytes")
+    _dims(h_out, "h_out", T, 16, HEAD_DIM)
+    _dims(d_out, "d_out", T, 16, HEAD_DIM)
+    _dims(d_topk_idx, "d_topk_idx", T, int(k))
+    _dims(d_scores, "d_scores", None, None)
+    _rows_at_least(d_scores, T, "d_scores")
+    _rows_at_least(block_table, B, "block_table")
+    tws = 0 if topk_ws is None else topk_ws.numel() * topk_ws.element_size()
+    _check(_load().mx4_decode_step(
+        _host_ptr(h_inputs, "h_inputs"), int(n_new), _ptr(d_staging), d_staging.numel(),
+        _ptr(k_pages), _ptr(v_pages), k_pages.stride(0), k_pages.stride(1), _ptr(idx_pages),
+        idx_pages.stride(0), int(k_pages.shape[0]), _ptr(block_table), B,
+        int(block_table.shape[1]), _ptr(seq_lens), int(q_per_seq), int(k), float(scale),
+        _ptr(d_scores), d_scores.stride(0), _ptr(d_topk_idx), _ptr(topk_ws), tws, _ptr(dec_ws),
+        dec_ws.numel() * dec_ws.element_size(), _ptr(d_out), _host_ptr(h_out, "h_out"),
+        _stream(stream)))
 
 
 def mx4_check_status(stream=None) -> int:

@@ -1,6 +1,6 @@
 // sparse_paged_decode: GQA decode attention (16 query heads sharing one KV head,
-// head_dim 128) over the selected tokens' MXFP4 K/V rows, split over the
-// selected list with an online softmax per split and a merge kernel.
+// head_dim 128) over the selected tokens' MXFP4 K/V rows, with an online
+// softmax over each run of selected entries and a merge of the runs.
 //
 // K/V pages are [pages, heads, 8704] ("vllm.models.minimax_m3.amd.ops.
 // mxfp4_pages", mxfp4_page_views: the [pages, heads, 128, 64] /
@@ -9,64 +9,62 @@
 // _build_cp_qkv), i.e. 16 query heads over one KV head, which makes the 16
 // heads the M = 16 side of a tensor-core MMA.
 //
-// split kernel -- one CTA of 8 warps per (decode token, split of up to 512
-// selected entries); warp w owns the 16-entry tiles w, w+8, w+16, w+24:
-//   1. The sequence's block-table row goes to shared memory and warp 0 turns Q
-//      into f16 MMA A fragments (bf16 scaled by a power of two, exact), kept in
-//      shared memory.  Each warp then resolves its tiles' entries to page rows
-//      and issues the gathers of all their scale words (one cp.async group),
-//      then of each tile's 64 B K and V rows (one group per tile; rows padded
-//      to 80 B so the fragment loads are bank-conflict free).
-//   2. When the scale words land, the warp derives, for its 64 entries, the V
-//      reference per 32-dim block (largest scale byte), K factors
-//      2^(scale - 127) and exact f16 V multipliers 2^(scale - reference).
-//   3. Each tile is processed as soon as its rows land, with no block-wide
-//      step: S = Q K^T with mma.sync m16n8k16 (K = hardware e2m1 -> f16,
-//      exact), one accumulator per 32-dim scale block, so the K scales are
-//      applied exactly in fp32; online softmax in fp32 (log2 units, lazy
-//      rescaling; weights scaled by 2^7 so the f16 P stays normal); P split
-//      into f16 hi + lo parts so P V keeps ~22 bits; O += P V with mma.sync, V
-//      fragments built by zipping the nibbles of two entries so one cvt yields
-//      an (entry, entry) pair, times the V multipliers.
-//   4. The 8 warps' (max, sum, O) are merged in shared memory, one float4 per
-//      lane and MMA n-tile (bank-conflict free), and the split writes its
-//      unnormalised [head][dim] output plus its running max (log2 units) and
-//      sum per head.
-// merge kernel -- one CTA per decode token combines the splits.
+// Work.  The selected lists of all decode tokens are cut into tiles of 16
+// entries (ceil(k / 16) tiles per token), and the tiles, token after token, into
+// equal contiguous ranges, one per warp of a persistent grid (one CTA of 8 warps
+// per SM).  Each warp streams its range through a ring of kRing shared-memory
+// tile slots with cp.async, so the gathers of the next kRing - 1 tiles are in
+// flight while it computes one.  The address of a selected row takes two
+// dependent loads (top-k index, then block-table entry); they run one and two
+// tiles ahead of the copies, so no wait sits on the critical path.
+//
+// On this GPU a random 64-byte row read costs a 128-byte DRAM access, so a
+// sparse selection moves up to twice the layout's 68 bytes per row; keeping
+// many rows in flight is what the kernel can do about it.
+//
+// Math per tile (tensor cores, mma.sync m16n8k16, fp32 accumulation):
+//   S = Q K^T with one accumulator per 32-dim scale block (K codes by the exact
+//   hardware e2m1 -> f16 conversion; the K scales applied in fp32);
+//   online softmax in log2 units with lazy rescaling (weights scaled by 2^7 so
+//   the f16 P stays normal); P split into f16 hi + lo parts so P V keeps about
+//   22 bits; O += P V with V fragments built by zipping the nibbles of two
+//   entries, times exact f16 multipliers 2^(scale - reference), where the
+//   reference is the warp's running largest scale byte per 32-dim block (O is
+//   rescaled by a power of two when it grows).
+// At each token boundary of its range a warp writes its run's partial result
+// (unnormalised O, running max and sum per head) to the workspace; the merge
+// kernel combines the runs of each token.
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace mx4 {
 
 constexpr int kHeads = 16;
-constexpr int kDecWarps = 8;
+constexpr int kDecWarps = 8;                        // warps per CTA (one CTA per SM)
 constexpr int kDecThreads = kDecWarps * 32;
-constexpr int kSplitTokens = 512;                   // selected entries per CTA
+constexpr int kRing = 4;                            // tile slots per warp
 constexpr int kTile = 16;                           // entries per MMA tile
-constexpr int kTiles = kSplitTokens / kTile;        // 32
-constexpr int kTilesPerWarp = kTiles / kDecWarps;   // 4
 constexpr int kRowPitch = 80;                       // staged row pitch (64 B + 16 B pad)
 constexpr int kTileV = kTile * kRowPitch;           // V rows follow the K rows
 constexpr int kTileSw = 2 * kTile * kRowPitch;      // then 16 K and 16 V scale words
 constexpr int kTileBytes = kTileSw + 2 * kTile * 4; // 2688 B
-constexpr int kBtCache = 2048;                      // block-table entries kept in smem
-constexpr int kFrag = kHeads * kHeadDim;            // 2048 outputs per split
+constexpr int kFrag = kHeads * kHeadDim;            // 2048 outputs per token
+constexpr int kRecFloats = kFrag + 2 * kHeads;      // partial record: O, max, sum
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kPScale = 128.f;  // p' = 2^(logit - m) * 2^7, at most 2^15 in f16
 constexpr float kLazy = 8.f;      // rescale only when the max grows by more than this
-static_assert(kTilesPerWarp * kDecWarps == kTiles && kTilesPerWarp == 4, "split geometry");
 static_assert(kTileBytes % 16 == 0, "16-byte aligned tiles");
-static_assert(kDecWarps * kFrag * 4 <= kDecWarps * kTilesPerWarp * kTileBytes,
-              "merge buffer fits in the tiles");
 
+struct WarpSmem {
+  uint8_t slot[kRing][kTileBytes];  // the ring of gathered tiles
+  uint4 qfrag[8][32];               // Q A fragments of the current token, per k16 slice and lane
+  float4 kf[kTile];                 // K scale factors 2^(s_b - 127) * cQ of the tile computed
+  uint16_t vm16[4][kTile];          // f16 V multipliers [block][entry] of that tile
+  uint32_t okm[kRing];              // valid-entry mask (bit 2e) of each slot
+};
 struct DecodeSmem {
-  uint8_t tile[kDecWarps][kTilesPerWarp][kTileBytes];  // 84 KB; reused by the final merge
-  uint4 qfrag[8][32];                                  // Q A fragments, per k16 slice and lane
-  float4 kf[kDecWarps][kTilesPerWarp][kTile];          // K scale factors 2^(s_b - 127) * cQ
-  uint16_t vm16[kDecWarps][kTilesPerWarp][4][kTile];   // f16 V multipliers [tile][block][entry]
-  int32_t bt[kBtCache];                                // the sequence's block-table row
-  float red_m[kDecWarps][kHeads];
-  float red_l[kDecWarps][kHeads];
-  int sigma;
+  WarpSmem w[kDecWarps];
 };
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
@@ -78,7 +76,6 @@ __device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool va
                "r"(valid ? 4 : 0));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n"); }
-__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;\n" ::: "memory"); }
 // wait until at most N of this thread's cp.async groups are pending
 template <int N>
 __device__ __forceinline__ void cp_async_wait_pending() {
@@ -121,422 +118,551 @@ __device__ __forceinline__ uint32_t drop_nan_bytes(uint32_t w) {
   return w & ~__vcmpeq4(w, 0xFFFFFFFFu);
 }
 
-__global__ void __launch_bounds__(kDecThreads, 2)
-decode_split_kernel(const uint16_t* __restrict__ q, int Q, const uint8_t* __restrict__ k_pages,
-                    const uint8_t* __restrict__ v_pages, int64_t kv_page_stride,
-                    int64_t num_pages, const int32_t* __restrict__ block_table, int64_t bt_width,
-                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ topk,
-                    int kw, float scale, int S, float* __restrict__ ws_o,
-                    float* __restrict__ ws_ml, uint32_t* status) {
-  extern __shared__ __align__(128) uint8_t smem_raw[];
-  DecodeSmem& s = *reinterpret_cast<DecodeSmem*>(smem_raw);
+// First tile of the range of warp g: the T * NT tiles cut into NW equal ranges.
+__host__ __device__ __forceinline__ int64_t warp_tile_begin(int64_t g, int64_t U, int64_t NW) {
+  return U * g / NW;
+}
 
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_launch_dependents();
+// Per-launch constants of the split kernel.
+struct DecodeArgs {
+  const uint16_t* q;
+  const uint8_t* k_pages;
+  const uint8_t* v_pages;
+  int64_t kv_page_stride;
+  int64_t num_pages;
+  const int32_t* block_table;
+  int64_t bt_width;
+  const int32_t* seq_lens;
+  const int32_t* topk;
+  float* ws;  // partial records [NW + T][kRecFloats]
+  uint32_t* status;
+  int64_t U;  // tiles in all
+  int NT;     // tiles per token
+  int kw;     // top-k width (entries per token)
+  int Q;      // decode tokens per sequence
+  float scale;
+};
+
+// Q of token t as f16 A fragments, into this warp's qfrag: bf16 scaled by 2^sigma
+// so the largest magnitude lands in [2^14, 2^15).  The conversion is exact for
+// every element whose exponent is at most 31 below the largest one's; smaller
+// elements round on the f16 subnormal grid (2^-24 after scaling).  Returns sigma.
+__device__ __forceinline__ int load_q_fragments(const uint16_t* __restrict__ q, int64_t t,
+                                                WarpSmem& w, int lane) {
   const int g = lane >> 2, tig = lane & 3;
-  const int64_t t = blockIdx.x / S;
-  const int sp = blockIdx.x % S;
-  const int64_t seq = t / Q;
-  const int64_t p = (int64_t)seq_lens[seq] - Q + (t % Q);
-  const int begin = sp * kSplitTokens;
-  const int cnt = max(0, min(kSplitTokens, kw - begin));
-
-  // ---- 1a. block-table row; Q as f16 A fragments (warp 0), scaled by 2^sigma
-  // so that bf16 fits f16 exactly
-  const int64_t npg = min(bt_width, max((int64_t)0, p / kPageTokens + 1));
-  for (int j = tid; j < min(npg, (int64_t)kBtCache); j += kDecThreads)
-    s.bt[j] = block_table[seq * bt_width + j];
-  if (warp == 0) {
-    uint4 qraw[2][4];
+  uint4 qraw[2][4];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-      for (int b = 0; b < 4; ++b)
-        qraw[hh][b] = *reinterpret_cast<const uint4*>(
-            q + (t * kHeads + g + 8 * hh) * kHeadDim + 32 * b + 8 * tig);
-    uint32_t amax = 0;
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const uint32_t w[4] = {qraw[hh][b].x, qraw[hh][b].y, qraw[hh][b].z, qraw[hh][b].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          amax = max(amax, (w[j] << 17) >> 1);     // |low bf16| as fp32 bits
-          amax = max(amax, (w[j] & 0x7FFF0000u));  // |high bf16|
-        }
-      }
-    amax = __reduce_max_sync(0xFFFFFFFFu, amax);
-    const int e = (int)(amax >> 23) - 127;
-    const int sigma = (amax == 0u) ? 0 : min(127, max(-126, 14 - e));
-    const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
+  for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
     for (int b = 0; b < 4; ++b)
+      qraw[hh][b] = *reinterpret_cast<const uint4*>(q + (t * kHeads + g + 8 * hh) * kHeadDim +
+                                                    32 * b + 8 * tig);
+  uint32_t amax = 0;
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        // slice 2b+h: k = 2tig,2tig+1 <-> dims 32b+8tig+4h+{0,1}; k = 2tig+8,+9 <-> +{2,3}
-        const uint32_t w0 = h ? qraw[0][b].z : qraw[0][b].x, w1 = h ? qraw[0][b].w : qraw[0][b].y;
-        const uint32_t u0 = h ? qraw[1][b].z : qraw[1][b].x, u1 = h ? qraw[1][b].w : qraw[1][b].y;
-        s.qfrag[2 * b + h][lane] = make_uint4(
-            pack_f16x2(bf16_bits_to_float(w0 & 0xFFFFu) * sc, bf16_bits_to_float(w0 >> 16) * sc),
-            pack_f16x2(bf16_bits_to_float(u0 & 0xFFFFu) * sc, bf16_bits_to_float(u0 >> 16) * sc),
-            pack_f16x2(bf16_bits_to_float(w1 & 0xFFFFu) * sc, bf16_bits_to_float(w1 >> 16) * sc),
-            pack_f16x2(bf16_bits_to_float(u1 & 0xFFFFu) * sc, bf16_bits_to_float(u1 >> 16) * sc));
+  for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t x[4] = {qraw[hh][b].x, qraw[hh][b].y, qraw[hh][b].z, qraw[hh][b].w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        amax = max(amax, (x[j] << 17) >> 1);     // |low bf16| as fp32 bits
+        amax = max(amax, (x[j] & 0x7FFF0000u));  // |high bf16|
       }
-    if (lane == 0) s.sigma = sigma;
-  }
-  pdl_wait();  // top-k indices and pages are touched from here on
+    }
+  amax = __reduce_max_sync(0xFFFFFFFFu, amax);
+  const int e = (int)(amax >> 23) - 127;
+  // sigma puts the largest |q| near 2^14 (never above it, so no f16 overflow); the
+  // upper clamp keeps 2^-sigma, folded into the K factors, a normal fp32 number
+  const int sigma = (amax == 0u) ? 0 : min(100, max(-113, 14 - e));
+  const float sc = __uint_as_float((uint32_t)(127 + sigma) << 23);
+#pragma unroll
+  for (int b = 0; b < 4; ++b)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      // slice 2b+h: k = 2tig,2tig+1 <-> dims 32b+8tig+4h+{0,1}; k = 2tig+8,+9 <-> +{2,3}
+      const uint32_t w0 = h ? qraw[0][b].z : qraw[0][b].x, w1 = h ? qraw[0][b].w : qraw[0][b].y;
+      const uint32_t u0 = h ? qraw[1][b].z : qraw[1][b].x, u1 = h ? qraw[1][b].w : qraw[1][b].y;
+      w.qfrag[2 * b + h][lane] = make_uint4(
+          pack_f16x2(bf16_bits_to_float(w0 & 0xFFFFu) * sc, bf16_bits_to_float(w0 >> 16) * sc),
+          pack_f16x2(bf16_bits_to_float(u0 & 0xFFFFu) * sc, bf16_bits_to_float(u0 >> 16) * sc),
+          pack_f16x2(bf16_bits_to_float(w1 & 0xFFFFu) * sc, bf16_bits_to_float(w1 >> 16) * sc),
+          pack_f16x2(bf16_bits_to_float(u1 & 0xFFFFu) * sc, bf16_bits_to_float(u1 >> 16) * sc));
+    }
+  return sigma;
+}
 
-  // ---- 1b. this warp's entries: lane l takes entry l/2 of each tile, its K row
-  // and K scale word (even l) or its V row and V scale word (odd l)
-  const int r = lane >> 1;
-  const bool isv = (lane & 1) != 0;
-  int32_t idx[kTilesPerWarp];
-#pragma unroll
-  for (int u = 0; u < kTilesPerWarp; ++u) {
-    const int e = (warp + kDecWarps * u) * kTile + r;
-    idx[u] = (e < cnt) ? topk[t * kw + begin + e] : -1;
-  }
-  __syncthreads();  // block-table row and Q fragments
-  uint32_t okm[kTilesPerWarp];
-  int rows[kTilesPerWarp];
-  const uint8_t* srcs[kTilesPerWarp];
-#pragma unroll
-  for (int u = 0; u < kTilesPerWarp; ++u) {
-    const int32_t i = idx[u];
-    bool ok = false;
-    const uint8_t* src = isv ? v_pages : k_pages;
-    if (i >= 0) {
-      if (i > p || (int64_t)i / kPageTokens >= bt_width) {
-        flag(status, MX4_STATUS_BAD_INDEX);
-      } else {
-        const int64_t slot = i / kPageTokens;
-        const int32_t pid = slot < kBtCache ? s.bt[slot] : block_table[seq * bt_width + slot];
-        if (pid < 0 || pid >= num_pages) {
-          flag(status, MX4_STATUS_BAD_PAGE);
+// 2^e as fp32 for e <= 127 (0 below the normal range).
+__device__ __forceinline__ float pow2f(int e) {
+  return e >= -126 ? __uint_as_float((uint32_t)(127 + e) << 23) : 0.f;
+}
+__device__ __forceinline__ int byte_of(uint32_t w, int b) { return (int)((w >> (8 * b)) & 0xFFu); }
+
+__global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const DecodeArgs a) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  DecodeSmem& sm = *reinterpret_cast<DecodeSmem*>(smem_raw);
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  WarpSmem& w = sm.w[warp];
+  pdl_launch_dependents();
+  const int g = lane >> 2, tig = lane & 3;
+  const int r = lane >> 1;           // entry of a tile whose row this lane gathers
+  const bool isv = (lane & 1) != 0;  // its V row and scale word (odd lanes) or K's (even)
+  const int64_t NW = (int64_t)gridDim.x * kDecWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kDecWarps + warp;
+  const int64_t u0 = warp_tile_begin(gw, a.U, NW), u1 = warp_tile_begin(gw + 1, a.U, NW);
+  pdl_wait();  // top-k indices (and q, pages) are touched from here on
+  if (u0 >= u1) return;  // no CTA-wide barrier in this kernel
+
+  // ---- the address pipeline: top-k index -> block-table entry -> copies.  Each
+  // stage walks the tiles in order, so its (token, tile of the token, sequence,
+  // position) advances by one tile at a time without divisions.
+  struct Pos {
+    int64_t u;
+    int t, j, seq;
+    int64_t p;  // the token's position: it attends to cached tokens 0 .. p
+  };
+  auto at = [&](int64_t u) {
+    Pos x;
+    x.u = u;
+    x.t = (int)(u / a.NT);
+    x.j = (int)(u - (int64_t)x.t * a.NT);
+    x.seq = x.t / a.Q;
+    x.p = u < u1 ? (int64_t)__ldg(a.seq_lens + x.seq) - a.Q + (x.t - x.seq * a.Q) : -1;
+    return x;
+  };
+  auto next = [&](Pos& x) {
+    ++x.u;
+    if (++x.j == a.NT) {
+      x.j = 0;
+      ++x.t;
+      x.seq = x.t / a.Q;
+      x.p = x.u < u1 ? (int64_t)__ldg(a.seq_lens + x.seq) - a.Q + (x.t - x.seq * a.Q) : -1;
+    }
+  };
+  auto load_idx = [&](const Pos& x) -> int32_t {
+    if (x.u >= u1) return -1;
+    const int e = x.j * kTile + r;
+    return e < a.kw ? __ldg(a.topk + (int64_t)x.t * a.kw + e) : -1;
+  };
+  auto resolve = [&](const Pos& x, int32_t i, int32_t& row) -> int32_t {
+    row = -1;
+    if (i < 0 || x.u >= u1) return -1;
+    const uint32_t slot = (uint32_t)i >> 7;
+    if ((int64_t)i > x.p || (int64_t)slot >= a.bt_width) {
+      if (!isv) flag(a.status, MX4_STATUS_BAD_INDEX);
+      return -1;
+    }
+    row = i & (kPageTokens - 1);
+    return __ldg(a.block_table + (int64_t)x.seq * a.bt_width + slot);
+  };
+  auto issue = [&](int64_t u, int sl, int32_t pid, int32_t row) {
+    if (u < u1) {
+      bool ok = false;
+      const uint8_t* src = isv ? a.v_pages : a.k_pages;
+      if (row >= 0) {
+        if (pid < 0 || pid >= a.num_pages) {
+          if (!isv) flag(a.status, MX4_STATUS_BAD_PAGE);
         } else {
-          src += (int64_t)pid * kv_page_stride;
+          src += (int64_t)pid * a.kv_page_stride;
           ok = true;
         }
       }
+      const uint32_t okm = __ballot_sync(0xFFFFFFFFu, ok);  // bit 2e: entry e valid
+      if (lane == 0) w.okm[sl] = okm;
+      const uint32_t base = smem_addr(&w.slot[sl][0]);
+      cp_async4(base + kTileSw + (isv ? kTile * 4 : 0) + r * 4,
+                src + kScaleOffset + (ok ? row : 0) * kRowScaleBytes, ok);
+      const uint32_t dst = base + (isv ? kTileV : 0) + r * kRowPitch;
+      const uint8_t* rs = src + (ok ? row : 0) * kRowDataBytes;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) cp_async16(dst + 16 * c, rs + 16 * c, ok);
     }
-    rows[u] = ok ? (i % kPageTokens) : -1;
-    srcs[u] = src;
-    okm[u] = __ballot_sync(0xFFFFFFFFu, ok);  // bit 2e: entry e of the tile is valid
-    cp_async4(smem_addr(&s.tile[warp][u][0]) + kTileSw + (isv ? kTile * 4 : 0) + r * 4,
-              src + kScaleOffset + (ok ? rows[u] : 0) * kRowScaleBytes, ok);
-  }
-  cp_async_commit();  // group: the scale words of all four tiles
+    cp_async_commit();  // one group per tile (empty past the range)
+  };
+
+  // prologue: the first kRing tiles' indices and pages (independent loads), the
+  // copies of the first kRing - 1
+  int32_t pid_b, row_b, i_a;
+  Pos x_res, x_idx;  // the tiles whose page / index the loop looks up next
+  {
+    int32_t ii[kRing], pp[kRing], rr[kRing];
+    Pos x = at(u0);
+    Pos xs[kRing];
 #pragma unroll
-  for (int u = 0; u < kTilesPerWarp; ++u) {
-    const bool ok = rows[u] >= 0;
-    const uint32_t dst = smem_addr(&s.tile[warp][u][0]) + (isv ? kTileV : 0) + r * kRowPitch;
-    const uint8_t* src = srcs[u] + (ok ? rows[u] : 0) * kRowDataBytes;
+    for (int s = 0; s < kRing; ++s) {
+      xs[s] = x;
+      ii[s] = load_idx(x);
+      next(x);
+    }
 #pragma unroll
-    for (int c = 0; c < 4; ++c) cp_async16(dst + 16 * c, src + 16 * c, ok);
-    cp_async_commit();  // group: the K and V rows of tile u
+    for (int s = 0; s < kRing; ++s) pp[s] = resolve(xs[s], ii[s], rr[s]);
+#pragma unroll
+    for (int s = 0; s < kRing - 1; ++s) issue(u0 + s, s, pp[s], rr[s]);
+    pid_b = pp[kRing - 1];
+    row_b = rr[kRing - 1];
+    x_res = x;  // tile u0 + kRing
+    i_a = load_idx(x_res);
+    x_idx = x_res;
+    next(x_idx);  // tile u0 + kRing + 1
   }
 
-  // logit (log2 units) = sum_b S_b * 2^(scale_b - 127) * cQ
-  const float cQ = ldexpf(scale * kLog2e, -s.sigma);
-
-  // ---- 1c. scale tables of the warp's 64 entries (while the rows are in flight):
-  // the V reference per 32-dim block (largest valid scale byte, NaN excluded),
-  // K factors 2^(s_b - 127) * cQ and f16 V multipliers 2^(s_b - ref_b)
-  cp_async_wait_pending<kTilesPerWarp>();
-  __syncwarp();
-  uint32_t refV = 0u;
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int u = (lane >> 4) + 2 * h, er = lane & 15;  // entries lane and lane + 32
-    const uint32_t* sw = reinterpret_cast<const uint32_t*>(&s.tile[warp][u][kTileSw]);
-    if ((okm[u] >> (2 * er)) & 1u) refV = __vmaxu4(refV, drop_nan_bytes(sw[kTile + er]));
-  }
-#pragma unroll
-  for (int of = 16; of > 0; of >>= 1) refV = __vmaxu4(refV, __shfl_xor_sync(0xFFFFFFFFu, refV, of));
-#pragma unroll
-  for (int h = 0; h < 2; ++h) {
-    const int u = (lane >> 4) + 2 * h, er = lane & 15;
-    const uint32_t* sw = reinterpret_cast<const uint32_t*>(&s.tile[warp][u][kTileSw]);
-    const uint32_t kw4 = sw[er], vw4 = sw[kTile + er];
-    s.kf[warp][u][er] = make_float4(e8m0_to_float(kw4 & 0xFFu) * cQ,
-                                    e8m0_to_float((kw4 >> 8) & 0xFFu) * cQ,
-                                    e8m0_to_float((kw4 >> 16) & 0xFFu) * cQ,
-                                    e8m0_to_float(kw4 >> 24) * cQ);
-#pragma unroll
-    for (int b = 0; b < 4; ++b)
-      s.vm16[warp][u][b][er] =
-          (uint16_t)f16_pow2((vw4 >> (8 * b)) & 0xFFu, (refV >> (8 * b)) & 0xFFu);
-  }
-  __syncwarp();
-
-  // ---- 3. this warp's tiles
+  // ---- per-run state
   float o[16][4];
-#pragma unroll
-  for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
-  float m_used[2] = {-INFINITY, -INFINITY};
-  float lsum[2] = {0.f, 0.f};
+  float m_used[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
+  uint32_t refV = 0u;  // largest V scale byte per 32-dim block so far (bytes 0..3)
+  float cQ = 0.f;
+  int64_t cur_t = -1;
+  const int blo = tig >> 1, bhi = blo + 2;  // scale blocks of this lane's O columns
 
+  auto flush = [&](int64_t t) {
+    float l0 = lsum[0], l1 = lsum[1];
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 1);
+    l0 += __shfl_xor_sync(0xFFFFFFFFu, l0, 2);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
+    l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
+    float* rec = a.ws + (gw + t) * kRecFloats;
+    const float flo = pow2f(byte_of(refV, blo) - 127), fhi = pow2f(byte_of(refV, bhi) - 127);
+    float4* r4 = reinterpret_cast<float4*>(rec);
 #pragma unroll
-  for (int u = 0; u < kTilesPerWarp; ++u) {
-    if ((warp + kDecWarps * u) * kTile >= cnt) break;
-    if (u == 0) cp_async_wait_pending<3>();  // row groups of tiles u+1 .. 3 may be pending
-    else if (u == 1) cp_async_wait_pending<2>();
-    else if (u == 2) cp_async_wait_pending<1>();
-    else cp_async_wait_pending<0>();
+    for (int j = 0; j < 16; ++j) {
+      const float f = j < 8 ? flo : fhi;
+      r4[j * 32 + lane] = make_float4(o[j][0] * f, o[j][1] * f, o[j][2] * f, o[j][3] * f);
+    }
+    if (tig == 0) {
+      rec[kFrag + g] = m_used[0];
+      rec[kFrag + g + 8] = m_used[1];
+      rec[kFrag + kHeads + g] = l0;
+      rec[kFrag + kHeads + g + 8] = l1;
+    }
+  };
+
+  int sl = 0;  // slot of tile u
+  int t_prev = -1;
+  int t = u0 / a.NT, jt = (int)(u0 - (int64_t)t * a.NT);  // token and tile of token of u
+  for (int64_t u = u0; u < u1; ++u) {
+    // copies of tile u + kRing - 1 (into the slot tile u - 1 used), its page looked
+    // up last iteration; the page of tile u + kRing; the index of tile u + kRing + 1
+    issue(u + kRing - 1, sl == 0 ? kRing - 1 : sl - 1, pid_b, row_b);
+    pid_b = resolve(x_res, i_a, row_b);
+    i_a = load_idx(x_idx);
+    next(x_res);
+    next(x_idx);
+
+    if (t != t_prev) {  // a new run: flush the last one, take this token's Q
+      if (cur_t >= 0) flush(cur_t);
+      cur_t = t;
+      t_prev = t;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+      m_used[0] = m_used[1] = -INFINITY;
+      lsum[0] = lsum[1] = 0.f;
+      refV = 0u;
+      const int sigma = load_q_fragments(a.q, t, w, lane);
+      cQ = a.scale * kLog2e * pow2f(-sigma);  // logit (log2 units) = sum_b S_b 2^(s_b-127) cQ
+    }
+    cp_async_wait_pending<kRing - 1>();  // tile u has landed
     __syncwarp();
-    const uint8_t* sk = &s.tile[warp][u][0];
-    const uint8_t* sv = sk + kTileV;
-    const uint16_t* vm = &s.vm16[warp][u][0][0];
-    const uint32_t okb = okm[u];
-
-    // S = Q K^T per 32-dim scale block, two n8 tiles of entries
-    float acc[2][4][4];
+    const uint32_t okb = w.okm[sl];
+    if (okb != 0u) {
+      const uint8_t* sk = &w.slot[sl][0];
+      const uint8_t* sv = sk + kTileV;
+      const uint32_t* sw = reinterpret_cast<const uint32_t*>(sk + kTileSw);
+      // ---- scale tables of the tile: V reference, K factors, V multipliers
+      {
+        const int er = lane & 15;
+        const uint32_t kwd = sw[er], vwd = sw[kTile + er];
+        uint32_t tmax = ((okb >> (2 * er)) & 1u) ? drop_nan_bytes(vwd) : 0u;
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-      const uint4 qa0 = s.qfrag[2 * b][lane], qa1 = s.qfrag[2 * b + 1][lane];
+        for (int of = 8; of > 0; of >>= 1)
+          tmax = __vmaxu4(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, of));
+        const uint32_t nref = __vmaxu4(refV, tmax);
+        if (nref != refV) {  // warp-uniform: bring O to the larger reference
+          const float flo = pow2f(byte_of(refV, blo) - byte_of(nref, blo));
+          const float fhi = pow2f(byte_of(refV, bhi) - byte_of(nref, bhi));
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt) {
-        acc[nt][b][0] = acc[nt][b][1] = acc[nt][b][2] = acc[nt][b][3] = 0.f;
-        uint32_t f[4];
-        e2m1x8_to_f16x2(
-            *reinterpret_cast<const uint32_t*>(sk + (nt * 8 + g) * kRowPitch + (4 * b + tig) * 4),
-            f);
-        mma_m16n8k16_f16(acc[nt][b], qa0.x, qa0.y, qa0.z, qa0.w, f[0], f[1]);
-        mma_m16n8k16_f16(acc[nt][b], qa1.x, qa1.y, qa1.z, qa1.w, f[2], f[3]);
-      }
-    }
-    // logits of this thread's entries nt*8 + 2 tig + cc (heads g and g + 8)
-    float lg[2][4];
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-      for (int cc = 0; cc < 2; ++cc) {
-        const int en = nt * 8 + 2 * tig + cc;
-        const float4 kf = s.kf[warp][u][en];
-        const float f[4] = {kf.x, kf.y, kf.z, kf.w};
-        float d0 = 0.f, d1 = 0.f;
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          d0 = fmaf(acc[nt][b][cc], f[b], d0);
-          d1 = fmaf(acc[nt][b][cc + 2], f[b], d1);
+          for (int j = 0; j < 16; ++j) {
+            const float f = j < 8 ? flo : fhi;
+            o[j][0] *= f;
+            o[j][1] *= f;
+            o[j][2] *= f;
+            o[j][3] *= f;
+          }
+          refV = nref;
         }
-        const bool valid = (okb >> (2 * en)) & 1u;
-        lg[nt][cc] = valid ? d0 : -INFINITY;
-        lg[nt][cc + 2] = valid ? d1 : -INFINITY;
-      }
-    float mx[2];
-    mx[0] = fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1]));
-    mx[1] = fmaxf(fmaxf(lg[0][2], lg[0][3]), fmaxf(lg[1][2], lg[1][3]));
+        if (lane < 16) {
+          w.kf[er] = make_float4(e8m0_to_float(kwd & 0xFFu) * cQ,
+                                 e8m0_to_float((kwd >> 8) & 0xFFu) * cQ,
+                                 e8m0_to_float((kwd >> 16) & 0xFFu) * cQ,
+                                 e8m0_to_float(kwd >> 24) * cQ);
+        } else {
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr) {
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xFFFFFFFFu, mx[rr], 1));
-      mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xFFFFFFFFu, mx[rr], 2));
-    }
-    const bool need = mx[0] > m_used[0] + kLazy || mx[1] > m_used[1] + kLazy;
-    if (__any_sync(0xFFFFFFFFu, need)) {
-      float corr[2];
+          for (int b = 0; b < 4; ++b)
+            w.vm16[b][er] = (uint16_t)f16_pow2((vwd >> (8 * b)) & 0xFFu, (refV >> (8 * b)) & 0xFFu);
+        }
+        __syncwarp();
+      }
+      const uint16_t* vm = &w.vm16[0][0];
+
+      // ---- S = Q K^T per 32-dim scale block, two n8 tiles of entries
+      float acc[2][4][4];
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const uint4 qa0 = w.qfrag[2 * b][lane], qa1 = w.qfrag[2 * b + 1][lane];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+          acc[nt][b][0] = acc[nt][b][1] = acc[nt][b][2] = acc[nt][b][3] = 0.f;
+          uint32_t f[4];
+          e2m1x8_to_f16x2(
+              *reinterpret_cast<const uint32_t*>(sk + (nt * 8 + g) * kRowPitch + (4 * b + tig) * 4),
+              f);
+          mma_m16n8k16_f16(acc[nt][b], qa0.x, qa0.y, qa0.z, qa0.w, f[0], f[1]);
+          mma_m16n8k16_f16(acc[nt][b], qa1.x, qa1.y, qa1.z, qa1.w, f[2], f[3]);
+        }
+      }
+      // logits of this thread's entries nt*8 + 2 tig + cc (heads g and g + 8)
+      float lg[2][4];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int en = nt * 8 + 2 * tig + cc;
+          const float4 kf = w.kf[en];
+          const float f[4] = {kf.x, kf.y, kf.z, kf.w};
+          float d0 = 0.f, d1 = 0.f;
+#pragma unroll
+          for (int b = 0; b < 4; ++b) {
+            d0 = fmaf(acc[nt][b][cc], f[b], d0);
+            d1 = fmaf(acc[nt][b][cc + 2], f[b], d1);
+          }
+          const bool valid = (okb >> (2 * en)) & 1u;
+          lg[nt][cc] = valid ? d0 : -INFINITY;
+          lg[nt][cc + 2] = valid ? d1 : -INFINITY;
+        }
+      float mx[2];
+      mx[0] = fmaxf(fmaxf(lg[0][0], lg[0][1]), fmaxf(lg[1][0], lg[1][1]));
+      mx[1] = fmaxf(fmaxf(lg[0][2], lg[0][3]), fmaxf(lg[1][2], lg[1][3]));
 #pragma unroll
       for (int rr = 0; rr < 2; ++rr) {
-        const float nm = mx[rr] > m_used[rr] + kLazy ? mx[rr] : m_used[rr];
-        corr[rr] = (nm == m_used[rr]) ? 1.f : exp2f(m_used[rr] - nm);
-        m_used[rr] = nm;
-        lsum[rr] *= corr[rr];
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xFFFFFFFFu, mx[rr], 1));
+        mx[rr] = fmaxf(mx[rr], __shfl_xor_sync(0xFFFFFFFFu, mx[rr], 2));
       }
+      const bool need = mx[0] > m_used[0] + kLazy || mx[1] > m_used[1] + kLazy;
+      if (__any_sync(0xFFFFFFFFu, need)) {
+        float corr[2];
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        o[j][0] *= corr[0];
-        o[j][1] *= corr[0];
-        o[j][2] *= corr[1];
-        o[j][3] *= corr[1];
+        for (int rr = 0; rr < 2; ++rr) {
+          const float nm = mx[rr] > m_used[rr] + kLazy ? mx[rr] : m_used[rr];
+          corr[rr] = (nm == m_used[rr]) ? 1.f : exp2f(m_used[rr] - nm);
+          m_used[rr] = nm;
+          lsum[rr] *= corr[rr];
+        }
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          o[j][0] *= corr[0];
+          o[j][1] *= corr[0];
+          o[j][2] *= corr[1];
+          o[j][3] *= corr[1];
+        }
       }
-    }
-    // p' = 2^(logit - m) * 2^7: the largest logit gets exactly 128
-    const float mb0 = (m_used[0] == -INFINITY) ? 0.f : m_used[0];
-    const float mb1 = (m_used[1] == -INFINITY) ? 0.f : m_used[1];
-    float pw[2][4];
+      // p' = 2^(logit - m) * 2^7: the largest logit gets exactly 128
+      const float mb0 = (m_used[0] == -INFINITY) ? 0.f : m_used[0];
+      const float mb1 = (m_used[1] == -INFINITY) ? 0.f : m_used[1];
+      float pw[2][4];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-      pw[nt][0] = exp2f(lg[nt][0] - mb0) * kPScale;
-      pw[nt][1] = exp2f(lg[nt][1] - mb0) * kPScale;
-      pw[nt][2] = exp2f(lg[nt][2] - mb1) * kPScale;
-      pw[nt][3] = exp2f(lg[nt][3] - mb1) * kPScale;
-    }
-    lsum[0] += (pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]);
-    lsum[1] += (pw[0][2] + pw[0][3]) + (pw[1][2] + pw[1][3]);
-    // P = hi + lo, both f16
-    uint32_t ph[4], pl[4];
-    ph[0] = pack_f16x2(pw[0][0], pw[0][1]);
-    ph[1] = pack_f16x2(pw[0][2], pw[0][3]);
-    ph[2] = pack_f16x2(pw[1][0], pw[1][1]);
-    ph[3] = pack_f16x2(pw[1][2], pw[1][3]);
-    pl[0] = pack_f16x2(pw[0][0] - f16_lo(ph[0]), pw[0][1] - f16_hi(ph[0]));
-    pl[1] = pack_f16x2(pw[0][2] - f16_lo(ph[1]), pw[0][3] - f16_hi(ph[1]));
-    pl[2] = pack_f16x2(pw[1][0] - f16_lo(ph[2]), pw[1][1] - f16_hi(ph[2]));
-    pl[3] = pack_f16x2(pw[1][2] - f16_lo(ph[3]), pw[1][3] - f16_hi(ph[3]));
+      for (int nt = 0; nt < 2; ++nt) {
+        pw[nt][0] = exp2f(lg[nt][0] - mb0) * kPScale;
+        pw[nt][1] = exp2f(lg[nt][1] - mb0) * kPScale;
+        pw[nt][2] = exp2f(lg[nt][2] - mb1) * kPScale;
+        pw[nt][3] = exp2f(lg[nt][3] - mb1) * kPScale;
+      }
+      lsum[0] += (pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]);
+      lsum[1] += (pw[0][2] + pw[0][3]) + (pw[1][2] + pw[1][3]);
+      // P = hi + lo, both f16
+      uint32_t ph[4], pl[4];
+      ph[0] = pack_f16x2(pw[0][0], pw[0][1]);
+      ph[1] = pack_f16x2(pw[0][2], pw[0][3]);
+      ph[2] = pack_f16x2(pw[1][0], pw[1][1]);
+      ph[3] = pack_f16x2(pw[1][2], pw[1][3]);
+      pl[0] = pack_f16x2(pw[0][0] - f16_lo(ph[0]), pw[0][1] - f16_hi(ph[0]));
+      pl[1] = pack_f16x2(pw[0][2] - f16_lo(ph[1]), pw[0][3] - f16_hi(ph[1]));
+      pl[2] = pack_f16x2(pw[1][0] - f16_lo(ph[2]), pw[1][1] - f16_hi(ph[2]));
+      pl[3] = pack_f16x2(pw[1][2] - f16_lo(ph[3]), pw[1][3] - f16_hi(ph[3]));
 
-    // O += P V: dim tile j = 8h + i, column g <-> dim 8(g + 8h) + i (block (g>>2) + 2h)
+      // ---- O += P V: dim tile j = 8h + i, column g <-> dim 8(g + 8h) + i (block (g>>2) + 2h)
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int wi = (g + 8 * h) * 4;
-      const int bh = (g >> 2) + 2 * h;
-      const uint32_t m01 = *reinterpret_cast<const uint32_t*>(&vm[bh * kTile + 2 * tig]);
-      const uint32_t m89 = *reinterpret_cast<const uint32_t*>(&vm[bh * kTile + 8 + 2 * tig]);
-      const uint32_t wA = *reinterpret_cast<const uint32_t*>(sv + (2 * tig) * kRowPitch + wi);
-      const uint32_t wB = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 1) * kRowPitch + wi);
-      const uint32_t wC = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 8) * kRowPitch + wi);
-      const uint32_t wD = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 9) * kRowPitch + wi);
-      // nibble zip: byte q of ze = (A.dim 2q) | (B.dim 2q) << 4; zo likewise for 2q+1
-      uint32_t ze01[4], zo01[4], ze89[4], zo89[4];
-      e2m1x8_to_f16x2(lop_merge(wA, wB << 4, 0x0F0F0F0Fu), ze01);
-      e2m1x8_to_f16x2(lop_merge(wA >> 4, wB, 0x0F0F0F0Fu), zo01);
-      e2m1x8_to_f16x2(lop_merge(wC, wD << 4, 0x0F0F0F0Fu), ze89);
-      e2m1x8_to_f16x2(lop_merge(wC >> 4, wD, 0x0F0F0F0Fu), zo89);
+      for (int h = 0; h < 2; ++h) {
+        const int wi = (g + 8 * h) * 4;
+        const int bh = (g >> 2) + 2 * h;
+        const uint32_t m01 = *reinterpret_cast<const uint32_t*>(&vm[bh * kTile + 2 * tig]);
+        const uint32_t m89 = *reinterpret_cast<const uint32_t*>(&vm[bh * kTile + 8 + 2 * tig]);
+        const uint32_t wA = *reinterpret_cast<const uint32_t*>(sv + (2 * tig) * kRowPitch + wi);
+        const uint32_t wB = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 1) * kRowPitch + wi);
+        const uint32_t wC = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 8) * kRowPitch + wi);
+        const uint32_t wD = *reinterpret_cast<const uint32_t*>(sv + (2 * tig + 9) * kRowPitch + wi);
+        // nibble zip: byte q of ze = (A.dim 2q) | (B.dim 2q) << 4; zo likewise for 2q+1
+        uint32_t ze01[4], zo01[4], ze89[4], zo89[4];
+        e2m1x8_to_f16x2(lop_merge(wA, wB << 4, 0x0F0F0F0Fu), ze01);
+        e2m1x8_to_f16x2(lop_merge(wA >> 4, wB, 0x0F0F0F0Fu), zo01);
+        e2m1x8_to_f16x2(lop_merge(wC, wD << 4, 0x0F0F0F0Fu), ze89);
+        e2m1x8_to_f16x2(lop_merge(wC >> 4, wD, 0x0F0F0F0Fu), zo89);
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const uint32_t b0 = hmul2((i & 1) ? zo01[i >> 1] : ze01[i >> 1], m01);
-        const uint32_t b1 = hmul2((i & 1) ? zo89[i >> 1] : ze89[i >> 1], m89);
-        mma_m16n8k16_f16(o[8 * h + i], ph[0], ph[1], ph[2], ph[3], b0, b1);
-        mma_m16n8k16_f16(o[8 * h + i], pl[0], pl[1], pl[2], pl[3], b0, b1);
+        for (int i = 0; i < 8; ++i) {
+          const uint32_t b0 = hmul2((i & 1) ? zo01[i >> 1] : ze01[i >> 1], m01);
+          const uint32_t b1 = hmul2((i & 1) ? zo89[i >> 1] : ze89[i >> 1], m89);
+          mma_m16n8k16_f16(o[8 * h + i], ph[0], ph[1], ph[2], ph[3], b0, b1);
+          mma_m16n8k16_f16(o[8 * h + i], pl[0], pl[1], pl[2], pl[3], b0, b1);
+        }
       }
     }
-  }
-  cp_async_wait_all();  // gathers of tiles past the end land before the merge reuses them
-
-  // ---- 4. merge the warps' partial results (fragment order, conflict free)
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr) {
-    lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 1);
-    lsum[rr] += __shfl_xor_sync(0xFFFFFFFFu, lsum[rr], 2);
-  }
-  __syncthreads();  // every warp is done with its tiles
-  if (tig == 0) {
-    s.red_m[warp][g] = m_used[0];
-    s.red_m[warp][g + 8] = m_used[1];
-    s.red_l[warp][g] = lsum[0];
-    s.red_l[warp][g + 8] = lsum[1];
-  }
-  __syncthreads();
-  float M[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-  for (int w = 0; w < kDecWarps; ++w) {
-    M[0] = fmaxf(M[0], s.red_m[w][g]);
-    M[1] = fmaxf(M[1], s.red_m[w][g + 8]);
-  }
-  float fw[2];
-#pragma unroll
-  for (int rr = 0; rr < 2; ++rr)
-    fw[rr] = (m_used[rr] == -INFINITY) ? 0.f : exp2f(m_used[rr] - M[rr]);
-  float fv[4];
-#pragma unroll
-  for (int b = 0; b < 4; ++b) fv[b] = ldexpf(1.f, (int)((refV >> (8 * b)) & 0xFFu) - 127);
-  // elements (j, 0..3) of lane l live in one float4 at red4[warp][j * 32 + l]
-  float4* red4 = reinterpret_cast<float4*>(&s.tile[0][0][0]);
-#pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const float f = fv[(2 * tig + 8 * (j >> 3)) >> 2];
-    const float f0 = fw[0] * f, f1 = fw[1] * f;
-    red4[warp * (kFrag / 4) + j * 32 + lane] =
-        make_float4(o[j][0] * f0, o[j][1] * f0, o[j][2] * f1, o[j][3] * f1);
-  }
-  __syncthreads();
-  // float4 x = j * 32 + lane -> element c: head = g + 8 (c/2) (g = lane/4),
-  // dim = 8 (2 tig + c%2 + 8 (j/8)) + j%8 (tig = lane%4)
-  const int64_t split = t * S + sp;
-  for (int x = tid; x < kFrag / 4; x += kDecThreads) {
-    float4 acc = red4[x];
-#pragma unroll
-    for (int w = 1; w < kDecWarps; ++w) {
-      const float4 y = red4[w * (kFrag / 4) + x];
-      acc.x += y.x;
-      acc.y += y.y;
-      acc.z += y.z;
-      acc.w += y.w;
+    __syncwarp();  // the slot of tile u is reused by the next iteration's copies
+    sl = (sl == kRing - 1) ? 0 : sl + 1;
+    if (++jt == a.NT) {
+      jt = 0;
+      ++t;
     }
-    const int ln = x & 31, j = x >> 5;
-    const int h0 = ln >> 2;
-    const int d0 = 8 * (2 * (ln & 3) + 8 * (j >> 3)) + (j & 7);
-    float* dst = ws_o + split * kFrag;
-    dst[h0 * kHeadDim + d0] = acc.x;
-    dst[h0 * kHeadDim + d0 + 8] = acc.y;
-    dst[(h0 + 8) * kHeadDim + d0] = acc.z;
-    dst[(h0 + 8) * kHeadDim + d0 + 8] = acc.w;
   }
-  if (tid < kHeads) {
-    float Mh = -INFINITY;
-    for (int w = 0; w < kDecWarps; ++w) Mh = fmaxf(Mh, s.red_m[w][tid]);
-    float l = 0.f;
-    if (Mh != -INFINITY)
-      for (int w = 0; w < kDecWarps; ++w)
-        if (s.red_m[w][tid] != -INFINITY) l += s.red_l[w][tid] * exp2f(s.red_m[w][tid] - Mh);
-    ws_ml[(split * kHeads + tid) * 2 + 0] = Mh;
-    ws_ml[(split * kHeads + tid) * 2 + 1] = l;
-  }
+  flush(cur_t);
+  asm volatile("cp.async.wait_all;\n" ::: "memory");  // no copy in flight at exit
 }
 
-// One CTA per decode token; thread (h, part) combines dims 4*part .. 4*part+3 of
-// head h over the splits: out = sum_s O_s 2^(m_s - M) / sum_s l_s 2^(m_s - M),
-// with O_s the split's unnormalised [head][dim] output and (m_s, l_s) its
-// running max (log2 units) and sum for the head.
-constexpr int kMergeThreads = kHeads * (kHeadDim / 4);  // 512
-constexpr int kMaxSplits = 128;
+// One CTA per decode token, thread x = (j, lane) of the fragment order: combines
+// the runs of the token, out = sum_r O_r 2^(m_r - M) / sum_r l_r 2^(m_r - M), with
+// O_r the run's unnormalised output and (m_r, l_r) its running max (log2 units)
+// and sum per head; the runs are those of the warps whose ranges meet the token's
+// tiles.  The result goes through shared memory to a [head][dim] store.
+constexpr int kMergeThreads = 512;
+constexpr int kMergeUnroll = 4;  // runs whose loads are in flight together
+static_assert(kMergeThreads * 4 == kFrag, "one float4 of the fragment order per thread");
+
 __global__ void __launch_bounds__(kMergeThreads)
-decode_merge_kernel(const float* __restrict__ ws_o, const float* __restrict__ ws_ml, int S,
+decode_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NW, int NT,
                     float* __restrict__ out) {
+  __shared__ __align__(16) float so[kFrag];
+  __shared__ int64_t s_g[2];
   pdl_launch_dependents();
-  pdl_wait();
   const int64_t t = blockIdx.x;
-  const int h = threadIdx.x / (kHeadDim / 4), d0 = 4 * (threadIdx.x % (kHeadDim / 4));
-  float M = -INFINITY;
-  for (int sp = 0; sp < S; ++sp) M = fmaxf(M, ws_ml[((t * S + sp) * kHeads + h) * 2]);
-  float l = 0.f;
-  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (M != -INFINITY) {
-    for (int sp = 0; sp < S; ++sp) {
-      const int64_t slot = (t * S + sp) * kHeads + h;
-      const float ms = ws_ml[slot * 2];
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - M);
-      l = fmaf(ws_ml[slot * 2 + 1], w, l);
-      const float4 x = *reinterpret_cast<const float4*>(ws_o + slot * kHeadDim + d0);
-      acc.x = fmaf(x.x, w, acc.x);
-      acc.y = fmaf(x.y, w, acc.y);
-      acc.z = fmaf(x.z, w, acc.z);
-      acc.w = fmaf(x.w, w, acc.w);
+  const int x = threadIdx.x, j = x >> 5, lane = x & 31, h0 = lane >> 2, tig = lane & 3;
+  if (x < 2) {
+    // the warp whose range holds the token's first (x = 0) or last (x = 1) tile:
+    // the last g with begin(g) <= tile
+    const int64_t tile = x == 0 ? t * NT : (t + 1) * NT - 1;
+    int64_t lo = 0, hi = NW - 1;
+    while (lo < hi) {
+      const int64_t mid = (lo + hi + 1) >> 1;
+      if (warp_tile_begin(mid, U, NW) <= tile) lo = mid; else hi = mid - 1;
+    }
+    s_g[x] = lo;
+  }
+  __syncthreads();
+  pdl_wait();
+  const int64_t g0 = s_g[0], g1 = s_g[1];
+  const bool gaps = U < NW;  // only then can a warp's range be empty (no run record)
+  auto live = [&](int64_t gw) {
+    return !gaps || warp_tile_begin(gw, U, NW) != warp_tile_begin(gw + 1, U, NW);
+  };
+  float M0 = -INFINITY, M1 = -INFINITY;
+  for (int64_t gw = g0; gw <= g1; gw += kMergeUnroll) {
+    float a0[kMergeUnroll], a1[kMergeUnroll];
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int64_t g = gw + u;
+      const bool ok = g <= g1 && live(g);
+      const float* rec = ws + (ok ? g + t : g0 + t) * kRecFloats;
+      a0[u] = ok ? rec[kFrag + h0] : -INFINITY;
+      a1[u] = ok ? rec[kFrag + h0 + 8] : -INFINITY;
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      M0 = fmaxf(M0, a0[u]);
+      M1 = fmaxf(M1, a1[u]);
     }
   }
-  float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (l > 0.f) r = make_float4(acc.x / l, acc.y / l, acc.z / l, acc.w / l);
-  *reinterpret_cast<float4*>(out + (t * kHeads + h) * kHeadDim + d0) = r;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  float L0 = 0.f, L1 = 0.f;
+  for (int64_t gw = g0; gw <= g1; gw += kMergeUnroll) {
+    float m0[kMergeUnroll], m1[kMergeUnroll], l0[kMergeUnroll], l1[kMergeUnroll];
+    float4 v[kMergeUnroll];
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      const int64_t g = gw + u;
+      const bool ok = g <= g1 && live(g);
+      const float* rec = ws + (ok ? g + t : g0 + t) * kRecFloats;
+      m0[u] = ok ? rec[kFrag + h0] : -INFINITY;
+      m1[u] = ok ? rec[kFrag + h0 + 8] : -INFINITY;
+      l0[u] = rec[kFrag + kHeads + h0];
+      l1[u] = rec[kFrag + kHeads + h0 + 8];
+      v[u] = reinterpret_cast<const float4*>(rec)[x];
+    }
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      // a run with no valid entry has max -inf, sum 0 and O 0: weight 0
+      const float w0 = (m0[u] == -INFINITY) ? 0.f : exp2f(m0[u] - M0);
+      const float w1 = (m1[u] == -INFINITY) ? 0.f : exp2f(m1[u] - M1);
+      L0 = fmaf(l0[u], w0, L0);
+      L1 = fmaf(l1[u], w1, L1);
+      acc.x = fmaf(v[u].x, w0, acc.x);
+      acc.y = fmaf(v[u].y, w0, acc.y);
+      acc.z = fmaf(v[u].z, w1, acc.z);
+      acc.w = fmaf(v[u].w, w1, acc.w);
+    }
+  }
+  // element c: head h0 + 8 (c >> 1), dim 8 (2 tig + (c & 1) + 8 (j >> 3)) + (j & 7)
+  const int d0 = 8 * (2 * tig + 8 * (j >> 3)) + (j & 7);
+  so[h0 * kHeadDim + d0] = L0 > 0.f ? acc.x / L0 : 0.f;
+  so[h0 * kHeadDim + d0 + 8] = L0 > 0.f ? acc.y / L0 : 0.f;
+  so[(h0 + 8) * kHeadDim + d0] = L1 > 0.f ? acc.z / L1 : 0.f;
+  so[(h0 + 8) * kHeadDim + d0 + 8] = L1 > 0.f ? acc.w / L1 : 0.f;
+  __syncthreads();
+  reinterpret_cast<float4*>(out + t * kFrag)[x] = reinterpret_cast<const float4*>(so)[x];
 }
 
-int decode_splits(int kw) { return (kw + kSplitTokens - 1) / kSplitTokens; }
+// Grid of the split kernel: one CTA per SM, fewer when the warps would get fewer
+// than kMinWarpTiles tiles each (a run's partial record costs a 8 KB write and
+// read, worth it only over a few tiles).
+constexpr int kMinWarpTiles = 4;
+static int64_t decode_grid(int64_t U, int num_sms) {
+  const int64_t want = U / (kDecWarps * kMinWarpTiles);
+  return std::max<int64_t>(1, std::min<int64_t>(want, num_sms > 0 ? num_sms : 1));
+}
 
-size_t decode_workspace_bytes(int64_t T, int kw) {
-  const int64_t S = decode_splits(kw);
-  return (size_t)(T * S * kHeads) * (kHeadDim + 2) * sizeof(float);
+size_t decode_workspace_bytes(int64_t T, int kw, int num_sms) {
+  if (T <= 0 || kw < 1) return 0;
+  const int64_t NT = (kw + kTile - 1) / kTile;
+  const int64_t NW = decode_grid(T * NT, num_sms) * kDecWarps;
+  return (size_t)(NW + T) * kRecFloats * sizeof(float);
 }
 
 cudaError_t launch_decode(const uint16_t* q, int64_t T, int Q, const uint8_t* k_pages,
                           const uint8_t* v_pages, int64_t kv_page_stride, int64_t num_pages,
                           const int32_t* block_table, int64_t bt_width, const int32_t* seq_lens,
                           const int32_t* topk, int kw, float scale, float* out, void* ws,
-                          uint32_t* status, cudaStream_t stream) {
+                          uint32_t* status, int num_sms, cudaStream_t stream) {
   if (T == 0) return cudaSuccess;
-  const int S = decode_splits(kw);
-  if (S > kMaxSplits) return cudaErrorInvalidValue;
-  float* ws_o = static_cast<float*>(ws);
-  float* ws_ml = ws_o + T * S * kFrag;
+  DecodeArgs a;
+  a.q = q;
+  a.k_pages = k_pages;
+  a.v_pages = v_pages;
+  a.kv_page_stride = kv_page_stride;
+  a.num_pages = num_pages;
+  a.block_table = block_table;
+  a.bt_width = bt_width;
+  a.seq_lens = seq_lens;
+  a.topk = topk;
+  a.ws = static_cast<float*>(ws);
+  a.status = status;
+  a.NT = (kw + kTile - 1) / kTile;
+  a.U = T * a.NT;
+  a.kw = kw;
+  a.Q = Q;
+  a.scale = scale;
+  const int64_t G = decode_grid(a.U, num_sms);
   const int smem = (int)sizeof(DecodeSmem);
   cudaError_t err =
       cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (err != cudaSuccess) return err;
-  err = launch_pdl(decode_split_kernel, dim3((unsigned)(T * S)), dim3(kDecThreads), smem, stream,
-                   q, Q, k_pages, v_pages, kv_page_stride, num_pages, block_table, bt_width,
-                   seq_lens, topk, kw, scale, S, ws_o, ws_ml, status);
+  err = launch_pdl(decode_split_kernel, dim3((unsigned)G), dim3(kDecThreads), smem, stream, a);
   if (err != cudaSuccess) return err;
   return launch_pdl(decode_merge_kernel, dim3((unsigned)T), dim3(kMergeThreads), 0, stream,
-                    (const float*)ws_o, (const float*)ws_ml, S, out);
+                    (const float*)a.ws, a.U, G * kDecWarps, a.NT, out);
 }
 
 }  // namespace mx4

@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <mutex>
 
 #include "common.cuh"
@@ -30,8 +31,8 @@ cudaError_t launch_norm_rope_insert(const float*, const float*, const float*, co
                                     uint16_t*, uint32_t*, cudaStream_t);
 cudaError_t launch_decode(const uint16_t*, int64_t, int, const uint8_t*, const uint8_t*, int64_t,
                           int64_t, const int32_t*, int64_t, const int32_t*, const int32_t*, int,
-                          float, float*, void*, uint32_t*, cudaStream_t);
-size_t decode_workspace_bytes(int64_t, int);
+                          float, float*, void*, uint32_t*, int, cudaStream_t);
+size_t decode_workspace_bytes(int64_t, int, int);
 cudaError_t launch_fp8_index_insert(const float*, int64_t, const int64_t*, float, uint8_t*,
                                     int64_t, int64_t, uint32_t*, cudaStream_t);
 cudaError_t launch_index_score_fp8(const uint16_t*, int, const uint8_t*, int64_t, int64_t,
@@ -93,11 +94,55 @@ int device_info(DeviceInfo** out) {
   return MX4_OK;
 }
 
+// SM count of the current device, for sizes that depend on the grid; a large
+// count (so a size on the safe side) when the device cannot be queried.
+int current_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    return 1024;
+  return n;
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int cuda_result(cudaError_t e, const char* what) {
   if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "%s launch: %s", what, cudaGetErrorString(e));
   return ok();
+}
+
+
+// Argument checks of sparse_paged_decode, shared by its allocation-free variant
+// and by the whole-step call (the same rules, the caller's name in the reason):
+// first the sizes and the geometry, then (after the caller's workspace check)
+// the pointers.
+int check_decode_sizes(const char* name, int64_t T, int q_per_seq, int H, int Hkv, int64_t B,
+                       int k, float scale) {
+  if (H != 16 || Hkv != 1)
+    return fail(MX4_ERR_UNSUPPORTED,
+                "%s: H = %d, Hkv = %d (supported: 16 query heads, 1 KV head)", name, H, Hkv);
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: q_per_seq = %d", name, q_per_seq);
+  if (k < 1 || k > 65536) return fail(MX4_ERR_UNSUPPORTED, "%s: k = %d", name, k);
+  if (B < 0 || T != B * q_per_seq) return fail(MX4_ERR_INVALID, "%s: T != B * q_per_seq", name);
+  if (T > 0x7FFFFFFF / 8) return fail(MX4_ERR_UNSUPPORTED, "%s: T = %lld too large", name, (long long)T);
+  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
+    return fail(MX4_ERR_INVALID, "%s: scale is not finite", name);
+  return MX4_OK;
+}
+
+int check_decode_pointers(const char* name, const uint16_t* q, const uint8_t* k_pages,
+                          const uint8_t* v_pages, int64_t kv_page_stride, int64_t kv_head_stride,
+                          int64_t num_pages, const int32_t* block_table, int64_t bt_width,
+                          const int32_t* seq_lens, const int32_t* topk_idx, const float* out) {
+  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !topk_idx || !out)
+    return fail(MX4_ERR_INVALID, "%s: NULL pointer", name);
+  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
+      kv_page_stride % 16 || kv_head_stride % 16)
+    return fail(MX4_ERR_INVALID, "%s: misaligned buffer or stride", name);
+  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || bt_width < 1)
+    return fail(MX4_ERR_INVALID, "%s: num_pages, page stride or bt_width", name);
+  return MX4_OK;
 }
 
 }  // namespace
@@ -291,7 +336,7 @@ int topk_select(const float* scores, int64_t ld_scores, const int32_t* seq_lens,
 
 size_t sparse_paged_decode_workspace(int64_t T, int k) {
   if (T < 0 || k < 1) return 0;
-  return mx4::decode_workspace_bytes(T, k);
+  return mx4::decode_workspace_bytes(T, k, current_sms());
 }
 
 int sparse_paged_decode(const uint16_t* q, int64_t T, int q_per_seq, int H, int Hkv,
@@ -300,36 +345,23 @@ int sparse_paged_decode(const uint16_t* q, int64_t T, int q_per_seq, int H, int 
                         int64_t B, int64_t bt_width, const int32_t* seq_lens,
                         const int32_t* topk_idx, int k, float scale, float* out, void* ws,
                         size_t ws_bytes, void* stream) {
-  if (H != 16 || Hkv != 1)
-    return fail(MX4_ERR_UNSUPPORTED,
-                "sparse_paged_decode: H = %d, Hkv = %d (supported: 16 query heads, 1 KV head)",
-                H, Hkv);
-  if (q_per_seq < 1 || q_per_seq > 8)
-    return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode: q_per_seq = %d", q_per_seq);
-  if (k < 1 || k > 65536) return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode: k = %d", k);
-  if (B < 0 || T != B * q_per_seq)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode: T != B * q_per_seq");
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode: scale is not finite");
+  static const char* kName = "sparse_paged_decode";
+  if (int rc = check_decode_sizes(kName, T, q_per_seq, H, Hkv, B, k, scale)) return rc;
   if (ws_bytes < sparse_paged_decode_workspace(T, k))
-    return fail(MX4_ERR_WORKSPACE, "sparse_paged_decode: workspace %zu < %zu bytes", ws_bytes,
+    return fail(MX4_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", kName, ws_bytes,
                 sparse_paged_decode_workspace(T, k));
   if (T == 0) return ok();
-  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !topk_idx || !out || !ws)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode: NULL pointer");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(ws, 16) || !aligned(k_pages, 16) ||
-      !aligned(v_pages, 16) || kv_page_stride % 16 || kv_head_stride % 16)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode: misaligned buffer or stride");
-  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || bt_width < 1)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode: num_pages, page stride or bt_width");
-  (void)kv_head_stride;  // one KV head: head 0 sits at the page base
+  if (int rc = check_decode_pointers(kName, q, k_pages, v_pages, kv_page_stride, kv_head_stride,
+                                     num_pages, block_table, bt_width, seq_lens, topk_idx, out))
+    return rc;
+  if (!ws || !aligned(ws, 16)) return fail(MX4_ERR_INVALID, "%s: workspace NULL or misaligned", kName);
   DeviceInfo* d;
   if (int rc = device_info(&d)) return rc;
   return cuda_result(mx4::launch_decode(q, T, q_per_seq, k_pages, v_pages, kv_page_stride,
                                         num_pages, block_table, bt_width, seq_lens, topk_idx, k,
-                                        scale, out, ws, d->status,
+                                        scale, out, ws, d->status, d->num_sms,
                                         static_cast<cudaStream_t>(stream)),
-                     "sparse_paged_decode");
+                     kName);
 }
 
 int mx4_check_status(void* stream, uint32_t* bits) {
@@ -404,39 +436,124 @@ extern "C" int sparse_paged_decode_noalloc(
     const uint8_t* v_pages, int64_t kv_page_stride, int64_t kv_head_stride, int64_t num_pages,
     const int32_t* block_table, int64_t B, int64_t bt_width, const int32_t* seq_lens,
     const int32_t* topk_idx, int k, float scale, float* out, void* stream) {
-  if (H != 16 || Hkv != 1)
-    return fail(MX4_ERR_UNSUPPORTED,
-                "sparse_paged_decode_noalloc: H = %d, Hkv = %d (16 query heads, 1 KV head)", H,
-                Hkv);
-  if (q_per_seq < 1 || q_per_seq > 8)
-    return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode_noalloc: q_per_seq = %d", q_per_seq);
-  if (k < 1 || k > 65536)
-    return fail(MX4_ERR_UNSUPPORTED, "sparse_paged_decode_noalloc: k = %d", k);
-  if (B < 0 || T != B * q_per_seq)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: T != B * q_per_seq");
-  if (!(scale == scale) || scale == INFINITY || scale == -INFINITY)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: scale is not finite");
-  const size_t need = mx4::decode_workspace_bytes(T, k);
+  static const char* kName = "sparse_paged_decode_noalloc";
+  if (int rc = check_decode_sizes(kName, T, q_per_seq, H, Hkv, B, k, scale)) return rc;
+  const size_t need = sparse_paged_decode_workspace(T, k);
   if (need > (size_t)MX4_NOALLOC_SCRATCH_BYTES)
     return fail(MX4_ERR_WORKSPACE,
-                "sparse_paged_decode_noalloc: T = %lld, k = %d needs %zu bytes of scratch, more "
-                "than the library's fixed %zu; use sparse_paged_decode with a caller workspace",
-                (long long)T, k, need, (size_t)MX4_NOALLOC_SCRATCH_BYTES);
+                "%s: T = %lld, k = %d needs %zu bytes of scratch, more than the library's "
+                "fixed %zu; use sparse_paged_decode with a caller workspace",
+                kName, (long long)T, k, need, (size_t)MX4_NOALLOC_SCRATCH_BYTES);
   if (T == 0) return ok();
-  if (!q || !k_pages || !v_pages || !block_table || !seq_lens || !topk_idx || !out)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: NULL pointer");
-  if (!aligned(q, 16) || !aligned(out, 16) || !aligned(k_pages, 16) || !aligned(v_pages, 16) ||
-      kv_page_stride % 16 || kv_head_stride % 16)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: misaligned buffer or stride");
-  if (num_pages < 1 || kv_page_stride < mx4::kPageBytes || bt_width < 1)
-    return fail(MX4_ERR_INVALID, "sparse_paged_decode_noalloc: num_pages, page stride or bt_width");
+  if (int rc = check_decode_pointers(kName, q, k_pages, v_pages, kv_page_stride, kv_head_stride,
+                                     num_pages, block_table, bt_width, seq_lens, topk_idx, out))
+    return rc;
   DeviceInfo* d;
   if (int rc = device_info(&d)) return rc;
   void* scratch = nullptr;
   if (int rc = noalloc_scratch(&scratch)) return rc;
   return cuda_result(mx4::launch_decode(q, T, q_per_seq, k_pages, v_pages, kv_page_stride,
                                         num_pages, block_table, bt_width, seq_lens, topk_idx, k,
-                                        scale, out, scratch, d->status,
+                                        scale, out, scratch, d->status, d->num_sms,
                                         static_cast<cudaStream_t>(stream)),
-                     "sparse_paged_decode_noalloc");
+                     kName);
+}
+
+// ---------------------------------------------------------------------------
+// mx4_decode_step: one decode step from host memory to host memory.
+
+namespace {
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+}  // namespace
+
+extern "C" void mx4_decode_step_input_offsets(int64_t T, int64_t n_new, size_t offsets[6]) {
+  const size_t T_ = T > 0 ? (size_t)T : 0, n_ = n_new > 0 ? (size_t)n_new : 0;
+  const size_t sizes[6] = {T_ * 16 * mx4::kHeadDim * 2, T_ * mx4::kHeadDim * 2,
+                           n_ * mx4::kHeadDim * 4,      n_ * mx4::kHeadDim * 4,
+                           n_ * mx4::kHeadDim * 4,      n_ * 8};
+  size_t off = 0;
+  for (int i = 0; i < 6; ++i) {
+    offsets[i] = off;
+    off += align256(sizes[i]);
+  }
+}
+
+extern "C" size_t mx4_decode_step_input_bytes(int64_t T, int64_t n_new) {
+  size_t off[6];
+  mx4_decode_step_input_offsets(T, n_new, off);
+  const size_t n_ = n_new > 0 ? (size_t)n_new : 0;
+  return std::max<size_t>(256, off[5] + align256(n_ * 8));
+}
+
+extern "C" int mx4_decode_step(const void* h_inputs, int64_t n_new, void* d_staging,
+                               size_t staging_bytes, uint8_t* k_pages, uint8_t* v_pages,
+                               int64_t kv_page_stride, int64_t kv_head_stride,
+                               uint8_t* idx_pages, int64_t idx_page_stride, int64_t num_pages,
+                               const int32_t* block_table, int64_t B, int64_t bt_width,
+                               const int32_t* seq_lens, int q_per_seq, int k, float scale,
+                               float* d_scores, int64_t ld_scores, int32_t* d_topk_idx,
+                               void* topk_ws, size_t topk_ws_bytes, void* dec_ws,
+                               size_t dec_ws_bytes, float* d_out, float* h_out, void* stream) {
+  static const char* kName = "mx4_decode_step";
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: q_per_seq = %d", kName, q_per_seq);
+  if (B < 0 || B > 65535) return fail(MX4_ERR_UNSUPPORTED, "%s: B = %lld", kName, (long long)B);
+  if (n_new < 0) return fail(MX4_ERR_INVALID, "%s: n_new < 0", kName);
+  const int64_t T = B * q_per_seq;
+  const size_t in_bytes = mx4_decode_step_input_bytes(T, n_new);
+  if (T == 0 && n_new == 0) return ok();
+  if (!h_inputs || !d_staging || !h_out) return fail(MX4_ERR_INVALID, "%s: NULL pointer", kName);
+  if (staging_bytes < in_bytes)
+    return fail(MX4_ERR_WORKSPACE, "%s: staging %zu < %zu bytes", kName, staging_bytes, in_bytes);
+  if (!aligned(d_staging, 256))
+    return fail(MX4_ERR_INVALID, "%s: staging buffer must be 256-byte aligned", kName);
+  size_t off[6];
+  mx4_decode_step_input_offsets(T, n_new, off);
+  uint8_t* st = static_cast<uint8_t*>(d_staging);
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(st + off[0]);
+  const uint16_t* iq = reinterpret_cast<const uint16_t*>(st + off[1]);
+  const float* k_new = reinterpret_cast<const float*>(st + off[2]);
+  const float* v_new = reinterpret_cast<const float*>(st + off[3]);
+  const float* idx_new = reinterpret_cast<const float*>(st + off[4]);
+  const int64_t* slots = reinterpret_cast<const int64_t*>(st + off[5]);
+  // validate every stage before anything is enqueued
+  if (int rc = check_decode_sizes(kName, T, q_per_seq, 16, 1, B, k, scale)) return rc;
+  if (T > 0)
+    if (int rc = check_decode_pointers(kName, q, k_pages, v_pages, kv_page_stride,
+                                       kv_head_stride, num_pages, block_table, bt_width,
+                                       seq_lens, d_topk_idx, d_out))
+      return rc;
+  if (T > 65535 || (ld_scores + 16383) / 16384 > 512)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: T = %lld or ld_scores = %lld beyond topk_select's limits",
+                kName, (long long)T, (long long)ld_scores);
+  if (!idx_pages || !d_scores || idx_page_stride % 16 || !aligned(idx_pages, 16) ||
+      idx_page_stride < mx4::kPageBytes || ld_scores < 1)
+    return fail(MX4_ERR_INVALID, "%s: index pages, page stride or scores", kName);
+  if (topk_ws_bytes < topk_select_workspace(T, k, ld_scores) ||
+      dec_ws_bytes < sparse_paged_decode_workspace(T, k))
+    return fail(MX4_ERR_WORKSPACE, "%s: a workspace is too small", kName);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemcpyAsync(d_staging, h_inputs, in_bytes, cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "%s: input copy: %s", kName, cudaGetErrorString(e));
+  if (n_new > 0) {
+    if (int rc = mx4_insert(k_new, v_new, idx_new, n_new, 1, slots, k_pages, v_pages,
+                            kv_page_stride, kv_head_stride, idx_pages, idx_page_stride,
+                            num_pages, stream))
+      return rc;
+  }
+  if (int rc = index_score(iq, T, q_per_seq, idx_pages, idx_page_stride, num_pages, block_table,
+                           B, bt_width, seq_lens, d_scores, ld_scores, stream))
+    return rc;
+  if (int rc = topk_select(d_scores, ld_scores, seq_lens, B, q_per_seq, k, d_topk_idx, topk_ws,
+                           topk_ws_bytes, stream))
+    return rc;
+  if (int rc = sparse_paged_decode(q, T, q_per_seq, 16, 1, k_pages, v_pages, kv_page_stride,
+                                   kv_head_stride, num_pages, block_table, B, bt_width, seq_lens,
+                                   d_topk_idx, k, scale, d_out, dec_ws, dec_ws_bytes, stream))
+    return rc;
+  e = cudaMemcpyAsync(h_out, d_out, (size_t)T * 16 * mx4::kHeadDim * sizeof(float),
+                      cudaMemcpyDeviceToHost, s);
+  if (e != cudaSuccess)
+    return fail(MX4_ERR_CUDA, "%s: output copy: %s", kName, cudaGetErrorString(e));
+  return ok();
 }

@@ -19,7 +19,8 @@ import math
 import numpy as np
 import torch
 
-from . import (FP8_PAGE_BYTES, fp8_index_insert, index_score, mx4_insert, sparse_paged_decode,
+from . import (FP8_PAGE_BYTES, fp8_index_insert, index_score, mx4_decode_step,
+               mx4_decode_step_input_layout, mx4_insert, sparse_paged_decode,
                sparse_paged_decode_workspace, topk_select, topk_select_workspace)
 from . import workloads as W
 
@@ -121,6 +122,10 @@ class DecodeStep:
             ("v", (n_ins, 1, W.HEAD_DIM), torch.float32),
             ("idx_k", (n_ins, W.HEAD_DIM), torch.float32),
             ("slots", (n_ins,), torch.int64)])
+        offs, nbytes = mx4_decode_step_input_layout(T, n_ins)
+        assert nbytes == self.input_layout["bytes"] and offs == [
+            self.input_layout[n][0] for n in ("q", "iq", "k", "v", "idx_k", "slots")], \
+            "packed input layout differs from the C step entry's"
         self.inputs = torch.empty(self.input_layout["bytes"], dtype=torch.uint8, device=device)
         views = _views(self.inputs, self.input_layout)
         self.q, self.iq = views["q"], views["iq"]
@@ -216,6 +221,17 @@ class DecodeStep:
         timed("sparse_paged_decode", lambda: sparse_paged_decode(
             self.q, wl.q, c.k_pages, c.v_pages, self.block_table, self.seq_lens, self.topk_idx,
             self.scale, self.out, self.dec_ws, stream=stream))
+
+    def run_host(self, h_inputs: torch.Tensor, h_out: torch.Tensor, stream=None):
+        """The whole step from host memory to host memory through the C entry point
+        mx4_decode_step: the packed host inputs (pack_inputs; the same layout as the
+        device input buffer) are copied in, the four stages run, and the output is
+        copied into the host tensor h_out [T, 16, 128] fp32.  Asynchronous."""
+        wl, c = self.wl, self.caches
+        mx4_decode_step(h_inputs, self.slots.numel(), self.inputs, c.k_pages, c.v_pages,
+                        c.idx_pages, self.block_table, self.seq_lens, wl.q, wl.k, self.scale,
+                        self.scores, self.topk_idx, self.topk_ws, self.dec_ws, self.out, h_out,
+                        stream=stream)
 
     def launches_per_step(self) -> int:
         """Kernels this library launches per step: insert, score, top-k (threshold and

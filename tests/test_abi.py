@@ -90,11 +90,22 @@ def test_host_validation_without_gpu(lib):
                                  None) == -1
 
 
+def _decode_ws(T, k, sms):
+    # one partial record (16 heads x 128 outputs, then 16 maxima and 16 sums, fp32)
+    # per (warp, token) run: at most one per warp plus one per token, with one CTA of
+    # 8 warps per SM, fewer CTAs when the warps would get fewer than 4 tiles of 16
+    # entries each
+    tiles = T * ((k + 15) // 16)
+    warps = 8 * max(1, min(sms, tiles // 32))
+    return (warps + T) * (16 * 128 + 32) * 4
+
+
 def test_workspace_sizes(lib):
     import mxfp4_sparse_paged_gb300 as m
-    # 16 heads x (128 outputs + max + sum) fp32 per (token, split of 512 selected)
-    assert m.sparse_paged_decode_workspace(64, 2048) == 64 * 4 * 16 * 130 * 4
-    assert m.sparse_paged_decode_workspace(1, 1) == 16 * 130 * 4
+    # without a GPU the SM count cannot be read: the size assumes 1024 SMs (a bound)
+    assert m.sparse_paged_decode_workspace(64, 2048) == _decode_ws(64, 2048, 1024)
+    assert m.sparse_paged_decode_workspace(1, 1) == _decode_ws(1, 1, 1024) == 9 * 8320
+    assert m.sparse_paged_decode_workspace(0, 2048) == 0
     # count [T] | threshold [T] | (offset, count) per 16384-score segment | kCand = 8192
     # keys and indices, each section padded to 16 bytes
     assert m.topk_select_workspace(64, 2048, 131072) == 2 * 64 * 4 + 64 * 8 * 8 + 2 * 64 * 8192 * 4
@@ -185,3 +196,28 @@ def test_bindings_refuse_inconsistent_shapes(lib, bad):
     with pytest.raises(ValueError) as ei:
         _calls(a, m)[call]()
     assert "CUDA tensor" not in str(ei.value), str(ei.value)
+
+
+def test_decode_step_host_validation_and_layout(lib):
+    # The whole-step call refuses NULL buffers and a short staging buffer before it
+    # enqueues anything; its packed input layout is q | iq | k | v | idx_k | slots,
+    # each section 256-byte aligned.
+    import mxfp4_sparse_paged_gb300 as m
+    L = m._load()
+    offs, nbytes = m.mx4_decode_step_input_layout(256, 256)
+    sizes = [256 * 16 * 128 * 2, 256 * 128 * 2, 256 * 512, 256 * 512, 256 * 512, 256 * 8]
+    want, o = [], 0
+    for sz in sizes:
+        want.append(o)
+        o += (sz + 255) // 256 * 256
+    assert offs == want and nbytes == o
+    assert m.mx4_decode_step_input_layout(4, 0)[0][2:] == [4 * 16 * 128 * 2 + 1024] * 4
+    f = ctypes.c_float(0.1)
+    args = [None, 0, None, 0, None, None, 8704, 8704, None, 8704, 1, None, 2, 1, None, 1, 16, f,
+            None, 64, None, None, 0, None, 0, None, None, None]
+    assert L.mx4_decode_step(*args) == -1 and "NULL" in _err(m)
+    buf = ctypes.create_string_buffer(64)
+    args[0] = args[26] = ctypes.cast(buf, ctypes.c_void_p)
+    args[2] = ctypes.c_void_p(4096)
+    args[3] = 16  # staging far below the packed inputs
+    assert L.mx4_decode_step(*args) == -3 and "staging" in _err(m)

@@ -88,20 +88,22 @@ def test_config1_full():
 def test_config2_sampled():
     wl = W.make(2)
     L = wl.seq_lens
-    seqs = sorted({int(np.argmin(L)), int(np.argmax(L)), 7, 33})
+    seqs = sorted({int(np.argmin(L)), int(np.argmax(L)), 3, 7, 19, 33, 45, 58, 63})
+    assert len(seqs) >= 8
     _compare(wl, seqs, *_gpu_step(wl))
 
 
 def test_config3_sampled_multi_token():
     wl = W.make(3)
-    _compare(wl, [0, 15], *_gpu_step(wl))
+    _compare(wl, [0, 2, 4, 6, 9, 11, 13, 15], *_gpu_step(wl))  # 8 of 16 sequences, 32 tokens
 
 
 def test_config4_sampled_with_insert():
     wl = W.make(4)
     L = wl.seq_lens
     short = int(np.nonzero(L < 2048)[0][0])
-    seqs = sorted({short, int(np.argmax(L)), int(np.argmin(L)), 5, 100, 250})
+    seqs = sorted({short, int(np.argmax(L)), int(np.argmin(L)), 5, 30, 60, 100, 150, 200, 250})
+    assert len(seqs) >= 8
     _compare(wl, seqs, *_gpu_step(wl))
 
 
@@ -323,6 +325,85 @@ def test_topk_segment_filter_paths():
             assert np.array_equal(out.cpu().numpy(), want), f"k={k} ld={ld}"
 
 
+def _sample_rank(n, k, kcand=8192, ksample=2048):
+    """The selection kernel's documented threshold rank for a row of n > kcand scores:
+    the sample key at rank m + 4 sqrt(m) + 8 (m = k * ksample / n), lowered to
+    2r + 64 when the candidates fall short.  Used only to build rows that reach each
+    branch; the expected selection always comes from the oracle."""
+    m_ = k * ksample / n
+    r0 = min(ksample - 1, int(m_ + 4.0 * math.sqrt(m_)) + 8)
+    ranks = [r0]
+    while ranks[-1] < ksample - 1:
+        ranks.append(min(ksample - 1, 2 * ranks[-1] + 64))
+    return ranks
+
+
+def _retry_row(n, k, level, rng, kcand=8192):
+    """A row of n scores whose evenly spaced 2048-key sample (positions j*n//2048) is
+    1000 - j, so the threshold at sample rank r is 1000 - r, and whose other keys sit
+    near -2000.  `level` = how many threshold reductions the selection needs: the keys
+    put between the thresholds of levels `level` - 1 and `level` make up the
+    candidates only from that level on.
+    level -1: 1800 sample keys are 100 and 248 are -5000, so the reductions fall
+    short until the threshold drops to -5000 and the candidates exceed the capacity.
+    level -2: every sample key is 100 (k > 2048), so the reductions run out of sample
+    ranks and the threshold is dropped altogether."""
+    row = (rng.standard_normal(n) - 2000.0).astype(np.float32)
+    pos = (np.arange(2048, dtype=np.int64) * n) // 2048
+    rest = np.setdiff1d(np.arange(n), pos)
+    if level == -1:
+        row[pos] = np.where(np.arange(2048) < 1800, 100.0, -5000.0).astype(np.float32)
+        return row
+    if level == -2:
+        assert k > 2048
+        row[pos] = 100.0
+        return row
+    ranks = _sample_rank(n, k, kcand)
+    hi = 1000.0 - ranks[level - 1]          # threshold of the level before: must fall short
+    lo = 1000.0 - ranks[level]              # threshold of this level
+    row[pos] = 1000.0 - np.arange(2048, dtype=np.float32)
+    target = min(kcand, k + 500)
+    need = target - (ranks[level] + 1)       # sample keys >= lo: ranks[level] + 1
+    pick = rng.choice(rest, size=need, replace=False)
+    row[pick] = rng.uniform(lo + 0.01, hi - 0.01, need).astype(np.float32)
+    return row
+
+
+@pytest.mark.parametrize("k", [2048, 8192])
+def test_topk_threshold_retry_paths(k):
+    # Rows on which the sampled threshold leaves fewer than k candidates, so the
+    # selection lowers it once (level 1) or twice (level 2) before the candidates
+    # fit, runs out of sample ranks and takes the exact path (level -1), or gets
+    # more than the candidate capacity at once (the sample all below the rest).
+    # Bit-exact against the oracle on the same fp32 scores; no status bits.
+    rng = np.random.default_rng(2024 + k)
+    n_rows = [131072, 131072, 65536, 40000, 131072, 9000]
+    levels = [1, 2, 1, 2, -1, 1]
+    if k == 8192:
+        n_rows, levels = [131072, 131072, 65536, 131072, 131072], [1, 2, 1, -1, -2]
+    rows = [_retry_row(n, k, lev, rng) for n, lev in zip(n_rows, levels)]
+    # sample far below the rest: threshold takes the whole row (> capacity)
+    n_low = 100000
+    low = rng.standard_normal(n_low).astype(np.float32)
+    low[(np.arange(2048, dtype=np.int64) * n_low) // 2048] = -100.0
+    rows.append(low)
+    lens = np.array([len(r) for r in rows], np.int32)
+    ld = int(lens.max())
+    sc = np.full((len(rows), ld), -np.inf, np.float32)
+    for t, r in enumerate(rows):
+        sc[t, :len(r)] = r
+    want = oracle.topk_select(sc.astype(np.float64), lens, 1, k)
+    out = torch.empty((len(rows), k), dtype=torch.int32, device=DEV)
+    ws_n = m.topk_select_workspace(len(rows), k, ld)
+    assert ws_n > 0  # the rows take the segment filter first
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=DEV)
+    m.topk_select(torch.from_numpy(sc).to(DEV), torch.from_numpy(lens).to(DEV), 1, k, out, ws)
+    assert m.mx4_check_status() == 0
+    got = out.cpu().numpy()
+    for t in range(len(rows)):
+        assert np.array_equal(got[t], want[t]), f"row {t} (n={lens[t]}, k={k})"
+
+
 @pytest.mark.parametrize("wid", [1, 4])
 def test_pipelined_steps_match_a_plain_step(wid):
     # The overlapped serving loop (packed inputs, one CUDA-graph launch a step)
@@ -339,6 +420,23 @@ def test_pipelined_steps_match_a_plain_step(wid):
     outs = [pipe.submit(pin) for _ in range(4)]
     torch.cuda.synchronize()
     for h_out, _ in outs[-2:]:
+        assert np.array_equal(h_out.numpy(), want)
+    m.mx4_check_status()
+
+
+@pytest.mark.parametrize("wid", [0, 4])
+def test_host_to_host_step_matches_a_plain_step(wid):
+    # mx4_decode_step (host inputs -> device -> the four stages -> host output, one C
+    # call) gives the plain step's output, call after call.
+    wl = W.make(wid)
+    caches, step, host = _gpu_step(wl)
+    want = step.out.cpu().numpy()
+    pin = step.pack_inputs(host)
+    h_out = torch.full(tuple(step.out.shape), float("nan"), dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        h_out.fill_(float("nan"))
+        step.run_host(pin, h_out)
+        torch.cuda.current_stream().synchronize()
         assert np.array_equal(h_out.numpy(), want)
     m.mx4_check_status()
 

@@ -1,7 +1,7 @@
 """sparse_paged_decode_noalloc: the decode entry point for callers that cannot
 allocate device memory (a host framework that owns all device memory and hands
 an extension only the operation's inputs and outputs, or a C or
-foreign-language runtime with no device allocator).  It keeps the split
+foreign-language runtime with no device allocator).  It keeps the run
 workspace in the library's own fixed device array instead of a caller buffer.
 
 Checked through the C ABI against sparse_paged_decode (caller workspace) on the
@@ -43,8 +43,9 @@ def test_noalloc_matches_workspace_entry_point_twice():
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch():
-    # T * splits * 16 heads * 130 floats above 32 MiB: refused before any launch
-    T, k = 1024, 2048
+    # (8 warps per SM + T) partial records of 8320 bytes above 32 MiB: refused before
+    # any launch
+    T, k = 4096, 16
     assert m.sparse_paged_decode_workspace(T, k) > m.NOALLOC_SCRATCH_BYTES
     q = torch.zeros((T, 16, 128), dtype=torch.bfloat16, device="cuda")
     pages = torch.zeros((1, 1, 8704), dtype=torch.uint8, device="cuda")
