@@ -298,7 +298,8 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
     torch.cuda.synchronize()
     ab = W.algorithmic_bytes(wl)
     names = (["mx4_insert"] if wl.spec.insert_in_step else []) + \
-        ["index_score", "topk_select", "sparse_paged_decode"]
+        ["index_topk", "sparse_paged_decode"]
+    split_names = ["index_score", "topk_select"]
     # The in-step insert rewrites the decode tokens' rows with the same values, so
     # every timed step does identical work.
     step.load_inputs(host)
@@ -349,13 +350,18 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
     # Per-kernel times: the same steps again with an event pair around each entry
     # point.  Events between kernels serialise them (no kernel starts under the
     # previous one), so this pass is kept out of the step timing above.
-    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names}
+    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names + split_names}
     for i in range(args.steps):
         flush_l2(i & 0xFF)
         step.run(stream=stream, events={n: per[n][i] for n in names})
+    # the same steps with the scorer and the selection as separate calls: the
+    # scorer's own time (for its roofline) and the pair the fused call replaces
+    for i in range(args.steps):
+        flush_l2(i & 0xFF)
+        step.run(stream=stream, events={n: per[n][i] for n in split_names}, fused=False)
     torch.cuda.synchronize()
     m.mx4_check_status()
-    kern_ms = {n: statistics.mean(_event_ms(per[n])) for n in names}
+    kern_ms = {n: statistics.mean(_event_ms(per[n])) for n in names + split_names}
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     value = job_value(wl.T, world, args.steps, total_ms)
 
@@ -389,7 +395,9 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
     hot = ab["index_score"] + ab["sparse_paged_decode"]
     hot_gbs = hot / ((sc_ms + dec_ms) / 1e3) / 1e9
     r_score = _roof("index_score", ab["index_score"], sc_ms, peak,
-                    _ncu_traffic(wl.spec.name, "index_score_traffic.json"))
+                    _ncu_traffic(wl.spec.name, "index_score_traffic.json"),
+                    {"timing": "the scorer alone (index_score call); inside the step it runs "
+                               "in index_topk with its key histograms"})
     r_dec = _roof("sparse_paged_decode (run kernel + merge kernel)", ab["sparse_paged_decode"],
                   dec_ms, peak, _ncu_traffic(wl.spec.name, "decode_split_traffic.json"),
                   {"traffic_kernel": "decode_split_kernel"})
@@ -397,13 +405,20 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
         "value": round(value, 1), "unit": UNIT, "ms_per_step": round(total_ms / args.steps, 4),
         "decode_tokens": wl.T, "cached_tokens": int(wl.seq_lens.astype(np.int64).sum()),
         "kernel_ms": {n: round(v, 5) for n, v in kern_ms.items()},
-        "kernel_ms_timing": "a second pass with a CUDA-event pair around each entry point; "
-                            "the events serialise the kernels",
+        "kernel_ms_timing": "a second pass with a CUDA-event pair around each entry point "
+                            "(the events serialise the kernels); index_score and topk_select "
+                            "from a third pass with the two as separate calls, which the step's "
+                            "index_topk replaces",
         "roofline_index_score": r_score, "roofline_decode": r_dec,
         "hot_path_hbm": {"kernels": "index_score + sparse_paged_decode",
                          "algorithmic_bytes": int(hot), "achieved_gbs": round(hot_gbs, 1),
                          "frac": round(hot_gbs / peak, 4),
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)"},
+        "hot_path_hbm_with_topk": {
+            "kernels": "index_topk (scorer + selection) + sparse_paged_decode",
+            "algorithmic_bytes": int(hot),
+            "achieved_gbs": round(hot / ((kern_ms["index_topk"] + dec_ms) / 1e3) / 1e9, 1),
+            "frac": round(hot / ((kern_ms["index_topk"] + dec_ms) / 1e3) / 1e9 / peak, 4)},
         "e2e": e2e, "clocks": ck, "soak_steps": soak_steps,
         "gpu_launches": step.launches_per_step() * args.steps,
         "wall_s_timed_region": round(wall, 4),
@@ -479,6 +494,7 @@ def run_gpu(args):
         "roofline_index_score": head_blk["roofline_index_score"],
         "roofline_decode": head_blk["roofline_decode"],
         "hot_path_hbm": head_blk["hot_path_hbm"],
+        "hot_path_hbm_with_topk": head_blk["hot_path_hbm_with_topk"],
         "kernel_ms": head_blk["kernel_ms"], "kernel_ms_timing": head_blk["kernel_ms_timing"],
         "step_launch": ("separate API calls" if args.eager else
                         "one CUDA-graph launch of the step's kernels (captured from the API calls)"),

@@ -18,7 +18,8 @@ import threading
 
 import torch
 
-__all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score", "topk_select", "sparse_paged_decode",
+__all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score",
+           "index_topk", "index_topk_workspace", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
            "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "mx4_decode_step",
            "mx4_decode_step_input_layout",
@@ -79,6 +80,11 @@ def _load():
                                         P, i64, P]
         lib.index_score.restype = i32
         lib.index_score.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, P]
+        lib.index_topk.restype = i32
+        lib.index_topk.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, i32, P, P,
+                                   sz, P]
+        lib.index_topk_workspace.restype = sz
+        lib.index_topk_workspace.argtypes = [i64, i32, i64]
         lib.topk_select.restype = i32
         lib.topk_select.argtypes = [P, i64, P, i64, i32, i32, P, P, sz, P]
         lib.topk_select_workspace.restype = sz
@@ -288,6 +294,39 @@ def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=
                                idx_pages.stride(0), int(idx_pages.shape[0]), _ptr(block_table), B,
                                int(block_table.shape[1]), _ptr(seq_lens), _ptr(scores),
                                scores.stride(0), _stream(stream)))
+
+
+def index_topk_workspace(T, k, ld_scores) -> int:
+    return int(_load().index_topk_workspace(int(T), int(k), int(ld_scores)))
+
+
+def index_topk(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, k, topk_idx, ws,
+               stream=None):
+    """index_score then topk_select in one call: scores (fp32 [T, ld]) and
+    topk_idx (int32 [T, k]); ws is a uint8 workspace of index_topk_workspace(T, k, ld)
+    bytes (None when that is 0)."""
+    _need(iq, torch.bfloat16, "iq")
+    _need(block_table, torch.int32, "block_table")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(scores, torch.float32, "scores")
+    _need(topk_idx, torch.int32, "topk_idx")
+    _pages(idx_pages, "idx_pages", 2)
+    _dims(seq_lens, "seq_lens", None)
+    B = int(seq_lens.shape[0])
+    T = B * int(q_per_seq)
+    _dims(iq, "iq", T, HEAD_DIM)
+    _dims(block_table, "block_table", None, None)
+    _rows_at_least(block_table, B, "block_table")
+    _dims(scores, "scores", None, None)
+    _rows_at_least(scores, T, "scores")
+    _dims(topk_idx, "topk_idx", None, int(k))
+    _rows_at_least(topk_idx, T, "topk_idx")
+    _check(_load().index_topk(_ptr(iq), T, int(q_per_seq), _ptr(idx_pages), idx_pages.stride(0),
+                              int(idx_pages.shape[0]), _ptr(block_table), B,
+                              int(block_table.shape[1]), _ptr(seq_lens), _ptr(scores),
+                              scores.stride(0), int(k), _ptr(topk_idx), _ptr(ws),
+                              0 if ws is None else ws.numel() * ws.element_size(),
+                              _stream(stream)))
 
 
 def topk_select_workspace(T, k, ld_scores) -> int:

@@ -250,6 +250,50 @@ int index_score(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx
                      "index_score");
 }
 
+size_t index_topk_workspace(int64_t T, int k, int64_t ld_scores) {
+  return mx4::topk_workspace_bytes(T, k, ld_scores);
+}
+
+int index_topk(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx_pages,
+               int64_t idx_page_stride, int64_t num_pages, const int32_t* block_table, int64_t B,
+               int64_t bt_width, const int32_t* seq_lens, float* scores, int64_t ld_scores, int k,
+               int32_t* topk_idx, void* ws, size_t ws_bytes, void* stream) {
+  static const char* kName = "index_topk";
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: q_per_seq = %d (supported 1..8)", kName, q_per_seq);
+  if (k < 1 || k > 65536) return fail(MX4_ERR_UNSUPPORTED, "%s: k = %d", kName, k);
+  if (B < 0 || B > 65535) return fail(MX4_ERR_UNSUPPORTED, "%s: B = %lld", kName, (long long)B);
+  if (T != B * q_per_seq)
+    return fail(MX4_ERR_INVALID, "%s: T = %lld != B * q_per_seq", kName, (long long)T);
+  if (T > 65535) return fail(MX4_ERR_UNSUPPORTED, "%s: %lld tokens (max 65535)", kName, (long long)T);
+  if (ld_scores < 1) return fail(MX4_ERR_INVALID, "%s: ld_scores < 1", kName);
+  if ((ld_scores + 16383) / 16384 > 512)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: ld_scores = %lld (max 8388608)", kName,
+                (long long)ld_scores);
+  const size_t need = index_topk_workspace(T, k, ld_scores);
+  if (ws_bytes < need)
+    return fail(MX4_ERR_WORKSPACE, "%s: workspace %zu < %zu bytes", kName, ws_bytes, need);
+  if (need > 0 && (!ws || !aligned(ws, 16)))
+    return fail(MX4_ERR_INVALID, "%s: workspace NULL or not 16-byte aligned", kName);
+  if (B == 0) return ok();
+  if (!iq || !idx_pages || !block_table || !seq_lens || !scores || !topk_idx)
+    return fail(MX4_ERR_INVALID, "%s: NULL pointer", kName);
+  if (!aligned(iq, 16) || !aligned(idx_pages, 16) || idx_page_stride % 16 || !aligned(scores, 4))
+    return fail(MX4_ERR_INVALID, "%s: misaligned iq, pages or page stride", kName);
+  if (num_pages < 1 || idx_page_stride < mx4::kPageBytes || bt_width < 1)
+    return fail(MX4_ERR_INVALID, "%s: num_pages, page stride or bt_width invalid", kName);
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = mx4::launch_index_score(iq, q_per_seq, idx_pages, idx_page_stride, num_pages,
+                                          block_table, (int)B, bt_width, seq_lens, scores,
+                                          ld_scores, d->status, d->num_sms, s);
+  if (e == cudaSuccess)
+    e = mx4::launch_topk(scores, ld_scores, seq_lens, T, q_per_seq, k, topk_idx,
+                         need > 0 ? ws : nullptr, d->status, d->num_sms, s);
+  return cuda_result(e, kName);
+}
+
 int fp8_index_insert(const float* idx_k, int64_t T, const int64_t* slot_mapping, float scale,
                      uint8_t* pages, int64_t page_stride, int64_t num_pages, void* stream) {
   if (T < 0) return fail(MX4_ERR_INVALID, "fp8_index_insert: T = %lld < 0", (long long)T);
@@ -529,7 +573,7 @@ extern "C" int mx4_decode_step(const void* h_inputs, int64_t n_new, void* d_stag
   if (!idx_pages || !d_scores || idx_page_stride % 16 || !aligned(idx_pages, 16) ||
       idx_page_stride < mx4::kPageBytes || ld_scores < 1)
     return fail(MX4_ERR_INVALID, "%s: index pages, page stride or scores", kName);
-  if (topk_ws_bytes < topk_select_workspace(T, k, ld_scores) ||
+  if (topk_ws_bytes < index_topk_workspace(T, k, ld_scores) ||
       dec_ws_bytes < sparse_paged_decode_workspace(T, k))
     return fail(MX4_ERR_WORKSPACE, "%s: a workspace is too small", kName);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -541,11 +585,9 @@ extern "C" int mx4_decode_step(const void* h_inputs, int64_t n_new, void* d_stag
                             num_pages, stream))
       return rc;
   }
-  if (int rc = index_score(iq, T, q_per_seq, idx_pages, idx_page_stride, num_pages, block_table,
-                           B, bt_width, seq_lens, d_scores, ld_scores, stream))
-    return rc;
-  if (int rc = topk_select(d_scores, ld_scores, seq_lens, B, q_per_seq, k, d_topk_idx, topk_ws,
-                           topk_ws_bytes, stream))
+  if (int rc = index_topk(iq, T, q_per_seq, idx_pages, idx_page_stride, num_pages, block_table,
+                          B, bt_width, seq_lens, d_scores, ld_scores, k, d_topk_idx, topk_ws,
+                          topk_ws_bytes, stream))
     return rc;
   if (int rc = sparse_paged_decode(q, T, q_per_seq, 16, 1, k_pages, v_pages, kv_page_stride,
                                    kv_head_stride, num_pages, block_table, B, bt_width, seq_lens,

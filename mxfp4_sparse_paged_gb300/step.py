@@ -9,8 +9,8 @@ cache [pages, 16384] of the other revision, filled from the same rows.
 
 `DecodeStep` holds the per-step buffers and workspaces and issues, on one
 stream, the hot path of a decode step: [mx4_insert of the new tokens] ->
-index_score -> topk_select -> sparse_paged_decode.  It allocates nothing per
-step.
+index_topk (score and select in one call; fused=False issues index_score and
+topk_select instead) -> sparse_paged_decode.  It allocates nothing per step.
 """
 from __future__ import annotations
 
@@ -19,7 +19,7 @@ import math
 import numpy as np
 import torch
 
-from . import (FP8_PAGE_BYTES, fp8_index_insert, index_score, mx4_decode_step,
+from . import (FP8_PAGE_BYTES, fp8_index_insert, index_score, index_topk, mx4_decode_step,
                mx4_decode_step_input_layout, mx4_insert, sparse_paged_decode,
                sparse_paged_decode_workspace, topk_select, topk_select_workspace)
 from . import workloads as W
@@ -105,9 +105,10 @@ def step_inputs_host(wl: W.Workload):
 class DecodeStep:
     """Buffers and the kernel sequence of one decode step of workload `wl`."""
 
-    def __init__(self, wl: W.Workload, caches: PagedCaches, device="cuda"):
+    def __init__(self, wl: W.Workload, caches: PagedCaches, device="cuda", fused=True):
         self.wl = wl
         self.caches = caches
+        self.fused = fused
         T, k = wl.T, wl.k
         self.ld = int(wl.max_len)
         self.scale = 1.0 / math.sqrt(W.HEAD_DIM)
@@ -197,9 +198,11 @@ class DecodeStep:
             put(self.idx_new, host["idx_k"])
             put(self.slots, host["slots"])
 
-    def run(self, stream=None, events=None):
+    def run(self, stream=None, events=None, fused=None):
         """Enqueue the step on `stream`.  `events` (optional dict name -> (start, end)
-        CUDA events) brackets each kernel for per-kernel timing."""
+        CUDA events) brackets each entry point for per-kernel timing; `fused`
+        overrides the step's choice of index_topk or index_score + topk_select."""
+        fused = self.fused if fused is None else fused
         c = self.caches
         wl = self.wl
 
@@ -214,10 +217,16 @@ class DecodeStep:
         if self.slots.numel():
             timed("mx4_insert", lambda: c.insert_rows(self.k_new, self.v_new, self.idx_new,
                                                       self.slots, stream=stream, fp8=False))
-        timed("index_score", lambda: index_score(self.iq, wl.q, c.idx_pages, self.block_table,
-                                                 self.seq_lens, self.scores, stream=stream))
-        timed("topk_select", lambda: topk_select(self.scores, self.seq_lens, wl.q, wl.k,
-                                                 self.topk_idx, self.topk_ws, stream=stream))
+        if fused:
+            timed("index_topk", lambda: index_topk(self.iq, wl.q, c.idx_pages, self.block_table,
+                                                   self.seq_lens, self.scores, wl.k, self.topk_idx,
+                                                   self.topk_ws, stream=stream))
+        else:
+            timed("index_score", lambda: index_score(self.iq, wl.q, c.idx_pages,
+                                                     self.block_table, self.seq_lens, self.scores,
+                                                     stream=stream))
+            timed("topk_select", lambda: topk_select(self.scores, self.seq_lens, wl.q, wl.k,
+                                                     self.topk_idx, self.topk_ws, stream=stream))
         timed("sparse_paged_decode", lambda: sparse_paged_decode(
             self.q, wl.q, c.k_pages, c.v_pages, self.block_table, self.seq_lens, self.topk_idx,
             self.scale, self.out, self.dec_ws, stream=stream))
@@ -234,10 +243,12 @@ class DecodeStep:
                         stream=stream)
 
     def launches_per_step(self) -> int:
-        """Kernels this library launches per step: insert, score, top-k (threshold and
-        segment filter when rows can exceed the candidate capacity, then select), decode
-        split + merge."""
-        return (1 if self.slots.numel() else 0) + 1 + (3 if self.topk_ws is not None else 1) + 2
+        """Kernels this library launches per step: insert; the scorer; the row
+        select (one CTA a row) and, when a row may exceed 16384 scores, the cluster
+        select, plus the threshold, filter and select kernels when one may exceed
+        131072; decode run kernel + merge."""
+        sel = 1 + (1 if self.ld > 16384 else 0) + (3 if self.topk_ws is not None else 0)
+        return (1 if self.slots.numel() else 0) + 1 + sel + 2
 
 
 class PipelinedSteps:

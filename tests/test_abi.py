@@ -112,6 +112,7 @@ def test_workspace_sizes(lib):
     assert m.topk_select_workspace(3, 2048, 20000) == 2 * 16 + 48 + 2 * 3 * 8192 * 4
     assert m.topk_select_workspace(64, 2048, 8192) == 0      # no row exceeds the capacity
     assert m.topk_select_workspace(64, 9000, 131072) == 0    # k above the capacity
+    assert m.index_topk_workspace(64, 2048, 131072) == m.topk_select_workspace(64, 2048, 131072)
 
 
 def test_bindings_refuse_host_tensors_before_any_call():

@@ -282,7 +282,7 @@ def test_topk_bit_exact_on_shared_scores():
             row = -np.abs(rng.standard_normal(n)).astype(np.float32)
         sc[t, :n] = row
     lens_ok = lens
-    for k in (1, 7, 2048):
+    for k in (1, 7, 2048, 20000):
         want = oracle.topk_select(sc.astype(np.float64), lens_ok, q, k)
         d_sc = torch.from_numpy(sc).to(DEV)
         out = torch.empty((B * q, k), dtype=torch.int32, device=DEV)
@@ -299,7 +299,7 @@ def test_topk_segment_filter_paths():
     # candidate capacity (workspace-free exact path), and an odd row stride
     # (scalar loads).
     rng = np.random.default_rng(11)
-    lens = np.array([40000, 131072, 70001, 16385, 99999, 8193], np.int32)
+    lens = np.array([40000, 131072, 70001, 16385, 99999, 8193, 200000], np.int32)
     B, q = len(lens), 1
     for ld_pad, ks in ((0, (2048, 9000)), (1, (2048,))):
         ld = int(lens.max()) + ld_pad
@@ -402,6 +402,78 @@ def test_topk_threshold_retry_paths(k):
     got = out.cpu().numpy()
     for t in range(len(rows)):
         assert np.array_equal(got[t], want[t]), f"row {t} (n={lens[t]}, k={k})"
+
+
+@pytest.mark.parametrize("wid", [2, 3, 4])
+def test_index_topk_matches_the_separate_calls(wid):
+    # index_topk (scorer with key histograms + selection from them) against
+    # index_score + topk_select on the full workload: scores and selections
+    # bit-identical (the same fp32 scores, the same exact selection rule).
+    wl = W.make(wid)
+    caches, step, host = _gpu_step(wl)  # the step runs index_topk
+    sc_f, idx_f = step.scores.clone(), step.topk_idx.clone()
+    step.run(fused=False)
+    m.mx4_check_status()
+    n = wl.positions() + 1
+    sc_s = step.scores.cpu().numpy()
+    sf = sc_f.cpu().numpy()
+    for t in range(wl.T):
+        assert np.array_equal(sf[t, :n[t]], sc_s[t, :n[t]]), f"scores of token {t}"
+    assert torch.equal(idx_f, step.topk_idx)
+
+
+def test_index_topk_heavy_ties_and_short_rows():
+    # Index keys with a few distinct rows: the scores take a handful of values, so
+    # thousands of keys tie with the k-th largest and the lowest indices among them
+    # are taken; rows of one CTA, of a cluster, and longer than a cluster covers.
+    # Bit-exact against the oracle's selection of the oracle's scores (equal-valued
+    # keys give equal fp32 scores).
+    rng = np.random.default_rng(8)
+    lens = np.array([20000, 8192, 300, 131072, 140000], np.int32)
+    B, q, k = len(lens), 1, 2048
+    pages = (lens + 127) // 128
+    P = int(pages.sum())
+    ids = rng.permutation(P).astype(np.int32)
+    bt = np.full((B, int(pages.max())), -1, np.int32)
+    o = 0
+    for s_, n_ in enumerate(pages):
+        bt[s_, :n_] = ids[o:o + n_]
+        o += n_
+    base = rng.standard_normal((4, 128)).astype(np.float32)
+    ip_o = np.full((P, 8704), 0xFF, np.uint8)
+    ip = torch.full((P, 8704), 0xFF, dtype=torch.uint8, device=DEV)
+    kv = torch.full((P, 1, 8704), 0xFF, dtype=torch.uint8, device=DEV)
+    for s_ in range(B):
+        L = int(lens[s_])
+        rows = base[rng.integers(0, 4, L)]
+        pos = np.arange(L)
+        slots = (bt[s_, pos // 128].astype(np.int64) * 128 + pos % 128)
+        oracle.mx4_insert(None, None, rows, slots, None, None, ip_o)
+        r = torch.from_numpy(rows).to(DEV)
+        m.mx4_insert(r.view(L, 1, 128), r.view(L, 1, 128), r, torch.from_numpy(slots).to(DEV),
+                     kv, kv.clone(), ip)
+    m.mx4_check_status()
+    assert np.array_equal(ip.cpu().numpy(), ip_o)
+    iq = torch.from_numpy(rng.standard_normal((B, 128)).astype(np.float32)).to(torch.bfloat16)
+    iq_bits = iq.view(torch.int16).numpy().view(np.uint16)
+    ld = int(lens.max())
+    want_sc = oracle.index_score(iq_bits, q, ip_o, bt, lens, ld)
+    want = oracle.topk_select(want_sc, lens, q, k)
+    scores = torch.empty((B, ld), dtype=torch.float32, device=DEV)
+    out = torch.empty((B, k), dtype=torch.int32, device=DEV)
+    ws = torch.full((m.index_topk_workspace(B, k, ld),), 0xAB, dtype=torch.uint8, device=DEV)
+    for _ in range(2):  # the workspace's contents on entry do not matter
+        m.index_topk(iq.to(DEV), q, ip, torch.from_numpy(bt).to(DEV),
+                     torch.from_numpy(lens).to(DEV), scores, k, out, ws)
+        assert m.mx4_check_status() == 0
+        assert np.array_equal(out.cpu().numpy(), want)
+
+
+@pytest.mark.parametrize("q", [1, 4])
+def test_index_topk_ragged_long_rows_against_oracle(q):
+    # rows around the candidate capacity and the segment size, q decode tokens each
+    wl = _custom([8191, 8192, 8193, 16385, 40000, 70001], q=q, k=2048, seed=90 + q)
+    _compare(wl, range(wl.B), *_gpu_step(wl))
 
 
 @pytest.mark.parametrize("wid", [1, 4])
