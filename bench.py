@@ -297,9 +297,6 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
     host = step_inputs_host(wl)
     torch.cuda.synchronize()
     ab = W.algorithmic_bytes(wl)
-    names = (["mx4_insert"] if wl.spec.insert_in_step else []) + \
-        ["index_topk", "sparse_paged_decode"]
-    split_names = ["index_score", "topk_select"]
     # The in-step insert rewrites the decode tokens' rows with the same values, so
     # every timed step does identical work.
     step.load_inputs(host)
@@ -347,21 +344,29 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
     ck = clocks.stop()
     m.mx4_check_status()
     step_ms = _event_ms(st)
-    # Per-kernel times: the same steps again with an event pair around each entry
-    # point.  Events between kernels serialise them (no kernel starts under the
-    # previous one), so this pass is kept out of the step timing above.
-    per = {n: [(ev(), ev()) for _ in range(args.steps)] for n in names + split_names}
-    for i in range(args.steps):
-        flush_l2(i & 0xFF)
-        step.run(stream=stream, events={n: per[n][i] for n in names})
-    # the same steps with the scorer and the selection as separate calls: the
-    # scorer's own time (for its roofline) and the pair the fused call replaces
-    for i in range(args.steps):
-        flush_l2(i & 0xFF)
-        step.run(stream=stream, events={n: per[n][i] for n in split_names}, fused=False)
-    torch.cuda.synchronize()
+    # Per-kernel times: each entry point captured alone as a CUDA graph and replayed
+    # with an event pair around each replay (GPU time only, no host launch cost),
+    # the L2 flushed before each.  The selection is timed after the scorer has run, so
+    # it reads the scores of this step.
+    calls = step.stage_calls()  # on the current stream: the capture stream while capturing
+    kern_ms = {}
+    reps = min(args.steps, 200)
+    for name, fn in calls.items():
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        evs = [(ev(), ev()) for _ in range(reps)]
+        for i in range(reps):
+            flush_l2(i & 0xFF)
+            evs[i][0].record(stream)
+            g.replay()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        kern_ms[name] = statistics.mean(_event_ms(evs))
+        del g
     m.mx4_check_status()
-    kern_ms = {n: statistics.mean(_event_ms(per[n])) for n in names + split_names}
     total_ms = max_over_ranks(sum(step_ms), world, dev)
     value = job_value(wl.T, world, args.steps, total_ms)
 
@@ -405,10 +410,9 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
         "value": round(value, 1), "unit": UNIT, "ms_per_step": round(total_ms / args.steps, 4),
         "decode_tokens": wl.T, "cached_tokens": int(wl.seq_lens.astype(np.int64).sum()),
         "kernel_ms": {n: round(v, 5) for n, v in kern_ms.items()},
-        "kernel_ms_timing": "a second pass with a CUDA-event pair around each entry point "
-                            "(the events serialise the kernels); index_score and topk_select "
-                            "from a third pass with the two as separate calls, which the step's "
-                            "index_topk replaces",
+        "kernel_ms_timing": "each entry point captured alone as a CUDA graph, mean of event "
+                            "pairs around its replays, L2 flushed before each; index_score and "
+                            "topk_select are the pair index_topk combines",
         "roofline_index_score": r_score, "roofline_decode": r_dec,
         "hot_path_hbm": {"kernels": "index_score + sparse_paged_decode",
                          "algorithmic_bytes": int(hot), "achieved_gbs": round(hot_gbs, 1),
@@ -679,6 +683,42 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def profile_step(args):
+    """One eager decode step of the workload (each entry point once) and one launch of
+    each extra leg (the norm/rotary writer, the fp8 index-K insert and scorer), inside
+    the NVTX range "mx4_step", after the cache fill and a few warm-up steps outside it;
+    for an ncu capture of every library kernel of a step (--nvtx --nvtx-include
+    "mx4_step/").  Prints nothing to time."""
+    import torch
+
+    import mxfp4_sparse_paged_gb300 as m
+    from mxfp4_sparse_paged_gb300.step import DecodeStep, PagedCaches, step_inputs_host
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream()
+    wl = W.make(args.workload if args.workload is not None else 4)
+    caches = PagedCaches(wl.num_pages, device=dev, fp8_index_scale=FP8_INDEX_SCALE)
+    caches.fill(wl)
+    step = DecodeStep(wl, caches, device=dev)
+    step.load_inputs(step_inputs_host(wl))
+    for _ in range(args.warmup):
+        step.run(stream=stream, fused=False)
+    flush_l2 = _flusher(dev)
+    flush_l2(1)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("mx4_step")
+    step.run(stream=stream, fused=False)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("mx4_step")
+    time_writer(wl, dev, stream, lambda v: None, 1)
+    time_fp8_scorer(wl, caches, step, stream, lambda v: None, 1)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    m.mx4_check_status()
+    print(f"profile step done: {wl.spec.name}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -692,6 +732,9 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0,
                     help="seconds of oracle time for the cpu_baseline legs of the GPU arm")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-step", action="store_true",
+                    help="one step and one launch of each extra leg inside the NVTX range "
+                         "mx4_step, for an ncu capture; no timing")
     ap.add_argument("--eager", action="store_true",
                     help="time the step as separate API calls instead of one CUDA-graph launch")
     args = ap.parse_args()
@@ -701,6 +744,8 @@ def main():
         if args.workload is None:
             args.workload = 4
         run_reference(args)
+    elif args.profile_step:
+        profile_step(args)
     else:
         run_gpu(args)
 

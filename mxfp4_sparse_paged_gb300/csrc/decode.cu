@@ -103,19 +103,14 @@ __device__ __forceinline__ float f16_hi(uint32_t v) {
   return __half2float(__ushort_as_half((unsigned short)(v >> 16)));
 }
 
-// f16 bit pattern of 2^e for e <= 0: normal down to 2^-14, subnormal down to
-// 2^-24, 0 below.  A scale byte of 255 (NaN) gives an f16 NaN.
-__device__ __forceinline__ uint32_t f16_pow2(uint32_t byte, uint32_t ref) {
+// f16 bit pattern of 2^(byte - ref) for byte <= ref: normal down to 2^-14,
+// subnormal down to 2^-24, 0 below.  A scale byte of 255 (NaN) gives an f16 NaN.
+__device__ __forceinline__ uint16_t f16_pow2(uint32_t byte, int ref) {
   if (byte == 255u) return 0x7E00u;
-  const int e = (int)byte - (int)ref;
-  if (e >= -14) return (uint32_t)(e + 15) << 10;
-  if (e >= -24) return 1u << (e + 24);
+  const int e = (int)byte - ref;
+  if (e >= -14) return (uint16_t)((e + 15) << 10);
+  if (e >= -24) return (uint16_t)(1u << (e + 24));
   return 0u;
-}
-
-// bytes equal to 0xFF (NaN scales) do not take part in the reference maximum
-__device__ __forceinline__ uint32_t drop_nan_bytes(uint32_t w) {
-  return w & ~__vcmpeq4(w, 0xFFFFFFFFu);
 }
 
 // First tile of the range of warp g: the T * NT tiles cut into NW equal ranges.
@@ -195,7 +190,6 @@ __device__ __forceinline__ int load_q_fragments(const uint16_t* __restrict__ q, 
 __device__ __forceinline__ float pow2f(int e) {
   return e >= -126 ? __uint_as_float((uint32_t)(127 + e) << 23) : 0.f;
 }
-__device__ __forceinline__ int byte_of(uint32_t w, int b) { return (int)((w >> (8 * b)) & 0xFFu); }
 
 __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const DecodeArgs a) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -308,7 +302,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
   // ---- per-run state
   float o[16][4];
   float m_used[2] = {-INFINITY, -INFINITY}, lsum[2] = {0.f, 0.f};
-  uint32_t refV = 0u;  // largest V scale byte per 32-dim block so far (bytes 0..3)
+  int ref[4] = {0, 0, 0, 0};  // largest valid V scale byte per 32-dim block so far
   float cQ = 0.f;
   int64_t cur_t = -1;
   const int blo = tig >> 1, bhi = blo + 2;  // scale blocks of this lane's O columns
@@ -320,7 +314,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
     l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 1);
     l1 += __shfl_xor_sync(0xFFFFFFFFu, l1, 2);
     float* rec = a.ws + (gw + t) * kRecFloats;
-    const float flo = pow2f(byte_of(refV, blo) - 127), fhi = pow2f(byte_of(refV, bhi) - 127);
+    const float flo = pow2f((blo ? ref[1] : ref[0]) - 127), fhi = pow2f((blo ? ref[3] : ref[2]) - 127);
     float4* r4 = reinterpret_cast<float4*>(rec);
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
@@ -355,7 +349,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
       for (int j = 0; j < 16; ++j) o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
       m_used[0] = m_used[1] = -INFINITY;
       lsum[0] = lsum[1] = 0.f;
-      refV = 0u;
+      ref[0] = ref[1] = ref[2] = ref[3] = 0;
       const int sigma = load_q_fragments(a.q, t, w, lane);
       cQ = a.scale * kLog2e * pow2f(-sigma);  // logit (log2 units) = sum_b S_b 2^(s_b-127) cQ
     }
@@ -366,18 +360,24 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
       const uint8_t* sk = &w.slot[sl][0];
       const uint8_t* sv = sk + kTileV;
       const uint32_t* sw = reinterpret_cast<const uint32_t*>(sk + kTileSw);
-      // ---- scale tables of the tile: V reference, K factors, V multipliers
+      // ---- scale tables of the tile: V reference, K factors, V multipliers.  Lane l
+      // takes entry l % 16 and the scale blocks 2 (l / 16) and 2 (l / 16) + 1.
       {
-        const int er = lane & 15;
+        const int er = lane & 15, bp = lane >> 4;
         const uint32_t kwd = sw[er], vwd = sw[kTile + er];
-        uint32_t tmax = ((okb >> (2 * er)) & 1u) ? drop_nan_bytes(vwd) : 0u;
+        const bool ev = (okb >> (2 * er)) & 1u;
+        int nref[4];
+        bool grow = false;
 #pragma unroll
-        for (int of = 8; of > 0; of >>= 1)
-          tmax = __vmaxu4(tmax, __shfl_xor_sync(0xFFFFFFFFu, tmax, of));
-        const uint32_t nref = __vmaxu4(refV, tmax);
-        if (nref != refV) {  // warp-uniform: bring O to the larger reference
-          const float flo = pow2f(byte_of(refV, blo) - byte_of(nref, blo));
-          const float fhi = pow2f(byte_of(refV, bhi) - byte_of(nref, bhi));
+        for (int b = 0; b < 4; ++b) {  // largest valid scale byte of the tile (NaN excluded)
+          uint32_t x = (vwd >> (8 * b)) & 0xFFu;
+          x = __reduce_max_sync(0xFFFFFFFFu, (ev && x != 0xFFu) ? x : 0u);
+          nref[b] = max(ref[b], (int)x);
+          grow |= nref[b] != ref[b];
+        }
+        if (grow) {  // warp-uniform: bring O to the larger reference
+          const float flo = pow2f((blo ? ref[1] : ref[0]) - (blo ? nref[1] : nref[0]));
+          const float fhi = pow2f((blo ? ref[3] : ref[2]) - (blo ? nref[3] : nref[2]));
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const float f = j < 8 ? flo : fhi;
@@ -386,18 +386,15 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
             o[j][2] *= f;
             o[j][3] *= f;
           }
-          refV = nref;
-        }
-        if (lane < 16) {
-          w.kf[er] = make_float4(e8m0_to_float(kwd & 0xFFu) * cQ,
-                                 e8m0_to_float((kwd >> 8) & 0xFFu) * cQ,
-                                 e8m0_to_float((kwd >> 16) & 0xFFu) * cQ,
-                                 e8m0_to_float(kwd >> 24) * cQ);
-        } else {
 #pragma unroll
-          for (int b = 0; b < 4; ++b)
-            w.vm16[b][er] = (uint16_t)f16_pow2((vwd >> (8 * b)) & 0xFFu, (refV >> (8 * b)) & 0xFFu);
+          for (int b = 0; b < 4; ++b) ref[b] = nref[b];
         }
+        const int sh = 16 * bp;
+        *reinterpret_cast<float2*>(&w.kf[er].x + 2 * bp) =
+            make_float2(e8m0_to_float((kwd >> sh) & 0xFFu) * cQ,
+                        e8m0_to_float((kwd >> (sh + 8)) & 0xFFu) * cQ);
+        w.vm16[2 * bp][er] = f16_pow2((vwd >> sh) & 0xFFu, bp ? ref[2] : ref[0]);
+        w.vm16[2 * bp + 1][er] = f16_pow2((vwd >> (sh + 8)) & 0xFFu, bp ? ref[3] : ref[1]);
         __syncwarp();
       }
       const uint16_t* vm = &w.vm16[0][0];

@@ -198,6 +198,27 @@ class DecodeStep:
             put(self.idx_new, host["idx_k"])
             put(self.slots, host["slots"])
 
+    def stage_calls(self, stream=None) -> dict:
+        """Each entry point of the step as a callable (name -> fn), for timing them one
+        at a time: the insert (when the workload inserts), index_topk, and the pair it
+        combines (index_score, topk_select), and sparse_paged_decode."""
+        c, wl = self.caches, self.wl
+        calls = {}
+        if self.slots.numel():
+            calls["mx4_insert"] = lambda: c.insert_rows(self.k_new, self.v_new, self.idx_new,
+                                                        self.slots, stream=stream, fp8=False)
+        calls["index_topk"] = lambda: index_topk(self.iq, wl.q, c.idx_pages, self.block_table,
+                                                 self.seq_lens, self.scores, wl.k, self.topk_idx,
+                                                 self.topk_ws, stream=stream)
+        calls["index_score"] = lambda: index_score(self.iq, wl.q, c.idx_pages, self.block_table,
+                                                   self.seq_lens, self.scores, stream=stream)
+        calls["topk_select"] = lambda: topk_select(self.scores, self.seq_lens, wl.q, wl.k,
+                                                   self.topk_idx, self.topk_ws, stream=stream)
+        calls["sparse_paged_decode"] = lambda: sparse_paged_decode(
+            self.q, wl.q, c.k_pages, c.v_pages, self.block_table, self.seq_lens, self.topk_idx,
+            self.scale, self.out, self.dec_ws, stream=stream)
+        return calls
+
     def run(self, stream=None, events=None, fused=None):
         """Enqueue the step on `stream`.  `events` (optional dict name -> (start, end)
         CUDA events) brackets each entry point for per-kernel timing; `fused`
@@ -243,11 +264,10 @@ class DecodeStep:
                         stream=stream)
 
     def launches_per_step(self) -> int:
-        """Kernels this library launches per step: insert; the scorer; the row
-        select (one CTA a row) and, when a row may exceed 16384 scores, the cluster
-        select, plus the threshold, filter and select kernels when one may exceed
-        131072; decode run kernel + merge."""
-        sel = 1 + (1 if self.ld > 16384 else 0) + (3 if self.topk_ws is not None else 0)
+        """Kernels this library launches per step: insert; the scorer; the top-k
+        selection (threshold and segment filter when a row can exceed the candidate
+        capacity, then select); decode run kernel + merge."""
+        sel = 3 if self.topk_ws is not None else 1
         return (1 if self.slots.numel() else 0) + 1 + sel + 2
 
 
