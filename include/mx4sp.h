@@ -165,6 +165,27 @@ int index_score(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t *idx
                 int64_t ld_scores, void *stream);
 
 /* ---------------------------------------------------------------------------
+ * index_score_mxq -- the index scorer in block-scaled mode: the MXFP4 keys are
+ * the A operand of a block-scaled tensor-core product as stored (e2m1 codes,
+ * e8m0 scale per 32 dims), and each index-q row is first converted to MXFP8,
+ * the other MX operand format of the pages' scaled matrix core ("vllm.models.
+ * minimax_m3.amd.mono.weights", module description and mxfp8_a_tiles: the
+ * f8f6f4 MFMA with e8m0 scales).  Per 32-dim block b of iq[t]:
+ *     E_b = floor(log2 max|x|) - 8, clamped to [-127, 127] (-127 for a zero block)
+ *     code = E4M3(x * 2^-E_b), nearest, ties to even, saturating at 448
+ * and then
+ *     scores[t*ld_scores + i] = sum_b 2^E_b * sum_{d in b} E4M3value(code_d) * dequant(indexK[s, i])[d]
+ * for 0 <= i <= p, accumulated in fp32 by the tensor core; -inf and unwritten
+ * entries as index_score.  Arguments, layouts, limits, ownership and status
+ * bits are those of index_score.  An opt-in mode: it differs from index_score
+ * by the query's MXFP8 rounding (a relative error of at most 2^-4 per element).
+ * ------------------------------------------------------------------------- */
+int index_score_mxq(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t *idx_pages,
+                    int64_t idx_page_stride, int64_t num_pages, const int32_t *block_table,
+                    int64_t B, int64_t bt_width, const int32_t *seq_lens, float *scores,
+                    int64_t ld_scores, void *stream);
+
+/* ---------------------------------------------------------------------------
  * topk_select -- per-token top-k selection of the tokens to attend.
  *
  * For decode token t with n = p + 1 valid scores (p as above): the min(k, n)

@@ -18,7 +18,7 @@ import threading
 
 import torch
 
-__all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score",
+__all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score", "index_score_mxq",
            "index_topk", "index_topk_workspace", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
            "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "mx4_decode_step",
@@ -80,6 +80,8 @@ def _load():
                                         P, i64, P]
         lib.index_score.restype = i32
         lib.index_score.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, P]
+        lib.index_score_mxq.restype = i32
+        lib.index_score_mxq.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, P]
         lib.index_topk.restype = i32
         lib.index_topk.argtypes = [P, i64, i32, P, i64, i64, P, i64, i64, P, P, i64, i32, P, P,
                                    sz, P]
@@ -278,6 +280,16 @@ def index_score_fp8(iq, q_per_seq, pages, block_table, seq_lens, scale, scores, 
 
 def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=None):
     """scores[t, i] = iq[t] . dequant(indexK[s, i]) for i <= position (fp32 [T, ld])."""
+    _score_call("index_score", iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream)
+
+
+def index_score_mxq(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=None):
+    """index_score with iq[t] converted to MXFP8 first (block-scaled tensor-core mode)."""
+    _score_call("index_score_mxq", iq, q_per_seq, idx_pages, block_table, seq_lens, scores,
+                stream)
+
+
+def _score_call(name, iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream):
     _need(iq, torch.bfloat16, "iq")
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
@@ -290,10 +302,10 @@ def index_score(iq, q_per_seq, idx_pages, block_table, seq_lens, scores, stream=
     _rows_at_least(block_table, B, "block_table")
     _dims(scores, "scores", None, None)
     _rows_at_least(scores, B * int(q_per_seq), "scores")
-    _check(_load().index_score(_ptr(iq), int(iq.shape[0]), int(q_per_seq), _ptr(idx_pages),
-                               idx_pages.stride(0), int(idx_pages.shape[0]), _ptr(block_table), B,
-                               int(block_table.shape[1]), _ptr(seq_lens), _ptr(scores),
-                               scores.stride(0), _stream(stream)))
+    _check(getattr(_load(), name)(_ptr(iq), int(iq.shape[0]), int(q_per_seq), _ptr(idx_pages),
+                                  idx_pages.stride(0), int(idx_pages.shape[0]), _ptr(block_table),
+                                  B, int(block_table.shape[1]), _ptr(seq_lens), _ptr(scores),
+                                  scores.stride(0), _stream(stream)))
 
 
 def index_topk_workspace(T, k, ld_scores) -> int:

@@ -99,6 +99,8 @@ struct Fp8Fmt {
   static constexpr int kPageBytes = kFp8PageBytes;
   static constexpr int kConsumers = 8;  // one 16-row tile of each page per warp
   static constexpr int kStages = 4;
+  static constexpr int kExtraBytes = 0;
+  static constexpr bool kWholePage = false;
   static constexpr int ctas_per_sm(int) { return 2; }
 
   template <int Q>

@@ -29,6 +29,8 @@ struct Mxfp4Fmt {
   static constexpr int kPageBytes = mx4::kPageBytes;
   static constexpr int kConsumers = 8;  // one 16-row tile of each page per warp
   static constexpr int kStages = 4;
+  static constexpr int kExtraBytes = 0;
+  static constexpr bool kWholePage = false;
   static constexpr int ctas_per_sm(int Q) { return Q <= 2 ? 4 : (Q <= 6 ? 2 : 1); }
 
   template <int Q>

@@ -20,6 +20,9 @@ cudaError_t launch_insert(const float*, const float*, const float*, int64_t, int
 cudaError_t launch_index_score(const uint16_t*, int, const uint8_t*, int64_t, int64_t,
                                const int32_t*, int, int64_t, const int32_t*, float*, int64_t,
                                uint32_t*, int, cudaStream_t);
+cudaError_t launch_index_score_mxq(const uint16_t*, int, const uint8_t*, int64_t, int64_t,
+                                   const int32_t*, int, int64_t, const int32_t*, float*, int64_t,
+                                   uint32_t*, int, cudaStream_t);
 cudaError_t launch_topk(const float*, int64_t, const int32_t*, int64_t, int, int, int32_t*,
                         void*, uint32_t*, int, cudaStream_t);
 size_t topk_workspace_bytes(int64_t, int, int64_t);
@@ -145,6 +148,34 @@ int check_decode_pointers(const char* name, const uint16_t* q, const uint8_t* k_
   return MX4_OK;
 }
 
+// Shared by index_score and index_score_mxq: same arguments, same limits.
+using ScoreLaunch = cudaError_t (*)(const uint16_t*, int, const uint8_t*, int64_t, int64_t,
+                                    const int32_t*, int, int64_t, const int32_t*, float*, int64_t,
+                                    uint32_t*, int, cudaStream_t);
+int score_entry(const char* name, ScoreLaunch launch, const uint16_t* iq, int64_t T,
+                int q_per_seq, const uint8_t* idx_pages, int64_t idx_page_stride,
+                int64_t num_pages, const int32_t* block_table, int64_t B, int64_t bt_width,
+                const int32_t* seq_lens, float* scores, int64_t ld_scores, void* stream) {
+  if (q_per_seq < 1 || q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: q_per_seq = %d (supported 1..8)", name, q_per_seq);
+  if (B < 0 || B > 65535) return fail(MX4_ERR_UNSUPPORTED, "%s: B = %lld", name, (long long)B);
+  if (T != B * q_per_seq)
+    return fail(MX4_ERR_INVALID, "%s: T = %lld != B * q_per_seq", name, (long long)T);
+  if (B == 0) return ok();
+  if (!iq || !idx_pages || !block_table || !seq_lens || !scores)
+    return fail(MX4_ERR_INVALID, "%s: NULL pointer", name);
+  if (!aligned(iq, 16) || !aligned(idx_pages, 16) || idx_page_stride % 16 || !aligned(scores, 4))
+    return fail(MX4_ERR_INVALID, "%s: misaligned iq, pages or page stride", name);
+  if (num_pages < 1 || idx_page_stride < mx4::kPageBytes || bt_width < 1 || ld_scores < 1)
+    return fail(MX4_ERR_INVALID, "%s: num_pages, page stride, bt_width or ld invalid", name);
+  DeviceInfo* d;
+  if (int rc = device_info(&d)) return rc;
+  return cuda_result(launch(iq, q_per_seq, idx_pages, idx_page_stride, num_pages, block_table,
+                            (int)B, bt_width, seq_lens, scores, ld_scores, d->status, d->num_sms,
+                            static_cast<cudaStream_t>(stream)),
+                     name);
+}
+
 }  // namespace
 
 extern "C" {
@@ -229,25 +260,18 @@ int index_score(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx
                 int64_t idx_page_stride, int64_t num_pages, const int32_t* block_table,
                 int64_t B, int64_t bt_width, const int32_t* seq_lens, float* scores,
                 int64_t ld_scores, void* stream) {
-  if (q_per_seq < 1 || q_per_seq > 8)
-    return fail(MX4_ERR_UNSUPPORTED, "index_score: q_per_seq = %d (supported 1..8)", q_per_seq);
-  if (B < 0 || B > 65535) return fail(MX4_ERR_UNSUPPORTED, "index_score: B = %lld", (long long)B);
-  if (T != B * q_per_seq)
-    return fail(MX4_ERR_INVALID, "index_score: T = %lld != B * q_per_seq", (long long)T);
-  if (B == 0) return ok();
-  if (!iq || !idx_pages || !block_table || !seq_lens || !scores)
-    return fail(MX4_ERR_INVALID, "index_score: NULL pointer");
-  if (!aligned(iq, 16) || !aligned(idx_pages, 16) || idx_page_stride % 16 || !aligned(scores, 4))
-    return fail(MX4_ERR_INVALID, "index_score: misaligned iq, pages or page stride");
-  if (num_pages < 1 || idx_page_stride < mx4::kPageBytes || bt_width < 1 || ld_scores < 1)
-    return fail(MX4_ERR_INVALID, "index_score: num_pages, page stride, bt_width or ld invalid");
-  DeviceInfo* d;
-  if (int rc = device_info(&d)) return rc;
-  return cuda_result(mx4::launch_index_score(iq, q_per_seq, idx_pages, idx_page_stride,
-                                             num_pages, block_table, (int)B, bt_width, seq_lens,
-                                             scores, ld_scores, d->status, d->num_sms,
-                                             static_cast<cudaStream_t>(stream)),
-                     "index_score");
+  return score_entry("index_score", mx4::launch_index_score, iq, T, q_per_seq, idx_pages,
+                     idx_page_stride, num_pages, block_table, B, bt_width, seq_lens, scores,
+                     ld_scores, stream);
+}
+
+int index_score_mxq(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t* idx_pages,
+                    int64_t idx_page_stride, int64_t num_pages, const int32_t* block_table,
+                    int64_t B, int64_t bt_width, const int32_t* seq_lens, float* scores,
+                    int64_t ld_scores, void* stream) {
+  return score_entry("index_score_mxq", mx4::launch_index_score_mxq, iq, T, q_per_seq,
+                     idx_pages, idx_page_stride, num_pages, block_table, B, bt_width, seq_lens,
+                     scores, ld_scores, stream);
 }
 
 size_t index_topk_workspace(int64_t T, int k, int64_t ld_scores) {

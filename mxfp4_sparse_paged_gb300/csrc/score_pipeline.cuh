@@ -17,6 +17,11 @@
 // page per warp (the format's tile math), and arrive on the stage's "empty"
 // mbarrier.  Every wait is bounded: on time-out the kernel sets
 // MX4_STATUS_TIMEOUT, stops, and drains the copies in flight before exiting.
+//
+// A format whose tile math takes a whole page at once (kWholePage: the
+// block-scaled tensor-core scorer) gets the stage ring and a region of
+// kExtraBytes of shared memory for its operand tiles, and runs its own consumer
+// loop over the same stages.
 #pragma once
 
 #include "common.cuh"
@@ -47,19 +52,35 @@ struct ScoreArgs {
   float scale;                 // the fp8 cache's scale (1 for MXFP4)
 };
 
-// Shared-memory layout of the kernel, in bytes: stages | barriers | stage info |
-// warp sums, flags | per-sequence page prefix [B].
+// Shared-memory layout of the kernel, in bytes: format region | stages |
+// barriers | stage info | warp sums, flags | per-sequence page prefix [B].
 template <class F, int Q>
 struct ScoreLayout {
   static constexpr int kStageBytes = F::kPageBytes + Q * kHeadDim * 2;
   static_assert(kStageBytes % 16 == 0, "bulk-copy alignment");
-  static constexpr int kStagesOff = 0;
-  static constexpr int kBarOff = F::kStages * kStageBytes;  // full[S], empty[S]
+  static_assert(F::kExtraBytes % 128 == 0, "format region alignment");
+  static constexpr int kStagesOff = F::kExtraBytes;
+  static constexpr int kBarOff = kStagesOff + F::kStages * kStageBytes;  // full[S], empty[S]
   static constexpr int kInfoOff = kBarOff + 2 * F::kStages * 8;
   static constexpr int kWarpSumOff = kInfoOff + 4 * F::kStages * 4;
   static constexpr int kFlagOff = kWarpSumOff + 32 * 4;  // abort, issued
   static constexpr int kPrefOff = (kFlagOff + 8 + 15) / 16 * 16;
   static size_t bytes(int B) { return (size_t)kPrefOff + (size_t)B * 4; }
+};
+
+// The stage ring as a whole-page consumer sees it: stage st holds a page (and the
+// sequence's index-q rows after it) once full[st] completes its phase; the
+// consumer arrives on empty[st] (one arrival per consumer warp) to free it.
+struct StageRing {
+  uint8_t* base;
+  int stage_bytes;
+  uint64_t* full;
+  uint64_t* empty;
+  const int* seq;
+  const int* page;
+  const int* len;
+  const int* ok;
+  volatile int* abort_flag;
 };
 
 template <class F, int Q>
@@ -192,39 +213,45 @@ score_kernel(const ScoreArgs a) {
   }
 
   // ================= consumers
-  typename F::template Tile<Q> tile;
-  int cur_seq = -1;
-  for (int kk = 0; kk < n; ++kk) {
-    const int st = kk % S, round = kk / S;
-    bool landed = false;
-    for (uint32_t i = 0; i < kWaitPolls && !landed; ++i) {
-      landed = mbar_test(smem_addr(&full[st]), round & 1);
-      if (!landed && *abort_flag) break;
-    }
-    if (!__all_sync(0xFFFFFFFFu, landed)) {
-      if (lane == 0) flag(a.status, MX4_STATUS_TIMEOUT);
-      *abort_flag = 1;
-      break;
-    }
-    const int seq = info_seq[st], pg = info_page[st], L = info_len[st];
-    if (info_ok[st]) {
-      const uint8_t* page = smem_raw + Lay::kStagesOff + st * Lay::kStageBytes;
-      if (seq != cur_seq) {
-        tile.set_queries(reinterpret_cast<const uint16_t*>(page + F::kPageBytes), lane, a.scale);
-        cur_seq = seq;
+  if constexpr (F::kWholePage) {
+    const StageRing ring{smem_raw + Lay::kStagesOff, Lay::kStageBytes, full, empty, info_seq,
+                         info_page, info_len, info_ok, abort_flag};
+    F::template consume<Q>(a, ring, smem_raw, n, warp, lane);
+  } else {
+    typename F::template Tile<Q> tile;
+    int cur_seq = -1;
+    for (int kk = 0; kk < n; ++kk) {
+      const int st = kk % S, round = kk / S;
+      bool landed = false;
+      for (uint32_t i = 0; i < kWaitPolls && !landed; ++i) {
+        landed = mbar_test(smem_addr(&full[st]), round & 1);
+        if (!landed && *abort_flag) break;
       }
-      // score of row r of this page for query qq: -inf past the token's position
-      auto emit = [&](int qq, int r, float v) {
-        const int64_t i_g = (int64_t)pg * kPageTokens + r;
-        const int64_t p = (int64_t)L - Q + qq;
-        if (i_g < L) a.scores[((int64_t)seq * Q + qq) * a.ld + i_g] = (i_g <= p) ? v : -INFINITY;
-      };
+      if (!__all_sync(0xFFFFFFFFu, landed)) {
+        if (lane == 0) flag(a.status, MX4_STATUS_TIMEOUT);
+        *abort_flag = 1;
+        break;
+      }
+      const int seq = info_seq[st], pg = info_page[st], L = info_len[st];
+      if (info_ok[st]) {
+        const uint8_t* page = smem_raw + Lay::kStagesOff + st * Lay::kStageBytes;
+        if (seq != cur_seq) {
+          tile.set_queries(reinterpret_cast<const uint16_t*>(page + F::kPageBytes), lane, a.scale);
+          cur_seq = seq;
+        }
+        // score of row r of this page for query qq: -inf past the token's position
+        auto emit = [&](int qq, int r, float v) {
+          const int64_t i_g = (int64_t)pg * kPageTokens + r;
+          const int64_t p = (int64_t)L - Q + qq;
+          if (i_g < L) a.scores[((int64_t)seq * Q + qq) * a.ld + i_g] = (i_g <= p) ? v : -INFINITY;
+        };
 #pragma unroll
-      for (int tt = 0; tt < kPageTokens / 16 / NC; ++tt)
-        tile.run(page, (warp + NC * tt) * 16, lane, emit);
+        for (int tt = 0; tt < kPageTokens / 16 / NC; ++tt)
+          tile.run(page, (warp + NC * tt) * 16, lane, emit);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_addr(&empty[st]));
   }
 }
 
