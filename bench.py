@@ -463,7 +463,8 @@ def run_gpu(args):
     wl, caches, step, host, kern_ms = head_live
     peak, _ = _peaks()
 
-    # the headline's extra legs: the overlapped serving loop, the writer, the fp8 scorer
+    # the headline's extra legs: the overlapped serving loop, the writer, the fp8 and
+    # block-scaled scorers
     from mxfp4_sparse_paged_gb300.step import PipelinedSteps
     pipe = PipelinedSteps(wl, caches, device=dev)
     pin = pipe.pack_inputs(host)
@@ -482,6 +483,7 @@ def run_gpu(args):
     pipe_ms = max_over_ranks(e0.elapsed_time(e1), world, dev)
     writer = time_writer(wl, dev, stream, flush_l2, min(args.steps, 200))
     fp8 = time_fp8_scorer(wl, caches, step, stream, flush_l2, min(args.steps, 200))
+    mxq = time_mxq_scorer(wl, caches, step, stream, flush_l2, min(args.steps, 200))
 
     # roofline of the step's dominant HBM-bound kernel (the one taking longer)
     dominant = "roofline_decode" if kern_ms["sparse_paged_decode"] > kern_ms["index_score"] \
@@ -512,6 +514,11 @@ def run_gpu(args):
         "norm_rope_writer": writer,
         "fp8_index_variant": dict(fp8, mxfp4_index_score_us=round(kern_ms["index_score"] * 1e3, 2),
                                   peak_gbs=peak, frac=round(fp8["achieved_gbs"] / peak, 4)),
+        "block_scaled_index_variant": dict(
+            mxq, mxfp4_index_score_us=round(kern_ms["index_score"] * 1e3, 2), peak_gbs=peak,
+            frac=round(mxq["achieved_gbs"] / peak, 4),
+            numerics="index-q converted to MXFP8 (OCP: per 32-dim block, shared exponent "
+                     "floor(log2 amax) - 8, E4M3 elements); tcgen05 block-scaled MMA"),
         "gpu_launches": head_blk["gpu_launches"],
         "clocks": head_blk["clocks"],
         "wall_s_timed_region": head_blk["wall_s_timed_region"],
@@ -563,6 +570,39 @@ def time_fp8_scorer(wl, caches, step, stream, flush_l2, steps):
     nbytes = int(W.HEAD_DIM * wl.seq_lens.astype(np.int64).sum())
     return {"kernel": "index_score_fp8", "scale": caches.fp8_index_scale, "us": round(us, 2),
             "algorithmic_bytes": nbytes, "achieved_gbs": round(nbytes / us / 1e3, 1),
+            "timing": "mean of CUDA-event pairs on the launching stream, L2 flushed before each"}
+
+
+def time_mxq_scorer(wl, caches, step, stream, flush_l2, steps):
+    """index_score_mxq -- the block-scaled tensor-core scorer, index-q converted to
+    MXFP8 -- over the step's own MXFP4 index-K cache, index-q, block table and
+    lengths: event-timed per launch on the launching stream after an L2 flush.
+    Algorithmic bytes as index_score's: one 68-byte key row per cached token."""
+    import torch
+
+    import mxfp4_sparse_paged_gb300 as m
+
+    def score():
+        m.index_score_mxq(step.iq, wl.q, caches.idx_pages, step.block_table, step.seq_lens,
+                          step.scores, stream=stream)
+
+    for _ in range(3):
+        flush_l2(1)
+        score()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)]
+    for i in range(steps):
+        flush_l2(i & 0xFF)
+        evs[i][0].record(stream)
+        score()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    m.mx4_check_status()
+    us = statistics.mean(a.elapsed_time(b) for a, b in evs) * 1e3
+    nbytes = W.algorithmic_bytes(wl)["index_score"]
+    return {"kernel": "index_score_mxq", "us": round(us, 2), "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(nbytes / us / 1e3, 1),
+            "traffic": _ncu_traffic(wl.spec.name, "index_score_mxq_traffic.json"),
             "timing": "mean of CUDA-event pairs on the launching stream, L2 flushed before each"}
 
 
@@ -685,7 +725,8 @@ def run_reference(args):
 
 def profile_step(args):
     """One eager decode step of the workload (each entry point once) and one launch of
-    each extra leg (the norm/rotary writer, the fp8 index-K insert and scorer), inside
+    each extra leg (the norm/rotary writer, the fp8 index-K insert and scorer, the
+    block-scaled scorer), inside
     the NVTX range "mx4_step", after the cache fill and a few warm-up steps outside it;
     for an ncu capture of every library kernel of a step (--nvtx --nvtx-include
     "mx4_step/").  Prints nothing to time."""
@@ -713,6 +754,7 @@ def profile_step(args):
     torch.cuda.nvtx.range_push("mx4_step")
     time_writer(wl, dev, stream, lambda v: None, 1)
     time_fp8_scorer(wl, caches, step, stream, lambda v: None, 1)
+    time_mxq_scorer(wl, caches, step, stream, lambda v: None, 1)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     m.mx4_check_status()
