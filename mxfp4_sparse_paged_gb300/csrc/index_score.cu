@@ -29,6 +29,9 @@ struct Mxfp4Fmt {
   static constexpr int kPageBytes = mx4::kPageBytes;
   static constexpr int kConsumers = 8;  // one 16-row tile of each page per warp
   static constexpr int kStages = 4;
+  static constexpr int kStageDataBytes = kPageBytes;
+  static constexpr int kFullCount = 1;             // the producer's expect-tx arrival
+  static constexpr int kEmptyCount = kConsumers;    // one arrival per consumer warp
   static constexpr int kExtraBytes = 0;
   static constexpr bool kWholePage = false;
   static constexpr int ctas_per_sm(int Q) { return Q <= 2 ? 4 : (Q <= 6 ? 2 : 1); }

@@ -18,20 +18,25 @@
 //   A: the 16 codes of K-chunk j of row m take the first 8 bytes of a 16-byte
 //      slot at (m/8)*1024 + j*128 + (m%8)*16 (the e2m1 operand of this MMA kind
 //      is packed two a byte, low nibble first, in 16-byte slots of which the
-//      last 8 bytes are ignored), so a page row's 64 bytes are spread as eight
-//      8-byte pieces; LBO (next K-chunk) = 128, SBO (next 8 rows) = 1024.
+//      last 8 bytes are ignored); LBO (next K-chunk) = 128, SBO (next 8 rows) =
+//      1024.  The producer copies each 8-byte piece of the page straight from
+//      global memory to its slot (cp.async), so the A tile is the stage itself.
 //   B: the 16 E4M3 bytes of K-chunk j of query n at (n/8)*1024 + j*128 + (n%8)*16.
-//   Scales in tensor memory: row m's word at lane m, column kColSfa + m/32;
+//   Scales in tensor memory: row m's word at lane m, column (key scales) + m/32;
 //   query n's word at lane n of every lane quarter (each quarter of the
-//   accumulator reads the query scales from its own 32 lanes), column kColSfb.
+//   accumulator reads the query scales from its own 32 lanes).
 //   Accumulator: lane m = page row m, column n = query n (fp32).
 //
-// Roles: the pipeline's producer warp streams pages into the stage ring; four
-// consumer warps (one per tensor-memory lane quarter) copy each page into the A
-// tile and its scale words into tensor memory, free the stage, and thread 0
-// issues the four MMAs; the warps read the accumulator back with tcgen05.ld and
-// write the scores.  Every wait is bounded and every exit frees the tensor
-// memory the CTA allocated.
+// Stage: A tile (16384 B) | the page's 512 scale bytes | the sequence's index-q
+// rows.  Its full barrier completes when the producer's bulk copies (scales,
+// queries; transaction-counted) and every producer lane's 8-byte copies
+// (cp.async.mbarrier.arrive) have landed; the MMA group's commit frees it.
+//
+// Consumers (four warps, one per tensor-memory lane quarter): per page, write
+// its scale words into tensor memory, and thread 0 issues the four MMAs into
+// one of two accumulators; then read back and store the previous page's
+// scores, whose MMAs ran meanwhile.  Every wait is bounded and every exit waits
+// for the MMAs in flight and frees the tensor memory the CTA allocated.
 #include "score_pipeline.cuh"
 
 namespace mx4 {
@@ -39,15 +44,16 @@ namespace mx4 {
 namespace mxq {
 
 constexpr int kATileBytes = 128 * 8 * 16;  // 128 rows x 8 K-chunks x 16-byte slots
+constexpr int kScaleBytes = 128 * 4;
 constexpr int kBTileBytes = 16 * 8 * 16;   // 16 query rows x 8 K-chunks x 16 bytes
-constexpr int kTmemCols = 32;              // the smallest allocation
-constexpr int kColD = 0;                   // accumulator: columns 0 .. 15
-constexpr int kColSfa = 16;                // key scales: columns 16 .. 19
-constexpr int kColSfb = 24;                // query scales: column 24
-// format region: A tile | B tile | MMA barrier | tensor-memory address | query scale bytes
-constexpr int kBarOff = kATileBytes + kBTileBytes;
-constexpr int kTaddrOff = kBarOff + 8;
-constexpr int kSfbOff = kTaddrOff + 8;
+constexpr int kTmemCols = 64;              // an allocation is a power of two >= 32
+constexpr int kColD = 0;                   // accumulators: columns 0..15 and 16..31
+constexpr int kColSfa = 32;                // key scales: columns 32..35 and 36..39
+constexpr int kColSfb = 40;                // query scales
+// format region: B tile | MMA barriers [2] | tensor-memory address | query scale bytes
+constexpr int kBarOff = kBTileBytes;
+constexpr int kTaddrOff = kBarOff + 16;
+constexpr int kSfbOff = kTaddrOff + 16;
 constexpr int kRegionBytes = (kSfbOff + 16 * 4 + 127) / 128 * 128;
 
 __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
@@ -88,6 +94,22 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tmem_st1(uint32_t taddr, uint32_t v) {
   asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};\n" ::"r"(taddr), "r"(v) : "memory");
 }
+__device__ __forceinline__ void commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                   bar)
+               : "memory");
+}
+
+// 8-byte copy global -> shared (L1-allocating; the only cp.async size below 16
+// bytes that fits an e2m1 K-chunk), and the arrival on `bar` that fires when all
+// of this thread's earlier cp.async copies have landed (counted in the barrier's
+// expected arrivals).
+__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];\n" ::"r"(bar) : "memory");
+}
 
 // E4M3 codes of four fp32 values (nearest, ties to even, saturating at 448),
 // x0 in the low byte.
@@ -102,17 +124,84 @@ __device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x
 
 struct MxqFmt {
   static constexpr int kPageBytes = mx4::kPageBytes;
+  static constexpr int kStageDataBytes = mxq::kATileBytes + mxq::kScaleBytes;
   static constexpr int kConsumers = 4;  // one warp per tensor-memory lane quarter
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 3;
+  static constexpr int kFullCount = 1 + 32;  // the expect-tx arrival + each producer lane's copies
+  static constexpr int kEmptyCount = 1;      // the MMA group's commit (or a skip)
   static constexpr int kExtraBytes = mxq::kRegionBytes;
   static constexpr bool kWholePage = true;
+  // Three CTAs per SM (three producer warps): the 8-byte copies allocate in L1,
+  // and the misses an SM can keep in flight, not the stage count, set the rate
+  // (measured on the b256 workload: 1 CTA x 8 stages 123 us, 2 x 5 74 us, 3 x 3 62 us).
   static constexpr int ctas_per_sm(int) { return 3; }
 
-  // The sequence's index-q rows (bf16, in the stage after the page) -> MXFP8:
-  // the B tile and the query scale words (written by each warp into its own lane
-  // quarter).  Thread t converts the 16 elements of
-  // K-chunk j = t % 8 of query n = t / 8; the two threads of a 32-element block
-  // share its largest magnitude.
+  // Producer warp: for each page of the CTA's range, once its stage is free, the
+  // page's 8-byte K-chunks go to their A-tile slots (instruction i of the 32 covers
+  // rows 8*(i/2) .. +7 and K-chunks 4*(i%2) .. +3: whole 32-byte sectors of the
+  // page), the scale row and the sequence's index-q rows by bulk copy.
+  template <int Q>
+  static __device__ void produce(const ScoreArgs& a, const StageRing& ring, const int* pref,
+                                 int p0, int n, int lane) {
+    constexpr int S = kStages;
+    for (int base = 0; base < n; base += 32) {
+      if (__any_sync(0xFFFFFFFFu, *ring.abort_flag != 0)) break;
+      PageRef pr{a.pages, -1, 0, 0, 0};
+      if (base + lane < n) pr = resolve_page(a, pref, p0 + base + lane);
+      const int cnt = min(32, n - base);
+      bool go = true;
+      for (int l = 0; l < cnt && go; ++l) {
+        const int kk = base + l, st = kk % S, round = kk / S;
+        const uint8_t* src = reinterpret_cast<const uint8_t*>(
+            __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(pr.src), l));
+        const int ok = __shfl_sync(0xFFFFFFFFu, pr.ok, l);
+        const int seq = __shfl_sync(0xFFFFFFFFu, pr.seq, l);
+        if (lane == 0) {
+          go = !*ring.abort_flag;
+          if (go && round > 0 && !mbar_wait(smem_addr(&ring.empty[st]), (round - 1) & 1)) {
+            flag(a.status, MX4_STATUS_TIMEOUT);
+            *ring.abort_flag = 1;
+            go = false;
+          }
+        }
+        go = __shfl_sync(0xFFFFFFFFu, go, 0);
+        if (!go) break;
+        if (lane == l) {
+          ring.seq[st] = pr.seq;
+          ring.page[st] = pr.page;
+          ring.len[st] = pr.len;
+          ring.ok[st] = pr.ok;
+        }
+        __syncwarp();
+        const uint32_t fb = smem_addr(&ring.full[st]);
+        const uint32_t d0 = smem_addr(ring.base + st * ring.stage_bytes);
+        if (ok) {
+          if (lane == 0) {
+            mbar_arrive_expect_tx(fb, mxq::kScaleBytes + Q * kHeadDim * 2);
+            bulk_copy_g2s(d0 + mxq::kATileBytes, src + kScaleOffset, mxq::kScaleBytes, fb);
+            bulk_copy_g2s(d0 + kStageDataBytes, a.iq + (int64_t)seq * Q * kHeadDim,
+                          Q * kHeadDim * 2, fb);
+          }
+#pragma unroll 8
+          for (int i = 0; i < 32; ++i) {
+            const int r = (i >> 1) * 8 + (lane & 7), j = (i & 1) * 4 + (lane >> 3);
+            mxq::cp_async8(d0 + (r >> 3) * 1024 + j * 128 + (r & 7) * 16, src + r * 64 + j * 8);
+          }
+          mxq::cp_async_arrive(fb);
+        } else {
+          if (lane == 0) mbar_arrive(fb);
+          mbar_arrive(fb);
+        }
+        if (lane == 0) *ring.issued = kk + 1;
+      }
+      if (!go) break;
+    }
+  }
+
+  // The sequence's index-q rows (bf16, in the stage) -> MXFP8: the B tile and the
+  // query scale words (written by each warp into its own lane quarter).  Thread t
+  // converts the 16 elements of K-chunk j = t % 8 of query n = t / 8; the two
+  // threads of a 32-element block share its largest magnitude.
   template <int Q>
   static __device__ __forceinline__ void set_queries(const uint16_t* qs, uint8_t* region,
                                                      uint32_t tm, int tid, int warp, int lane) {
@@ -148,10 +237,10 @@ struct MxqFmt {
       codes.z = mxq::e4m3x4(x[8], x[9], x[10], x[11]);
       codes.w = mxq::e4m3x4(x[12], x[13], x[14], x[15]);
     }
-    *reinterpret_cast<uint4*>(region + mxq::kATileBytes + (n >> 3) * 1024 + j * 128 +
-                              (n & 7) * 16) = codes;
+    *reinterpret_cast<uint4*>(region + (n >> 3) * 1024 + j * 128 + (n & 7) * 16) = codes;
     uint8_t* sfb = region + mxq::kSfbOff;
     if ((j & 1) == 0) sfb[n * 4 + (j >> 1)] = (uint8_t)(n < Q ? E + 127 : 127);
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");  // the B tile, for the MMA
     mxq::named_sync();
     const uint32_t word = *reinterpret_cast<const uint32_t*>(sfb + (lane & 15) * 4);
     mxq::tmem_st1(tm + ((uint32_t)(32 * warp) << 16) + mxq::kColSfb, word);
@@ -163,12 +252,11 @@ struct MxqFmt {
     constexpr int S = kStages;
     const int tid = warp * 32 + lane;
     if (n == 0) return;  // no pages for this CTA: nothing allocated
-    uint8_t* atile = region;
-    uint64_t* mma_bar = reinterpret_cast<uint64_t*>(region + mxq::kBarOff);
+    uint64_t* mma_bar = reinterpret_cast<uint64_t*>(region + mxq::kBarOff);  // one per accumulator
     uint32_t* taddr_slot = reinterpret_cast<uint32_t*>(region + mxq::kTaddrOff);
-    const uint32_t bar = smem_addr(mma_bar);
     if (tid == 0) {
-      mbar_init(bar, 1);
+      mbar_init(smem_addr(&mma_bar[0]), 1);
+      mbar_init(smem_addr(&mma_bar[1]), 1);
       fence_barrier_init();
     }
     if (warp == 0) {
@@ -183,11 +271,46 @@ struct MxqFmt {
     mxq::tc_fence_after();
     const uint32_t tm = *taddr_slot;
     const uint32_t lane_base = tm + ((uint32_t)(32 * warp) << 16);
-    const uint32_t a_addr = smem_addr(atile), b_addr = a_addr + mxq::kATileBytes;
+    const uint32_t b_addr = smem_addr(region);
 
     int cur_seq = -1;
-    uint32_t mma_phase = 0;
-    bool mma_pending = false;  // an MMA group whose completion was not seen
+    uint32_t phases = 0;   // bit b: the phase of mma_bar[b] to wait for next
+    uint32_t groups = 0;   // MMA groups issued; group g accumulates in buffer g & 1
+    uint32_t running = 0;  // bit b: buffer b's last group has not been waited for
+    bool pending = false;  // a group issued and not read back yet: (p_seq, p_pg, p_len, p_buf)
+    int p_seq = 0, p_pg = 0, p_len = 0;
+    uint32_t p_buf = 0;
+    bool failed = false;
+
+    // Wait for the pending group, read its accumulator and store its scores.
+    auto read_back = [&]() -> bool {
+      const bool done = mbar_wait(smem_addr(&mma_bar[p_buf]), (phases >> p_buf) & 1u);
+      if (!mxq::all_consumers(done)) return false;
+      phases ^= 1u << p_buf;
+      running &= ~(1u << p_buf);
+      pending = false;
+      mxq::tc_fence_after();
+      uint32_t d[8];
+      asm volatile(
+          "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
+          : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]),
+            "=r"(d[7])
+          : "r"(lane_base + mxq::kColD + 16u * p_buf)
+          : "memory");
+      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+      const int64_t i_g = (int64_t)p_pg * kPageTokens + 32 * warp + lane;
+      if (i_g < p_len) {
+#pragma unroll
+        for (int qq = 0; qq < Q; ++qq) {
+          const int64_t p = (int64_t)p_len - Q + qq;
+          a.scores[((int64_t)p_seq * Q + qq) * a.ld + i_g] =
+              (i_g <= p) ? __uint_as_float(d[qq]) : -INFINITY;
+        }
+      }
+      mxq::tc_fence_before();
+      return true;
+    };
+
     for (int kk = 0; kk < n; ++kk) {
       const int st = kk % S, round = kk / S;
       bool landed = false;
@@ -196,91 +319,79 @@ struct MxqFmt {
         if (!landed && *ring.abort_flag) break;
       }
       if (!mxq::all_consumers(landed)) {
-        if (tid == 0) flag(a.status, MX4_STATUS_TIMEOUT);
-        *ring.abort_flag = 1;
+        failed = true;
         break;
       }
+      // the producer's 8-byte copies and bulk copies are visible from here; make
+      // them visible to the tensor core's reads too
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
       const int seq = ring.seq[st], pg = ring.page[st], L = ring.len[st];
       const bool ok = ring.ok[st] != 0;
-      const uint8_t* page = ring.base + st * ring.stage_bytes;
-      if (ok) {
-        if (seq != cur_seq) {
-          set_queries<Q>(reinterpret_cast<const uint16_t*>(page + kPageBytes), region, tm, tid,
-                         warp, lane);
-          cur_seq = seq;
-        }
-        // page rows -> A tile: 16-byte piece p (row p/4, K-chunks 2(p%4), 2(p%4)+1)
-#pragma unroll
-        for (int it = 0; it < 4; ++it) {
-          const int p = it * 128 + tid, r = p >> 2, c = p & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(page + p * 16);
-          uint8_t* dst = atile + (r >> 3) * 1024 + (2 * c) * 128 + (r & 7) * 16;
-          *reinterpret_cast<uint2*>(dst) = make_uint2(v.x, v.y);
-          *reinterpret_cast<uint2*>(dst + 128) = make_uint2(v.z, v.w);
-        }
-        // this lane quarter's scale words: row 32*warp + lane at column kColSfa + warp
-        const uint32_t sw =
-            *reinterpret_cast<const uint32_t*>(page + kScaleOffset + 4 * (32 * warp + lane));
-        mxq::tmem_st1(lane_base + mxq::kColSfa + warp, sw);
-        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-      }
-      mxq::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(smem_addr(&ring.empty[st]));  // the page is copied out
-      if (!ok) continue;
-      mxq::named_sync();
-      if (tid == 0) {
-        mxq::tc_fence_after();
-#pragma unroll
-        for (uint32_t kb = 0; kb < 4; ++kb) {
-          const uint64_t ad = mxq::smem_desc(a_addr + kb * 256, 128, 1024);
-          const uint64_t bd = mxq::smem_desc(b_addr + kb * 256, 128, 1024);
-          asm volatile(
-              "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
-              " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, "
-              "%3, [%4], [%5], p;\n}\n" ::"r"(tm + mxq::kColD),
-              "l"(ad), "l"(bd), "r"(mxq::idesc(kb)), "r"(tm + mxq::kColSfa),
-              "r"(tm + mxq::kColSfb), "r"(kb)
-              : "memory");
-        }
-        asm volatile(
-            "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
-                bar)
-            : "memory");
-      }
-      mma_pending = true;
-      const bool done = mbar_wait(bar, mma_phase);
-      if (!mxq::all_consumers(done)) {
-        if (tid == 0) flag(a.status, MX4_STATUS_TIMEOUT);
-        *ring.abort_flag = 1;
+      const uint8_t* stage = ring.base + st * ring.stage_bytes;
+      if (ok && seq != cur_seq && pending && !read_back()) {  // the B tile is about to change
+        failed = true;
         break;
       }
-      mma_pending = false;
-      mma_phase ^= 1u;
-      mxq::tc_fence_after();
-      uint32_t d[8];
-      asm volatile(
-          "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];\n"
-          : "=r"(d[0]), "=r"(d[1]), "=r"(d[2]), "=r"(d[3]), "=r"(d[4]), "=r"(d[5]), "=r"(d[6]),
-            "=r"(d[7])
-          : "r"(lane_base + mxq::kColD)
-          : "memory");
-      asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-      const int row = 32 * warp + lane;
-      const int64_t i_g = (int64_t)pg * kPageTokens + row;
-      if (i_g < L) {
-#pragma unroll
-        for (int qq = 0; qq < Q; ++qq) {
-          const int64_t p = (int64_t)L - Q + qq;
-          a.scores[((int64_t)seq * Q + qq) * a.ld + i_g] =
-              (i_g <= p) ? __uint_as_float(d[qq]) : -INFINITY;
+      if (ok) {
+        if (seq != cur_seq) {
+          set_queries<Q>(reinterpret_cast<const uint16_t*>(stage + kStageDataBytes), region, tm,
+                         tid, warp, lane);
+          cur_seq = seq;
         }
+        const uint32_t buf = groups & 1u;
+        // this lane quarter's key scale words: row 32*warp + lane, column + warp
+        const uint32_t sw =
+            *reinterpret_cast<const uint32_t*>(stage + mxq::kATileBytes + 4 * (32 * warp + lane));
+        mxq::tmem_st1(lane_base + mxq::kColSfa + 4u * buf + warp, sw);
+        asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+        mxq::tc_fence_before();
+        mxq::named_sync();
+        if (tid == 0) {
+          mxq::tc_fence_after();
+          const uint32_t a_addr = smem_addr(stage);
+#pragma unroll
+          for (uint32_t kb = 0; kb < 4; ++kb) {
+            const uint64_t ad = mxq::smem_desc(a_addr + kb * 256, 128, 1024);
+            const uint64_t bd = mxq::smem_desc(b_addr + kb * 256, 128, 1024);
+            asm volatile(
+                "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
+                " tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, "
+                "%2, %3, [%4], [%5], p;\n}\n" ::"r"(tm + mxq::kColD + 16u * buf),
+                "l"(ad), "l"(bd), "r"(mxq::idesc(kb)), "r"(tm + mxq::kColSfa + 4u * buf),
+                "r"(tm + mxq::kColSfb), "r"(kb)
+                : "memory");
+          }
+          mxq::commit(smem_addr(&mma_bar[buf]));
+          mxq::commit(smem_addr(&ring.empty[st]));  // the stage is free once the group is done
+        }
+        ++groups;
+        running |= 1u << buf;
+      } else if (tid == 0) {
+        mbar_arrive(smem_addr(&ring.empty[st]));
       }
-      mxq::tc_fence_before();
+      if (pending && !read_back()) {
+        failed = true;
+        break;
+      }
+      if (ok) {
+        pending = true;
+        p_seq = seq;
+        p_pg = pg;
+        p_len = L;
+        p_buf = (groups - 1u) & 1u;
+      }
     }
-    // teardown: every consumer gets here (the loop's exits are taken by all 128)
-    if (mma_pending && !mbar_wait(bar, mma_phase) && tid == 0) flag(a.status, MX4_STATUS_TIMEOUT);
+    if (!failed && pending && !read_back()) failed = true;
+    if (failed) {
+      if (tid == 0) flag(a.status, MX4_STATUS_TIMEOUT);
+      *ring.abort_flag = 1;
+    }
+    // teardown (every consumer gets here): no MMA group may still run when the
+    // tensor memory is freed (a buffer holds at most one group not waited for)
+    for (uint32_t b = 0; b < 2; ++b)
+      if (((running >> b) & 1u) && !mbar_wait(smem_addr(&mma_bar[b]), (phases >> b) & 1u) &&
+          tid == 0)
+        flag(a.status, MX4_STATUS_TIMEOUT);
     mxq::tc_fence_before();
     mxq::named_sync();
     mxq::tc_fence_after();

@@ -19,9 +19,11 @@
 // MX4_STATUS_TIMEOUT, stops, and drains the copies in flight before exiting.
 //
 // A format whose tile math takes a whole page at once (kWholePage: the
-// block-scaled tensor-core scorer) gets the stage ring and a region of
-// kExtraBytes of shared memory for its operand tiles, and runs its own consumer
-// loop over the same stages.
+// block-scaled tensor-core scorer) gets a region of kExtraBytes of shared memory
+// for its operand tiles and runs its own producer and consumer loops over the
+// same stage ring, prefix scan, page resolution and drain.  A format sets the
+// bytes of a stage before the index-q rows (kStageDataBytes) and the arrival
+// counts of its full and empty barriers.
 #pragma once
 
 #include "common.cuh"
@@ -56,7 +58,7 @@ struct ScoreArgs {
 // barriers | stage info | warp sums, flags | per-sequence page prefix [B].
 template <class F, int Q>
 struct ScoreLayout {
-  static constexpr int kStageBytes = F::kPageBytes + Q * kHeadDim * 2;
+  static constexpr int kStageBytes = F::kStageDataBytes + Q * kHeadDim * 2;
   static_assert(kStageBytes % 16 == 0, "bulk-copy alignment");
   static_assert(F::kExtraBytes % 128 == 0, "format region alignment");
   static constexpr int kStagesOff = F::kExtraBytes;
@@ -68,20 +70,45 @@ struct ScoreLayout {
   static size_t bytes(int B) { return (size_t)kPrefOff + (size_t)B * 4; }
 };
 
-// The stage ring as a whole-page consumer sees it: stage st holds a page (and the
-// sequence's index-q rows after it) once full[st] completes its phase; the
-// consumer arrives on empty[st] (one arrival per consumer warp) to free it.
+// The stage ring as a whole-page format sees it: stage st holds a page (and the
+// sequence's index-q rows after kStageDataBytes) once full[st] completes its
+// phase; the consumer frees it with the format's arrivals on empty[st].
 struct StageRing {
   uint8_t* base;
   int stage_bytes;
   uint64_t* full;
   uint64_t* empty;
-  const int* seq;
-  const int* page;
-  const int* len;
-  const int* ok;
+  int* seq;
+  int* page;
+  int* len;
+  int* ok;
   volatile int* abort_flag;
+  int* issued;  // stages the producer has filled (for the drain)
 };
+
+// Page P of the flattened page list: its sequence, its page number within the
+// sequence, the sequence's length and its address.  ok = 0 (and the status bit
+// set) for a page id outside the pool.
+struct PageRef {
+  const uint8_t* src;
+  int seq, page, len, ok;
+};
+__device__ __forceinline__ PageRef resolve_page(const ScoreArgs& a, const int* pref, int P) {
+  int lo = 0, hi = a.B - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (pref[mid] > P) hi = mid; else lo = mid + 1;
+  }
+  PageRef r;
+  r.seq = lo;
+  r.page = P - (lo > 0 ? pref[lo - 1] : 0);
+  r.len = a.seq_lens[lo];
+  const int32_t pid = a.block_table[(int64_t)lo * a.bt_width + r.page];
+  r.ok = (pid >= 0 && pid < a.num_pages) ? 1 : 0;
+  if (!r.ok) flag(a.status, MX4_STATUS_BAD_PAGE);
+  r.src = r.ok ? a.pages + (int64_t)pid * a.page_stride : a.pages;
+  return r;
+}
 
 template <class F, int Q>
 __global__ void __launch_bounds__((F::kConsumers + 1) * 32, F::ctas_per_sm(Q))
@@ -133,8 +160,8 @@ score_kernel(const ScoreArgs a) {
   }
   if (tid == 0) {
     for (int i = 0; i < S; ++i) {
-      mbar_init(smem_addr(&full[i]), 1);
-      mbar_init(smem_addr(&empty[i]), NC);
+      mbar_init(smem_addr(&full[i]), F::kFullCount);
+      mbar_init(smem_addr(&empty[i]), F::kEmptyCount);
     }
     *abort_flag = 0;
     *issued = 0;
@@ -148,57 +175,50 @@ score_kernel(const ScoreArgs a) {
   const int p0 = (int)((int64_t)total * blockIdx.x / G);
   const int n = (int)((int64_t)total * (blockIdx.x + 1) / G) - p0;
 
+  const StageRing ring{smem_raw + Lay::kStagesOff, Lay::kStageBytes, full, empty, info_seq,
+                       info_page, info_len, info_ok, abort_flag, issued};
   if (warp == NC) {
     // ================= producer
-    for (int base = 0; base < n; base += 32) {
-      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
-      const int k = base + lane;
-      int seqk = -1, jk = 0, lenk = 0, okk = 0;
-      const uint8_t* src = a.pages;
-      if (k < n) {
-        const int P = p0 + k;
-        int lo = 0, hi = B - 1;
-        while (lo < hi) {
-          const int mid = (lo + hi) >> 1;
-          if (pref[mid] > P) hi = mid; else lo = mid + 1;
-        }
-        seqk = lo;
-        jk = P - (lo > 0 ? pref[lo - 1] : 0);
-        lenk = a.seq_lens[seqk];
-        const int32_t pid = a.block_table[(int64_t)seqk * a.bt_width + jk];
-        okk = (pid >= 0 && pid < a.num_pages) ? 1 : 0;
-        if (!okk) flag(a.status, MX4_STATUS_BAD_PAGE);
-        else src = a.pages + (int64_t)pid * a.page_stride;
-      }
-      const int cnt = min(32, n - base);
-      for (int l = 0; l < cnt; ++l) {
-        if (lane == l) {
-          const int kk = base + l, st = kk % S, round = kk / S;
-          bool go = !*abort_flag;
-          if (go && round > 0 && !mbar_wait(smem_addr(&empty[st]), (round - 1) & 1)) {
-            flag(a.status, MX4_STATUS_TIMEOUT);
-            *abort_flag = 1;
-            go = false;
-          }
-          if (go) {
-            info_seq[st] = seqk;
-            info_page[st] = jk;
-            info_len[st] = lenk;
-            info_ok[st] = okk;
-            const uint32_t fb = smem_addr(&full[st]);
-            const uint32_t dst = smem_addr(smem_raw + Lay::kStagesOff + st * Lay::kStageBytes);
-            if (okk) {
-              mbar_arrive_expect_tx(fb, F::kPageBytes + Q * kHeadDim * 2);
-              bulk_copy_g2s(dst, src, F::kPageBytes, fb);
-              bulk_copy_g2s(dst + F::kPageBytes, a.iq + (int64_t)seqk * Q * kHeadDim,
-                            Q * kHeadDim * 2, fb);
-            } else {
-              mbar_arrive(fb);
+    if constexpr (F::kWholePage) {
+      F::template produce<Q>(a, ring, pref, p0, n, lane);
+    } else {
+      for (int base = 0; base < n; base += 32) {
+        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
+        const int k = base + lane;
+        PageRef pr{a.pages, -1, 0, 0, 0};
+        if (k < n) pr = resolve_page(a, pref, p0 + k);
+        const int seqk = pr.seq, jk = pr.page, lenk = pr.len, okk = pr.ok;
+        const uint8_t* src = pr.src;
+        const int cnt = min(32, n - base);
+        for (int l = 0; l < cnt; ++l) {
+          if (lane == l) {
+            const int kk = base + l, st = kk % S, round = kk / S;
+            bool go = !*abort_flag;
+            if (go && round > 0 && !mbar_wait(smem_addr(&empty[st]), (round - 1) & 1)) {
+              flag(a.status, MX4_STATUS_TIMEOUT);
+              *abort_flag = 1;
+              go = false;
             }
-            *issued = kk + 1;
+            if (go) {
+              info_seq[st] = seqk;
+              info_page[st] = jk;
+              info_len[st] = lenk;
+              info_ok[st] = okk;
+              const uint32_t fb = smem_addr(&full[st]);
+              const uint32_t dst = smem_addr(smem_raw + Lay::kStagesOff + st * Lay::kStageBytes);
+              if (okk) {
+                mbar_arrive_expect_tx(fb, F::kPageBytes + Q * kHeadDim * 2);
+                bulk_copy_g2s(dst, src, F::kPageBytes, fb);
+                bulk_copy_g2s(dst + F::kPageBytes, a.iq + (int64_t)seqk * Q * kHeadDim,
+                              Q * kHeadDim * 2, fb);
+              } else {
+                mbar_arrive(fb);
+              }
+              *issued = kk + 1;
+            }
           }
+          __syncwarp();
         }
-        __syncwarp();
       }
     }
     // Drain: wait (bounded) until the copies of the last stages issued have landed,
@@ -214,8 +234,6 @@ score_kernel(const ScoreArgs a) {
 
   // ================= consumers
   if constexpr (F::kWholePage) {
-    const StageRing ring{smem_raw + Lay::kStagesOff, Lay::kStageBytes, full, empty, info_seq,
-                         info_page, info_len, info_ok, abort_flag};
     F::template consume<Q>(a, ring, smem_raw, n, warp, lane);
   } else {
     typename F::template Tile<Q> tile;
