@@ -378,6 +378,46 @@ int mx4_decode_step(const void *h_inputs, int64_t n_new, void *d_staging, size_t
                     void *stream);
 
 /* ---------------------------------------------------------------------------
+ * mx4_decode_steps -- n_steps decode steps in order, host memory to host
+ * memory, with the copies of neighbouring steps overlapping the compute: step
+ * i's inputs go to the device on h2d_stream while step i-1 computes on
+ * `stream`, and step i's output comes back on d2h_stream while step i+1
+ * computes.  Each step is exactly mx4_decode_step (insert, index_topk,
+ * sparse_paged_decode on the shared page caches, in step order, so every
+ * step's insert lands before the next step reads the caches).
+ *
+ *   h_inputs   HOST packed inputs of step i at h_inputs + i * h_inputs_stride
+ *              (stride 0: the same inputs every step); page-locked memory is
+ *              needed for the copies to overlap
+ *   d_staging  DEVICE, two input sets: set b at d_staging + b * S, S =
+ *              mx4_decode_step_input_bytes(T, n_new) rounded up to 256;
+ *              staging_bytes >= 2 * S, 256-byte aligned
+ *   d_out      DEVICE fp32, two output sets [2][T, 16, 128]
+ *   h_out      HOST fp32: step i's output [T, 16, 128] at byte offset
+ *              i * h_out_stride (stride 0: every step into the same buffer, in
+ *              step order)
+ *   stream, h2d_stream, d2h_stream  the compute stream (may be the default
+ *              stream) and two copy streams for the inputs and the outputs, of
+ *              the caller: distinct, the copy streams not the default stream
+ *   the rest   as mx4_decode_step (one set of scores, top-k indices and
+ *              workspaces, reused by every step)
+ * The copies start after the work already on `stream`, and `stream` waits for
+ * the last copy at the end: once `stream` reaches this point every h_out
+ * holds its step's result.  The call returns without waiting; it creates and
+ * releases its own events.  Errors as mx4_decode_step, checked for both sets
+ * before anything is enqueued; MX4_ERR_INVALID for missing or equal streams.
+ * ------------------------------------------------------------------------- */
+int mx4_decode_steps(int64_t n_steps, const void *h_inputs, size_t h_inputs_stride,
+                     int64_t n_new, void *d_staging, size_t staging_bytes, uint8_t *k_pages,
+                     uint8_t *v_pages, int64_t kv_page_stride, int64_t kv_head_stride,
+                     uint8_t *idx_pages, int64_t idx_page_stride, int64_t num_pages,
+                     const int32_t *block_table, int64_t B, int64_t bt_width,
+                     const int32_t *seq_lens, int q_per_seq, int k, float scale, float *d_scores,
+                     int64_t ld_scores, int32_t *d_topk_idx, void *topk_ws, size_t topk_ws_bytes,
+                     void *dec_ws, size_t dec_ws_bytes, float *d_out, float *h_out,
+                     size_t h_out_stride, void *stream, void *h2d_stream, void *d2h_stream);
+
+/* ---------------------------------------------------------------------------
  * mx4_check_status -- synchronise `stream`, return MX4_OK if no kernel of this
  * library has flagged bad data on the current device since the last check,
  * else MX4_ERR_BOUNDS with the flagged MX4_STATUS_* bits in *bits (if bits is

@@ -21,7 +21,7 @@ import torch
 __all__ = ["mx4_insert", "mx4_norm_rope_insert", "fp8_index_insert", "index_score_fp8", "index_score", "index_score_mxq",
            "index_topk", "index_topk_workspace", "topk_select", "sparse_paged_decode",
            "topk_select_workspace", "sparse_paged_decode_workspace", "mx4_check_status",
-           "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "mx4_decode_step",
+           "sparse_paged_decode_noalloc", "NOALLOC_SCRATCH_BYTES", "mx4_decode_step", "mx4_decode_steps",
            "mx4_decode_step_input_layout",
            "mx4_last_error", "mx4_page_bytes", "library_path", "Mx4Error", "PAGE_BYTES",
            "PAGE_TOKENS", "HEAD_DIM"]
@@ -107,6 +107,10 @@ def _load():
         lib.mx4_decode_step.argtypes = [P, i64, P, sz, P, P, i64, i64, P, i64, i64, P, i64, i64,
                                         P, i32, i32, ctypes.c_float, P, i64, P, P, sz, P, sz, P,
                                         P, P]
+        lib.mx4_decode_steps.restype = i32
+        lib.mx4_decode_steps.argtypes = [i64, P, sz, i64, P, sz, P, P, i64, i64, P, i64, i64, P,
+                                         i64, i64, P, i32, i32, ctypes.c_float, P, i64, P, P, sz,
+                                         P, sz, P, P, sz, P, P, P]
         lib.mx4_check_status.restype = i32
         lib.mx4_check_status.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
         _lib = lib
@@ -444,16 +448,10 @@ def mx4_decode_step_input_layout(T, n_new):
     return [int(x) for x in off], int(_load().mx4_decode_step_input_bytes(int(T), int(n_new)))
 
 
-def mx4_decode_step(h_inputs, n_new, d_staging, k_pages, v_pages, idx_pages, block_table,
-                    seq_lens, q_per_seq, k, scale, d_scores, d_topk_idx, topk_ws, dec_ws, d_out,
-                    h_out, stream=None):
-    """One decode step from host memory to host memory: copy the packed host inputs
-    (uint8 CPU tensor, layout mx4_decode_step_input_layout) to d_staging, insert the
-    n_new new tokens, score, select, attend, and copy the output (fp32 [T, 16, 128])
-    into the host tensor h_out.  Asynchronous on `stream`."""
-    _need(h_inputs, torch.uint8, "h_inputs")
-    _need(h_out, torch.float32, "h_out")
-    _need(d_staging, torch.uint8, "d_staging")
+def _step_args(n_new, k_pages, v_pages, idx_pages, block_table, seq_lens, q_per_seq, k, scale,
+               d_scores, d_topk_idx, topk_ws, dec_ws, d_out, out_sets):
+    """Checks shared by the step entry points; returns (T, the marshalled cache,
+    table and workspace arguments between the staging size and d_out)."""
     _need(block_table, torch.int32, "block_table")
     _need(seq_lens, torch.int32, "seq_lens")
     _need(d_scores, torch.float32, "d_scores")
@@ -466,24 +464,83 @@ def mx4_decode_step(h_inputs, n_new, d_staging, k_pages, v_pages, idx_pages, blo
         raise ValueError("k_pages and v_pages must have the same shape and strides")
     B = int(seq_lens.shape[0])
     T = B * int(q_per_seq)
-    _, nbytes = mx4_decode_step_input_layout(T, n_new)
-    if h_inputs.numel() < nbytes or d_staging.numel() < nbytes:
-        raise ValueError(f"input buffers need {nbytes} bytes")
-    _dims(h_out, "h_out", T, 16, HEAD_DIM)
-    _dims(d_out, "d_out", T, 16, HEAD_DIM)
+    if out_sets == 1:
+        _dims(d_out, "d_out", T, 16, HEAD_DIM)
+    else:
+        _dims(d_out, "d_out", out_sets, T, 16, HEAD_DIM)
     _dims(d_topk_idx, "d_topk_idx", T, int(k))
     _dims(d_scores, "d_scores", None, None)
     _rows_at_least(d_scores, T, "d_scores")
     _rows_at_least(block_table, B, "block_table")
     tws = 0 if topk_ws is None else topk_ws.numel() * topk_ws.element_size()
+    args = (_ptr(k_pages), _ptr(v_pages), k_pages.stride(0), k_pages.stride(1), _ptr(idx_pages),
+            idx_pages.stride(0), int(k_pages.shape[0]), _ptr(block_table), B,
+            int(block_table.shape[1]), _ptr(seq_lens), int(q_per_seq), int(k), float(scale),
+            _ptr(d_scores), d_scores.stride(0), _ptr(d_topk_idx), _ptr(topk_ws), tws,
+            _ptr(dec_ws), dec_ws.numel() * dec_ws.element_size())
+    return T, args
+
+
+def mx4_decode_step(h_inputs, n_new, d_staging, k_pages, v_pages, idx_pages, block_table,
+                    seq_lens, q_per_seq, k, scale, d_scores, d_topk_idx, topk_ws, dec_ws, d_out,
+                    h_out, stream=None):
+    """One decode step from host memory to host memory: copy the packed host inputs
+    (uint8 CPU tensor, layout mx4_decode_step_input_layout) to d_staging, insert the
+    n_new new tokens, score, select, attend, and copy the output (fp32 [T, 16, 128])
+    into the host tensor h_out.  Asynchronous on `stream`."""
+    _need(h_inputs, torch.uint8, "h_inputs")
+    _need(h_out, torch.float32, "h_out")
+    _need(d_staging, torch.uint8, "d_staging")
+    T, args = _step_args(n_new, k_pages, v_pages, idx_pages, block_table, seq_lens, q_per_seq,
+                         k, scale, d_scores, d_topk_idx, topk_ws, dec_ws, d_out, 1)
+    _, nbytes = mx4_decode_step_input_layout(T, n_new)
+    if h_inputs.numel() < nbytes or d_staging.numel() < nbytes:
+        raise ValueError(f"input buffers need {nbytes} bytes")
+    _dims(h_out, "h_out", T, 16, HEAD_DIM)
     _check(_load().mx4_decode_step(
-        _host_ptr(h_inputs, "h_inputs"), int(n_new), _ptr(d_staging), d_staging.numel(),
-        _ptr(k_pages), _ptr(v_pages), k_pages.stride(0), k_pages.stride(1), _ptr(idx_pages),
-        idx_pages.stride(0), int(k_pages.shape[0]), _ptr(block_table), B,
-        int(block_table.shape[1]), _ptr(seq_lens), int(q_per_seq), int(k), float(scale),
-        _ptr(d_scores), d_scores.stride(0), _ptr(d_topk_idx), _ptr(topk_ws), tws, _ptr(dec_ws),
-        dec_ws.numel() * dec_ws.element_size(), _ptr(d_out), _host_ptr(h_out, "h_out"),
-        _stream(stream)))
+        _host_ptr(h_inputs, "h_inputs"), int(n_new), _ptr(d_staging), d_staging.numel(), *args,
+        _ptr(d_out), _host_ptr(h_out, "h_out"), _stream(stream)))
+
+
+def mx4_decode_steps(n_steps, h_inputs, n_new, d_staging, k_pages, v_pages, idx_pages,
+                     block_table, seq_lens, q_per_seq, k, scale, d_scores, d_topk_idx, topk_ws,
+                     dec_ws, d_out, h_out, stream, h2d_stream, d2h_stream, same_inputs=False):
+    """n_steps decode steps in order, host memory to host memory, the copies of
+    neighbouring steps overlapping the compute on two copy streams.  h_inputs: uint8
+    CPU tensor [n_steps, bytes] of packed inputs (or [bytes] with same_inputs=True:
+    the same inputs every step); d_staging: uint8 device buffer of two input sets;
+    d_out: fp32 device [2, T, 16, 128]; h_out: fp32 CPU [n_steps, T, 16, 128] (or
+    [T, 16, 128], every step's output in turn).  Asynchronous on `stream`, which
+    waits for the last output copy."""
+    _need(h_inputs, torch.uint8, "h_inputs")
+    _need(h_out, torch.float32, "h_out")
+    _need(d_staging, torch.uint8, "d_staging")
+    for name, st in (("h2d_stream", h2d_stream), ("d2h_stream", d2h_stream)):
+        if not isinstance(st, torch.cuda.Stream):
+            raise ValueError(f"{name} must be a torch.cuda.Stream")
+    T, args = _step_args(n_new, k_pages, v_pages, idx_pages, block_table, seq_lens, q_per_seq,
+                         k, scale, d_scores, d_topk_idx, topk_ws, dec_ws, d_out, 2)
+    _, nbytes = mx4_decode_step_input_layout(T, n_new)
+    set_bytes = (nbytes + 255) // 256 * 256
+    n_steps = int(n_steps)
+    if same_inputs:
+        _dims(h_inputs, "h_inputs", None)
+        in_stride = 0
+    else:
+        _dims(h_inputs, "h_inputs", n_steps, None)
+        in_stride = int(h_inputs.shape[1])
+    if h_inputs.shape[-1] < nbytes or d_staging.numel() < 2 * set_bytes:
+        raise ValueError(f"h_inputs rows need {nbytes} bytes, d_staging {2 * set_bytes}")
+    if h_out.dim() == 3:
+        _dims(h_out, "h_out", T, 16, HEAD_DIM)
+        out_stride = 0
+    else:
+        _dims(h_out, "h_out", n_steps, T, 16, HEAD_DIM)
+        out_stride = T * 16 * HEAD_DIM * 4
+    _check(_load().mx4_decode_steps(
+        n_steps, _host_ptr(h_inputs, "h_inputs"), in_stride, int(n_new), _ptr(d_staging),
+        d_staging.numel(), *args, _ptr(d_out), _host_ptr(h_out, "h_out"), out_stride,
+        _stream(stream), _stream(h2d_stream), _stream(d2h_stream)))
 
 
 def mx4_check_status(stream=None) -> int:

@@ -553,6 +553,97 @@ extern "C" size_t mx4_decode_step_input_bytes(int64_t T, int64_t n_new) {
   return std::max<size_t>(256, off[5] + align256(n_ * 8));
 }
 
+namespace {
+
+// The arguments of one decode step that stay the same from step to step.
+struct StepCfg {
+  int64_t n_new;
+  uint8_t* k_pages;
+  uint8_t* v_pages;
+  int64_t kv_page_stride, kv_head_stride;
+  uint8_t* idx_pages;
+  int64_t idx_page_stride, num_pages;
+  const int32_t* block_table;
+  int64_t B, bt_width;
+  const int32_t* seq_lens;
+  int q_per_seq, k;
+  float scale;
+  float* d_scores;
+  int64_t ld_scores;
+  int32_t* d_topk_idx;
+  void* topk_ws;
+  size_t topk_ws_bytes;
+  void* dec_ws;
+  size_t dec_ws_bytes;
+};
+
+// Validation of a step whose packed inputs sit at `staging` (`staging_bytes`
+// available) and whose output goes to d_out; nothing is enqueued.
+int step_check(const char* name, const StepCfg& c, const void* staging, size_t staging_bytes,
+               const float* d_out) {
+  if (c.q_per_seq < 1 || c.q_per_seq > 8)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: q_per_seq = %d", name, c.q_per_seq);
+  if (c.B < 0 || c.B > 65535)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: B = %lld", name, (long long)c.B);
+  if (c.n_new < 0) return fail(MX4_ERR_INVALID, "%s: n_new < 0", name);
+  const int64_t T = c.B * c.q_per_seq;
+  const size_t in_bytes = mx4_decode_step_input_bytes(T, c.n_new);
+  if (!staging) return fail(MX4_ERR_INVALID, "%s: NULL staging buffer", name);
+  if (staging_bytes < in_bytes)
+    return fail(MX4_ERR_WORKSPACE, "%s: staging %zu < %zu bytes", name, staging_bytes, in_bytes);
+  if (!aligned(staging, 256))
+    return fail(MX4_ERR_INVALID, "%s: staging buffer must be 256-byte aligned", name);
+  size_t off[6];
+  mx4_decode_step_input_offsets(T, c.n_new, off);
+  const uint8_t* st = static_cast<const uint8_t*>(staging);
+  if (int rc = check_decode_sizes(name, T, c.q_per_seq, 16, 1, c.B, c.k, c.scale)) return rc;
+  if (T > 0)
+    if (int rc = check_decode_pointers(
+            name, reinterpret_cast<const uint16_t*>(st + off[0]), c.k_pages, c.v_pages,
+            c.kv_page_stride, c.kv_head_stride, c.num_pages, c.block_table, c.bt_width,
+            c.seq_lens, c.d_topk_idx, d_out))
+      return rc;
+  if (T > 65535 || (c.ld_scores + 16383) / 16384 > 512)
+    return fail(MX4_ERR_UNSUPPORTED, "%s: T = %lld or ld_scores = %lld beyond topk_select's limits",
+                name, (long long)T, (long long)c.ld_scores);
+  if (!c.idx_pages || !c.d_scores || c.idx_page_stride % 16 || !aligned(c.idx_pages, 16) ||
+      c.idx_page_stride < mx4::kPageBytes || c.ld_scores < 1)
+    return fail(MX4_ERR_INVALID, "%s: index pages, page stride or scores", name);
+  if (c.topk_ws_bytes < index_topk_workspace(T, c.k, c.ld_scores) ||
+      c.dec_ws_bytes < sparse_paged_decode_workspace(T, c.k))
+    return fail(MX4_ERR_WORKSPACE, "%s: a workspace is too small", name);
+  return MX4_OK;
+}
+
+// The device part of a step whose packed inputs are already at `staging`:
+// insert, score + select, decode into d_out, on `stream`.
+int step_compute(const StepCfg& c, uint8_t* staging, float* d_out, void* stream) {
+  const int64_t T = c.B * c.q_per_seq;
+  size_t off[6];
+  mx4_decode_step_input_offsets(T, c.n_new, off);
+  const uint16_t* q = reinterpret_cast<const uint16_t*>(staging + off[0]);
+  const uint16_t* iq = reinterpret_cast<const uint16_t*>(staging + off[1]);
+  const float* k_new = reinterpret_cast<const float*>(staging + off[2]);
+  const float* v_new = reinterpret_cast<const float*>(staging + off[3]);
+  const float* idx_new = reinterpret_cast<const float*>(staging + off[4]);
+  const int64_t* slots = reinterpret_cast<const int64_t*>(staging + off[5]);
+  if (c.n_new > 0)
+    if (int rc = mx4_insert(k_new, v_new, idx_new, c.n_new, 1, slots, c.k_pages, c.v_pages,
+                            c.kv_page_stride, c.kv_head_stride, c.idx_pages, c.idx_page_stride,
+                            c.num_pages, stream))
+      return rc;
+  if (int rc = index_topk(iq, T, c.q_per_seq, c.idx_pages, c.idx_page_stride, c.num_pages,
+                          c.block_table, c.B, c.bt_width, c.seq_lens, c.d_scores, c.ld_scores,
+                          c.k, c.d_topk_idx, c.topk_ws, c.topk_ws_bytes, stream))
+    return rc;
+  return sparse_paged_decode(q, T, c.q_per_seq, 16, 1, c.k_pages, c.v_pages, c.kv_page_stride,
+                             c.kv_head_stride, c.num_pages, c.block_table, c.B, c.bt_width,
+                             c.seq_lens, c.d_topk_idx, c.k, c.scale, d_out, c.dec_ws,
+                             c.dec_ws_bytes, stream);
+}
+
+}  // namespace
+
 extern "C" int mx4_decode_step(const void* h_inputs, int64_t n_new, void* d_staging,
                                size_t staging_bytes, uint8_t* k_pages, uint8_t* v_pages,
                                int64_t kv_page_stride, int64_t kv_head_stride,
@@ -563,63 +654,124 @@ extern "C" int mx4_decode_step(const void* h_inputs, int64_t n_new, void* d_stag
                                void* topk_ws, size_t topk_ws_bytes, void* dec_ws,
                                size_t dec_ws_bytes, float* d_out, float* h_out, void* stream) {
   static const char* kName = "mx4_decode_step";
-  if (q_per_seq < 1 || q_per_seq > 8)
-    return fail(MX4_ERR_UNSUPPORTED, "%s: q_per_seq = %d", kName, q_per_seq);
-  if (B < 0 || B > 65535) return fail(MX4_ERR_UNSUPPORTED, "%s: B = %lld", kName, (long long)B);
-  if (n_new < 0) return fail(MX4_ERR_INVALID, "%s: n_new < 0", kName);
+  const StepCfg c{n_new,    k_pages,     v_pages,   kv_page_stride, kv_head_stride,
+                  idx_pages, idx_page_stride, num_pages, block_table,   B,
+                  bt_width, seq_lens,    q_per_seq, k,              scale,
+                  d_scores, ld_scores,   d_topk_idx, topk_ws,       topk_ws_bytes,
+                  dec_ws,   dec_ws_bytes};
+  if (q_per_seq >= 1 && q_per_seq <= 8 && B == 0 && n_new == 0) return ok();
+  if (!h_inputs || !h_out) return fail(MX4_ERR_INVALID, "%s: NULL pointer", kName);
+  if (int rc = step_check(kName, c, d_staging, staging_bytes, d_out)) return rc;
   const int64_t T = B * q_per_seq;
-  const size_t in_bytes = mx4_decode_step_input_bytes(T, n_new);
-  if (T == 0 && n_new == 0) return ok();
-  if (!h_inputs || !d_staging || !h_out) return fail(MX4_ERR_INVALID, "%s: NULL pointer", kName);
-  if (staging_bytes < in_bytes)
-    return fail(MX4_ERR_WORKSPACE, "%s: staging %zu < %zu bytes", kName, staging_bytes, in_bytes);
-  if (!aligned(d_staging, 256))
-    return fail(MX4_ERR_INVALID, "%s: staging buffer must be 256-byte aligned", kName);
-  size_t off[6];
-  mx4_decode_step_input_offsets(T, n_new, off);
-  uint8_t* st = static_cast<uint8_t*>(d_staging);
-  const uint16_t* q = reinterpret_cast<const uint16_t*>(st + off[0]);
-  const uint16_t* iq = reinterpret_cast<const uint16_t*>(st + off[1]);
-  const float* k_new = reinterpret_cast<const float*>(st + off[2]);
-  const float* v_new = reinterpret_cast<const float*>(st + off[3]);
-  const float* idx_new = reinterpret_cast<const float*>(st + off[4]);
-  const int64_t* slots = reinterpret_cast<const int64_t*>(st + off[5]);
-  // validate every stage before anything is enqueued
-  if (int rc = check_decode_sizes(kName, T, q_per_seq, 16, 1, B, k, scale)) return rc;
-  if (T > 0)
-    if (int rc = check_decode_pointers(kName, q, k_pages, v_pages, kv_page_stride,
-                                       kv_head_stride, num_pages, block_table, bt_width,
-                                       seq_lens, d_topk_idx, d_out))
-      return rc;
-  if (T > 65535 || (ld_scores + 16383) / 16384 > 512)
-    return fail(MX4_ERR_UNSUPPORTED, "%s: T = %lld or ld_scores = %lld beyond topk_select's limits",
-                kName, (long long)T, (long long)ld_scores);
-  if (!idx_pages || !d_scores || idx_page_stride % 16 || !aligned(idx_pages, 16) ||
-      idx_page_stride < mx4::kPageBytes || ld_scores < 1)
-    return fail(MX4_ERR_INVALID, "%s: index pages, page stride or scores", kName);
-  if (topk_ws_bytes < index_topk_workspace(T, k, ld_scores) ||
-      dec_ws_bytes < sparse_paged_decode_workspace(T, k))
-    return fail(MX4_ERR_WORKSPACE, "%s: a workspace is too small", kName);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t e = cudaMemcpyAsync(d_staging, h_inputs, in_bytes, cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaMemcpyAsync(d_staging, h_inputs, mx4_decode_step_input_bytes(T, n_new),
+                                  cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "%s: input copy: %s", kName, cudaGetErrorString(e));
-  if (n_new > 0) {
-    if (int rc = mx4_insert(k_new, v_new, idx_new, n_new, 1, slots, k_pages, v_pages,
-                            kv_page_stride, kv_head_stride, idx_pages, idx_page_stride,
-                            num_pages, stream))
-      return rc;
-  }
-  if (int rc = index_topk(iq, T, q_per_seq, idx_pages, idx_page_stride, num_pages, block_table,
-                          B, bt_width, seq_lens, d_scores, ld_scores, k, d_topk_idx, topk_ws,
-                          topk_ws_bytes, stream))
-    return rc;
-  if (int rc = sparse_paged_decode(q, T, q_per_seq, 16, 1, k_pages, v_pages, kv_page_stride,
-                                   kv_head_stride, num_pages, block_table, B, bt_width, seq_lens,
-                                   d_topk_idx, k, scale, d_out, dec_ws, dec_ws_bytes, stream))
-    return rc;
+  if (int rc = step_compute(c, static_cast<uint8_t*>(d_staging), d_out, stream)) return rc;
   e = cudaMemcpyAsync(h_out, d_out, (size_t)T * 16 * mx4::kHeadDim * sizeof(float),
                       cudaMemcpyDeviceToHost, s);
   if (e != cudaSuccess)
     return fail(MX4_ERR_CUDA, "%s: output copy: %s", kName, cudaGetErrorString(e));
+  return ok();
+}
+
+extern "C" int mx4_decode_steps(int64_t n_steps, const void* h_inputs, size_t h_inputs_stride,
+                                int64_t n_new, void* d_staging, size_t staging_bytes,
+                                uint8_t* k_pages, uint8_t* v_pages, int64_t kv_page_stride,
+                                int64_t kv_head_stride, uint8_t* idx_pages,
+                                int64_t idx_page_stride, int64_t num_pages,
+                                const int32_t* block_table, int64_t B, int64_t bt_width,
+                                const int32_t* seq_lens, int q_per_seq, int k, float scale,
+                                float* d_scores, int64_t ld_scores, int32_t* d_topk_idx,
+                                void* topk_ws, size_t topk_ws_bytes, void* dec_ws,
+                                size_t dec_ws_bytes, float* d_out, float* h_out,
+                                size_t h_out_stride, void* stream, void* h2d_stream,
+                                void* d2h_stream) {
+  static const char* kName = "mx4_decode_steps";
+  const StepCfg c{n_new,    k_pages,     v_pages,   kv_page_stride, kv_head_stride,
+                  idx_pages, idx_page_stride, num_pages, block_table,   B,
+                  bt_width, seq_lens,    q_per_seq, k,              scale,
+                  d_scores, ld_scores,   d_topk_idx, topk_ws,       topk_ws_bytes,
+                  dec_ws,   dec_ws_bytes};
+  if (n_steps < 0) return fail(MX4_ERR_INVALID, "%s: n_steps < 0", kName);
+  if (n_steps == 0 || (q_per_seq >= 1 && q_per_seq <= 8 && B == 0 && n_new == 0)) return ok();
+  if (!h_inputs || !h_out || !d_out) return fail(MX4_ERR_INVALID, "%s: NULL pointer", kName);
+  if (!h2d_stream || !d2h_stream || stream == h2d_stream || stream == d2h_stream ||
+      h2d_stream == d2h_stream)
+    return fail(MX4_ERR_INVALID, "%s: two copy streams, not the default stream, distinct from "
+                "each other and from the compute stream, are needed", kName);
+  const int64_t T = B * q_per_seq;
+  const size_t in_bytes = q_per_seq >= 1 && q_per_seq <= 8 && B >= 0 && n_new >= 0
+                              ? mx4_decode_step_input_bytes(T, n_new)
+                              : 0;
+  const size_t set_bytes = align256(in_bytes);  // staging set b at d_staging + b * set_bytes
+  if (staging_bytes < 2 * set_bytes)
+    return fail(MX4_ERR_WORKSPACE, "%s: staging %zu < 2 x %zu bytes", kName, staging_bytes,
+                set_bytes);
+  uint8_t* stage[2] = {static_cast<uint8_t*>(d_staging),
+                       static_cast<uint8_t*>(d_staging) + set_bytes};
+  const size_t out_elems = (size_t)T * 16 * mx4::kHeadDim;
+  float* out[2] = {d_out, d_out + out_elems};
+  if (!aligned(out[1], 16)) return fail(MX4_ERR_INVALID, "%s: misaligned d_out", kName);
+  for (int b = 0; b < 2; ++b)
+    if (int rc = step_check(kName, c, stage[b], set_bytes, out[b])) return rc;
+
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  cudaStream_t hs = static_cast<cudaStream_t>(h2d_stream);
+  cudaStream_t ds = static_cast<cudaStream_t>(d2h_stream);
+  // events: start, inputs_ready[2], compute_done[2], out_done[2]
+  cudaEvent_t ev[7] = {};
+  int made = 0;
+  cudaError_t e = cudaSuccess;
+  for (; made < 7 && e == cudaSuccess; ++made)
+    e = cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming);
+  auto release = [&]() {
+    for (int i = 0; i < 7; ++i)
+      if (ev[i]) cudaEventDestroy(ev[i]);  // released once the stream reaches them
+  };
+  if (e != cudaSuccess) {
+    release();
+    return fail(MX4_ERR_CUDA, "%s: event: %s", kName, cudaGetErrorString(e));
+  }
+  cudaEvent_t start = ev[0], *inputs_ready = ev + 1, *compute_done = ev + 3, *out_done = ev + 5;
+  // the copies are ordered after the work already on `stream`
+  e = cudaEventRecord(start, cs);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(hs, start, 0);
+  if (e == cudaSuccess) e = cudaStreamWaitEvent(ds, start, 0);
+  int rc = MX4_OK;
+  const uint8_t* hin = static_cast<const uint8_t*>(h_inputs);
+  uint8_t* hout = reinterpret_cast<uint8_t*>(h_out);
+  for (int64_t i = 0; i < n_steps && e == cudaSuccess && rc == MX4_OK; ++i) {
+    const int b = (int)(i & 1);
+    // step i's inputs into set b, once step i-2 has finished computing from it
+    if (i >= 2) e = cudaStreamWaitEvent(hs, compute_done[b], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(stage[b], hin + (size_t)i * h_inputs_stride, in_bytes,
+                          cudaMemcpyHostToDevice, hs);
+    if (e == cudaSuccess) e = cudaEventRecord(inputs_ready[b], hs);
+    // compute once the inputs are in and step i-2's output has been read back
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, inputs_ready[b], 0);
+    if (e == cudaSuccess && i >= 2) e = cudaStreamWaitEvent(cs, out_done[b], 0);
+    if (e != cudaSuccess) break;
+    rc = step_compute(c, stage[b], out[b], stream);
+    if (rc != MX4_OK) break;
+    e = cudaEventRecord(compute_done[b], cs);
+    // read step i's output back
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(ds, compute_done[b], 0);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(hout + (size_t)i * h_out_stride, out[b], out_elems * sizeof(float),
+                          cudaMemcpyDeviceToHost, ds);
+    if (e == cudaSuccess) e = cudaEventRecord(out_done[b], ds);
+  }
+  // `stream` reaches the end of the call only after the last output copy (and so
+  // after every copy of the call, both copy streams being in order)
+  cudaError_t e2 = cudaEventRecord(start, ds);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(cs, start, 0);
+  if (e2 == cudaSuccess) e2 = cudaEventRecord(start, hs);
+  if (e2 == cudaSuccess) e2 = cudaStreamWaitEvent(cs, start, 0);
+  release();
+  if (rc != MX4_OK) return rc;
+  if (e != cudaSuccess) return fail(MX4_ERR_CUDA, "%s: %s", kName, cudaGetErrorString(e));
+  if (e2 != cudaSuccess) return fail(MX4_ERR_CUDA, "%s: %s", kName, cudaGetErrorString(e2));
   return ok();
 }

@@ -20,6 +20,7 @@ import numpy as np
 import torch
 
 from . import (FP8_PAGE_BYTES, fp8_index_insert, index_score, index_topk, mx4_decode_step,
+               mx4_decode_steps,
                mx4_decode_step_input_layout, mx4_insert, sparse_paged_decode,
                sparse_paged_decode_workspace, topk_select, topk_select_workspace)
 from . import workloads as W
@@ -262,6 +263,27 @@ class DecodeStep:
                         c.idx_pages, self.block_table, self.seq_lens, wl.q, wl.k, self.scale,
                         self.scores, self.topk_idx, self.topk_ws, self.dec_ws, self.out, h_out,
                         stream=stream)
+
+    def run_host_steps(self, h_inputs: torch.Tensor, h_out: torch.Tensor, n_steps: int,
+                       stream: torch.cuda.Stream, h2d: torch.cuda.Stream,
+                       d2h: torch.cuda.Stream):
+        """n_steps steps from host memory to host memory through the C entry point
+        mx4_decode_steps: the copies of neighbouring steps overlap the compute
+        (inputs on h2d, outputs on d2h, kernels on stream).  h_inputs: one packed
+        pinned buffer used by every step ([bytes]) or one per step ([n_steps, bytes]);
+        h_out: pinned fp32 [T, 16, 128] (every step's output in turn) or
+        [n_steps, T, 16, 128].  The second staging and output sets are allocated on
+        first use.  Asynchronous; `stream` waits for the last output copy."""
+        wl, c = self.wl, self.caches
+        if getattr(self, "_staging2", None) is None:
+            set_bytes = (self.input_layout["bytes"] + 255) // 256 * 256
+            self._staging2 = torch.empty(2 * set_bytes, dtype=torch.uint8, device=self.out.device)
+            self._out2 = torch.empty((2,) + tuple(self.out.shape), dtype=torch.float32,
+                                     device=self.out.device)
+        mx4_decode_steps(n_steps, h_inputs, self.slots.numel(), self._staging2, c.k_pages,
+                         c.v_pages, c.idx_pages, self.block_table, self.seq_lens, wl.q, wl.k,
+                         self.scale, self.scores, self.topk_idx, self.topk_ws, self.dec_ws,
+                         self._out2, h_out, stream, h2d, d2h, same_inputs=(h_inputs.dim() == 1))
 
     def launches_per_step(self) -> int:
         """Kernels this library launches per step: insert; the scorer; the top-k

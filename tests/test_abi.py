@@ -222,3 +222,31 @@ def test_decode_step_host_validation_and_layout(lib):
     args[2] = ctypes.c_void_p(4096)
     args[3] = 16  # staging far below the packed inputs
     assert L.mx4_decode_step(*args) == -3 and "staging" in _err(m)
+
+
+def test_decode_steps_host_validation(lib):
+    # The multi-step call refuses a negative step count, a missing copy stream or two
+    # equal streams and
+    # a staging buffer below two input sets before it enqueues anything; zero steps
+    # is a no-op.
+    import mxfp4_sparse_paged_gb300 as m
+    L = m._load()
+    f = ctypes.c_float(0.1)
+    buf = ctypes.create_string_buffer(64)
+    host = ctypes.cast(buf, ctypes.c_void_p)
+    s1, s2, s3 = ctypes.c_void_p(16), ctypes.c_void_p(32), ctypes.c_void_p(48)
+    _, nbytes = m.mx4_decode_step_input_layout(2, 0)
+    args = [1, host, 0, 0, ctypes.c_void_p(4096), 2 * nbytes - 256, None, None, 8704, 8704,
+            None, 8704, 1, None, 2, 1, None, 1, 16, f, None, 64, None, None, 0, None, 0,
+            ctypes.c_void_p(8192), host, 0, s1, s2, s3]
+    a = list(args); a[0] = -1
+    assert L.mx4_decode_steps(*a) == -1 and "n_steps" in _err(m)
+    a = list(args); a[0] = 0
+    assert L.mx4_decode_steps(*a) == 0
+    a = list(args); a[32] = s2
+    assert L.mx4_decode_steps(*a) == -1 and "streams" in _err(m)
+    a = list(args); a[31] = None
+    assert L.mx4_decode_steps(*a) == -1 and "streams" in _err(m)
+    a = list(args); a[30] = None   # the compute stream may be the default one
+    assert L.mx4_decode_steps(*a) == -3 and "staging" in _err(m)
+    assert L.mx4_decode_steps(*args) == -3 and "staging" in _err(m)

@@ -513,6 +513,32 @@ def test_host_to_host_step_matches_a_plain_step(wid):
     m.mx4_check_status()
 
 
+@pytest.mark.parametrize("wid", [1, 4])
+def test_multi_step_host_call_matches_plain_steps(wid):
+    # mx4_decode_steps (5 steps in one C call, inputs and outputs in host memory, the
+    # copies of neighbouring steps overlapped on two copy streams) gives every step
+    # the plain step's output; with per-step buffers and with one shared buffer.
+    wl = W.make(wid)
+    caches, step, host = _gpu_step(wl)
+    want = step.out.cpu().numpy()
+    pin = step.pack_inputs(host)
+    n = 5
+    per_step = torch.stack([pin] * n).pin_memory()
+    h_outs = torch.full((n,) + tuple(step.out.shape), float("nan"), dtype=torch.float32)
+    h_outs = h_outs.pin_memory()
+    cs = torch.cuda.Stream()
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    step.run_host_steps(per_step, h_outs, n, cs, h2d, d2h)
+    cs.synchronize()
+    for i in range(n):
+        assert np.array_equal(h_outs[i].numpy(), want), f"step {i}"
+    h_out = torch.full(tuple(step.out.shape), float("nan"), dtype=torch.float32).pin_memory()
+    step.run_host_steps(pin, h_out, n, cs, h2d, d2h)
+    cs.synchronize()
+    assert np.array_equal(h_out.numpy(), want)
+    m.mx4_check_status()
+
+
 # ----------------------------------------------------------------- decode edges
 
 def test_decode_single_selected_token_is_exact_value_row():
