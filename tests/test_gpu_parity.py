@@ -753,6 +753,10 @@ def test_norm_rope_insert_against_oracle(H, Hkv):
     nd = sum(_check_quantised(kpn[:, h], kp_o[:, h], slots, yk[:, h], tk[:, h], f"K head {h}")
              for h in range(Hkv))
     nd += _check_quantised(ipn, ip_o, slots, yik, tik, "index-K")
+    # rows whose bytes differ from the exact quantiser's for fl32(y): each is inside
+    # the band; the count is printed so a drift toward the ceiling shows in the logs
+    print(f"writer (H={H}, Hkv={Hkv}): {nd} of {T * (Hkv + 1)} K / index-K rows differ "
+          f"from the exact quantiser's bytes (ceiling 2 %)")
     assert nd <= 0.02 * T * (Hkv + 1)
 
 
