@@ -417,8 +417,8 @@ def measure_workload(wid, args, dev, stream, flush_l2, world, barrier, headline=
     hot_gbs = hot / ((sc_ms + dec_ms) / 1e3) / 1e9
     r_score = _roof("index_score", ab["index_score"], sc_ms, peak,
                     _ncu_traffic(wl.spec.name, "index_score_traffic.json"),
-                    {"timing": "the scorer alone (index_score call); inside the step it runs "
-                               "in index_topk with its key histograms"})
+                    {"timing": "the scorer alone (index_score call); inside the step it is "
+                               "the first kernel of index_topk"})
     r_dec = _roof("sparse_paged_decode (run kernel + merge kernel)", ab["sparse_paged_decode"],
                   dec_ms, peak, _ncu_traffic(wl.spec.name, "decode_split_traffic.json"),
                   {"traffic_kernel": "decode_split_kernel"})
