@@ -527,10 +527,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
 // and sum per head; the runs are those of the warps whose ranges meet the token's
 // tiles.  The result goes through shared memory to a [head][dim] store.
 constexpr int kMergeThreads = 512;
-constexpr int kMergeUnroll = 4;  // runs whose loads are in flight together
+constexpr int kMergeUnroll = 6;  // runs whose loads are in flight together
 static_assert(kMergeThreads * 4 == kFrag, "one float4 of the fragment order per thread");
 
-__global__ void __launch_bounds__(kMergeThreads)
+__global__ void __launch_bounds__(kMergeThreads, 2)
 decode_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NW, int NT,
                     float* __restrict__ out) {
   __shared__ __align__(16) float so[kFrag];
@@ -556,23 +556,9 @@ decode_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NW, int NT,
   auto live = [&](int64_t gw) {
     return !gaps || warp_tile_begin(gw, U, NW) != warp_tile_begin(gw + 1, U, NW);
   };
+  // one pass over the runs, kMergeUnroll of them in flight: the running max per
+  // head rescales what is summed so far when a run raises it
   float M0 = -INFINITY, M1 = -INFINITY;
-  for (int64_t gw = g0; gw <= g1; gw += kMergeUnroll) {
-    float a0[kMergeUnroll], a1[kMergeUnroll];
-#pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
-      const int64_t g = gw + u;
-      const bool ok = g <= g1 && live(g);
-      const float* rec = ws + (ok ? g + t : g0 + t) * kRecFloats;
-      a0[u] = ok ? rec[kFrag + h0] : -INFINITY;
-      a1[u] = ok ? rec[kFrag + h0 + 8] : -INFINITY;
-    }
-#pragma unroll
-    for (int u = 0; u < kMergeUnroll; ++u) {
-      M0 = fmaxf(M0, a0[u]);
-      M1 = fmaxf(M1, a1[u]);
-    }
-  }
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   float L0 = 0.f, L1 = 0.f;
   for (int64_t gw = g0; gw <= g1; gw += kMergeUnroll) {
@@ -589,6 +575,23 @@ decode_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NW, int NT,
       l1[u] = rec[kFrag + kHeads + h0 + 8];
       v[u] = reinterpret_cast<const float4*>(rec)[x];
     }
+    float N0 = M0, N1 = M1;
+#pragma unroll
+    for (int u = 0; u < kMergeUnroll; ++u) {
+      N0 = fmaxf(N0, m0[u]);
+      N1 = fmaxf(N1, m1[u]);
+    }
+    // what is summed so far is 0 while the max is still -inf
+    const float r0 = (M0 == -INFINITY) ? 0.f : exp2f(M0 - N0);
+    const float r1 = (M1 == -INFINITY) ? 0.f : exp2f(M1 - N1);
+    L0 *= r0;
+    L1 *= r1;
+    acc.x *= r0;
+    acc.y *= r0;
+    acc.z *= r1;
+    acc.w *= r1;
+    M0 = N0;
+    M1 = N1;
 #pragma unroll
     for (int u = 0; u < kMergeUnroll; ++u) {
       // a run with no valid entry has max -inf, sum 0 and O 0: weight 0
