@@ -258,10 +258,21 @@ score_kernel(const ScoreArgs a) {
           cur_seq = seq;
         }
         // score of row r of this page for query qq: -inf past the token's position
+        // (L - Q + qq); rows at or past L are not written.  With three or more
+        // queries, the page's first score of query 0 and the limits relative to the
+        // page are taken once per page (measured: faster for q = 4, slower for q = 1).
+        float* const base = a.scores + (int64_t)seq * Q * a.ld + (int64_t)pg * kPageTokens;
+        const int nrows = min(kPageTokens, L - pg * kPageTokens);
+        const int last0 = L - Q - pg * kPageTokens;  // query 0's last finite row
         auto emit = [&](int qq, int r, float v) {
-          const int64_t i_g = (int64_t)pg * kPageTokens + r;
-          const int64_t p = (int64_t)L - Q + qq;
-          if (i_g < L) a.scores[((int64_t)seq * Q + qq) * a.ld + i_g] = (i_g <= p) ? v : -INFINITY;
+          if constexpr (Q >= 3) {
+            if (r < nrows) base[qq * a.ld + r] = (r <= last0 + qq) ? v : -INFINITY;
+          } else {
+            const int64_t i_g = (int64_t)pg * kPageTokens + r;
+            const int64_t p = (int64_t)L - Q + qq;
+            if (i_g < L)
+              a.scores[((int64_t)seq * Q + qq) * a.ld + i_g] = (i_g <= p) ? v : -INFINITY;
+          }
         };
 #pragma unroll
         for (int tt = 0; tt < kPageTokens / 16 / NC; ++tt)
