@@ -40,13 +40,13 @@ struct Mxfp4Fmt {
   struct Tile {
     static constexpr int NT = (Q + 1) / 2;  // n8 tiles: 4 block-columns per query
     uint32_t breg[NT][8][2];
-    float inv_scale[Q];
+    float isc[NT];  // 2^-sigma of this lane's query in n8 tile nt: 2 nt + (tig >> 1)
 
     // index-q of the sequence -> f16 B fragments, scaled by 2^sigma per query so
     // its largest magnitude lands in [2^14, 2^15)
     __device__ __forceinline__ void set_queries(const uint16_t* qs, int lane, float) {
       const int g = lane >> 2, tig = lane & 3;
-      float sc[Q];
+      float sc[Q], inv[Q];
 #pragma unroll
       for (int qq = 0; qq < Q; ++qq) {
         const uint2 v = *reinterpret_cast<const uint2*>(qs + qq * kHeadDim + 4 * lane);
@@ -55,7 +55,15 @@ struct Mxfp4Fmt {
         am = __reduce_max_sync(0xFFFFFFFFu, am);
         const int sigma = (am == 0u) ? 0 : min(100, max(-113, 14 - ((int)(am >> 23) - 127)));
         sc[qq] = __uint_as_float((uint32_t)(127 + sigma) << 23);
-        inv_scale[qq] = __uint_as_float((uint32_t)(127 - sigma) << 23);
+        inv[qq] = __uint_as_float((uint32_t)(127 - sigma) << 23);
+      }
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {  // selected once, without lane-dependent indexing
+        const int qq = 2 * nt + (tig >> 1);
+        isc[nt] = inv[0];
+#pragma unroll
+        for (int q2 = 1; q2 < Q; ++q2)
+          if (q2 == qq) isc[nt] = inv[q2];
       }
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
@@ -123,12 +131,8 @@ struct Mxfp4Fmt {
         vg8 += __shfl_xor_sync(0xFFFFFFFFu, vg8, 1);
         const int qq = 2 * nt + (tig >> 1);
         if ((tig & 1) == 0 && qq < Q) {
-          float isc = inv_scale[0];
-#pragma unroll
-          for (int q2 = 1; q2 < Q; ++q2)
-            if (q2 == qq) isc = inv_scale[q2];
-          emit(qq, r0 + g, vg * isc);
-          emit(qq, r0 + g + 8, vg8 * isc);
+          emit(qq, r0 + g, vg * isc[nt]);
+          emit(qq, r0 + g + 8, vg8 * isc[nt]);
         }
       }
     }
