@@ -521,33 +521,42 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
   asm volatile("cp.async.wait_all;\n" ::: "memory");  // no copy in flight at exit
 }
 
-// One CTA per decode token, thread x = (j, lane) of the fragment order: combines
+// gridDim.y CTAs per decode token (1 or 4), each 4 / gridDim.y quarters of the
+// fragment order (quarter y: fragments j of 4 y .. 4 y + 3), thread x = (j, lane)
+// of the fragment order: combines
 // the runs of the token, out = sum_r O_r 2^(m_r - M) / sum_r l_r 2^(m_r - M), with
 // O_r the run's unnormalised output and (m_r, l_r) its running max (log2 units)
 // and sum per head; the runs are those of the warps whose ranges meet the token's
-// tiles.  The result goes through shared memory to a [head][dim] store.
-constexpr int kMergeThreads = 512;
-constexpr int kMergeUnroll = 6;  // runs whose loads are in flight together
-static_assert(kMergeThreads * 4 == kFrag, "one float4 of the fragment order per thread");
+// tiles.  A quarter is 16 heads x 32 dims of the output, in runs of 4 dims: it goes
+// through shared memory to 16-byte stores.  A token met by many warps (many
+// records) takes 4 CTAs, so the records of few tokens spread over the SMs.
+constexpr int kMergeQuarter = kFrag / 4 / 4;  // 128 float4 of the fragment order
+constexpr int kMergeSplitRuns = 8;            // more runs per token than this: 4 CTAs
 
-__global__ void __launch_bounds__(kMergeThreads, 2)
+// SPLIT CTAs per token of 512 / SPLIT threads; runs whose loads are in flight
+// together: 6 at 512 threads (two CTAs per SM), 8 at 128.
+template <int SPLIT>
+__global__ void __launch_bounds__(4 * kMergeQuarter / SPLIT, SPLIT == 1 ? 2 : 1)
 decode_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NW, int NT,
                     float* __restrict__ out) {
-  __shared__ __align__(16) float so[kFrag];
+  constexpr int kMergeUnroll = SPLIT == 1 ? 6 : 8;
+  __shared__ __align__(16) float so[4][kHeads][32];
   __shared__ int64_t s_g[2];
   pdl_launch_dependents();
   const int64_t t = blockIdx.x;
-  const int x = threadIdx.x, j = x >> 5, lane = x & 31, h0 = lane >> 2, tig = lane & 3;
-  if (x < 2) {
-    // the warp whose range holds the token's first (x = 0) or last (x = 1) tile:
-    // the last g with begin(g) <= tile
-    const int64_t tile = x == 0 ? t * NT : (t + 1) * NT - 1;
+  const int x = blockIdx.y * blockDim.x + threadIdx.x, j = x >> 5, lane = x & 31;
+  const int qy = x / kMergeQuarter, lq = threadIdx.x / kMergeQuarter;  // quarter, local
+  const int h0 = lane >> 2, tig = lane & 3;
+  if (threadIdx.x < 2) {
+    // the warp whose range holds the token's first (0) or last (1) tile: the last
+    // g with begin(g) <= tile
+    const int64_t tile = threadIdx.x == 0 ? t * NT : (t + 1) * NT - 1;
     int64_t lo = 0, hi = NW - 1;
     while (lo < hi) {
       const int64_t mid = (lo + hi + 1) >> 1;
       if (warp_tile_begin(mid, U, NW) <= tile) lo = mid; else hi = mid - 1;
     }
-    s_g[x] = lo;
+    s_g[threadIdx.x] = lo;
   }
   __syncthreads();
   pdl_wait();
@@ -605,14 +614,19 @@ decode_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NW, int NT,
       acc.w = fmaf(v[u].w, w1, acc.w);
     }
   }
-  // element c: head h0 + 8 (c >> 1), dim 8 (2 tig + (c & 1) + 8 (j >> 3)) + (j & 7)
-  const int d0 = 8 * (2 * tig + 8 * (j >> 3)) + (j & 7);
-  so[h0 * kHeadDim + d0] = L0 > 0.f ? acc.x / L0 : 0.f;
-  so[h0 * kHeadDim + d0 + 8] = L0 > 0.f ? acc.y / L0 : 0.f;
-  so[(h0 + 8) * kHeadDim + d0] = L1 > 0.f ? acc.z / L1 : 0.f;
-  so[(h0 + 8) * kHeadDim + d0 + 8] = L1 > 0.f ? acc.w / L1 : 0.f;
+  // element c: head h0 + 8 (c >> 1), dim 8 (2 tig + (c & 1) + 8 (j >> 3)) + (j & 7);
+  // within the quarter (dims 64 (qy >> 1) + 8 col + 4 (qy & 1) + e, e = j & 3): the
+  // column 4 col + e of so
+  const int e = j & 3;
+  so[lq][h0][4 * (2 * tig) + e] = L0 > 0.f ? acc.x / L0 : 0.f;
+  so[lq][h0][4 * (2 * tig + 1) + e] = L0 > 0.f ? acc.y / L0 : 0.f;
+  so[lq][h0 + 8][4 * (2 * tig) + e] = L1 > 0.f ? acc.z / L1 : 0.f;
+  so[lq][h0 + 8][4 * (2 * tig + 1) + e] = L1 > 0.f ? acc.w / L1 : 0.f;
   __syncthreads();
-  reinterpret_cast<float4*>(out + t * kFrag)[x] = reinterpret_cast<const float4*>(so)[x];
+  const int r = threadIdx.x & (kMergeQuarter - 1), hh = r >> 3, col = r & 7;
+  const int d = 64 * (qy >> 1) + 8 * col + 4 * (qy & 1);
+  *reinterpret_cast<float4*>(out + t * kFrag + hh * kHeadDim + d) =
+      *reinterpret_cast<const float4*>(&so[lq][hh][4 * col]);
 }
 
 // Grid of the split kernel: one CTA per SM, fewer when the warps would get fewer
@@ -661,7 +675,11 @@ cudaError_t launch_decode(const uint16_t* q, int64_t T, int Q, const uint8_t* k_
   if (err != cudaSuccess) return err;
   err = launch_pdl(decode_split_kernel, dim3((unsigned)G), dim3(kDecThreads), smem, stream, a);
   if (err != cudaSuccess) return err;
-  return launch_pdl(decode_merge_kernel, dim3((unsigned)T), dim3(kMergeThreads), 0, stream,
+  if (G * kDecWarps > (int64_t)kMergeSplitRuns * T)
+    return launch_pdl(decode_merge_kernel<4>, dim3((unsigned)T, 4), dim3(kMergeQuarter), 0, stream,
+                      (const float*)a.ws, a.U, G * kDecWarps, a.NT, out);
+  return launch_pdl(decode_merge_kernel<1>, dim3((unsigned)T, 1), dim3(4 * kMergeQuarter), 0,
+                    stream,
                     (const float*)a.ws, a.U, G * kDecWarps, a.NT, out);
 }
 
