@@ -177,7 +177,9 @@ int index_score(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t *idx
  *     scores[t*ld_scores + i] = sum_b 2^E_b * sum_{d in b} E4M3value(code_d) * dequant(indexK[s, i])[d]
  * for 0 <= i <= p, accumulated in fp32 by the tensor core; -inf and unwritten
  * entries as index_score.  Arguments, layouts, limits, ownership and status
- * bits are those of index_score.  An opt-in mode: it differs from index_score
+ * bits are those of index_score, except that idx_pages must be 32-byte aligned
+ * and idx_page_stride a multiple of 32 (MX4_ERR_INVALID otherwise: the pages are
+ * read by tensor copies of the pool).  An opt-in mode: it differs from index_score
  * by the query's MXFP8 rounding (a relative error of at most 2^-4 per element).
  * ------------------------------------------------------------------------- */
 int index_score_mxq(const uint16_t *iq, int64_t T, int q_per_seq, const uint8_t *idx_pages,

@@ -30,6 +30,7 @@ struct Mxfp4Fmt {
   static constexpr int kConsumers = 8;  // one 16-row tile of each page per warp
   static constexpr int kStages = 4;
   static constexpr int kStageDataBytes = kPageBytes;
+  static constexpr int kStageAlign = 16;
   static constexpr int kFullCount = 1;             // the producer's expect-tx arrival
   static constexpr int kEmptyCount = kConsumers;    // one arrival per consumer warp
   static constexpr int kExtraBytes = 0;

@@ -14,29 +14,33 @@
 // with A = e2m1, B = e4m3 and UE8M0 scales; step kb picks byte kb of each
 // row's 32-bit scale word, which is the page's own scale row.
 //
-// Operand layouts (K-major, no swizzle, 8-row x 16-byte core matrices):
-//   A: the 16 codes of K-chunk j of row m take the first 8 bytes of a 16-byte
-//      slot at (m/8)*1024 + j*128 + (m%8)*16 (the e2m1 operand of this MMA kind
-//      is packed two a byte, low nibble first, in 16-byte slots of which the
-//      last 8 bytes are ignored); LBO (next K-chunk) = 128, SBO (next 8 rows) =
-//      1024.  The producer copies each 8-byte piece of the page straight from
-//      global memory to its slot (cp.async), so the A tile is the stage itself.
-//   B: the 16 E4M3 bytes of K-chunk j of query n at (n/8)*1024 + j*128 + (n%8)*16.
+// Operand layouts (K-major):
+//   A: the e2m1 operand of this MMA kind takes 16 codes (packed two a byte, low
+//      nibble first) in the first 8 bytes of a 16-byte slot, the other 8 bytes
+//      unread.  A tensor copy of the pool with the 4-bit type that writes exactly
+//      that (16U4_ALIGN16B) and 128-byte swizzle puts a page's 128 rows into the A
+//      tile as 8-row x 128-byte atoms, the 16-byte slots of row r XOR-permuted by
+//      r % 8; the descriptor's SBO (next 8 rows) is 1024 and K-step kb starts 32
+//      bytes along the row.  The A tile is the stage itself.
+//   B: no swizzle, 8-row x 16-byte core matrices: the 16 E4M3 bytes of K-chunk j of
+//      query n at (n/8)*1024 + j*128 + (n%8)*16; LBO = 128, SBO = 1024.
 //   Scales in tensor memory: row m's word at lane m, column (key scales) + m/32;
 //   query n's word at lane n of every lane quarter (each quarter of the
 //   accumulator reads the query scales from its own 32 lanes).
 //   Accumulator: lane m = page row m, column n = query n (fp32).
 //
-// Stage: A tile (16384 B) | the page's 512 scale bytes | the sequence's index-q
-// rows.  Its full barrier completes when the producer's bulk copies (scales,
-// queries; transaction-counted) and every producer lane's 8-byte copies
-// (cp.async.mbarrier.arrive) have landed; the MMA group's commit frees it.
+// Stage (1024-byte aligned): A tile (16384 B) | the page's 512 scale bytes | the
+// sequence's index-q rows.  Its full barrier completes when the tensor copy (8192
+// bytes read) and the bulk copies (transaction-counted) have landed; the MMA group's
+// commit frees it.
 //
 // Consumers (four warps, one per tensor-memory lane quarter): per page, write
 // its scale words into tensor memory, and thread 0 issues the four MMAs into
 // one of two accumulators; then read back and store the previous page's
 // scores, whose MMAs ran meanwhile.  Every wait is bounded and every exit waits
 // for the MMAs in flight and frees the tensor memory the CTA allocated.
+#include <cudaTypedefs.h>  // PFN_cuTensorMapEncodeTiled
+
 #include "score_pipeline.cuh"
 
 namespace mx4 {
@@ -62,6 +66,13 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
   d |= (uint64_t)1 << 46;  // descriptor version; base offset 0, no swizzle
   return d;
+}
+
+// Descriptor of a K-major operand in 128-byte swizzle atoms (8 rows x 128 bytes,
+// the 16-byte chunks of row r XOR-permuted by r % 8, as the tensor copy writes them):
+// SBO = 1024 to the next 8 rows; a K-step starts 32 bytes further along the row.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+  return smem_desc(addr, 16, 1024) | ((uint64_t)2 << 61);
 }
 
 // Instruction descriptor of K-step kb: A e2m1 (5), B e4m3 (0), UE8M0 scales,
@@ -100,17 +111,6 @@ __device__ __forceinline__ void commit(uint32_t bar) {
                : "memory");
 }
 
-// 8-byte copy global -> shared (L1-allocating; the only cp.async size below 16
-// bytes that fits an e2m1 K-chunk), and the arrival on `bar` that fires when all
-// of this thread's earlier cp.async copies have landed (counted in the barrier's
-// expected arrivals).
-__device__ __forceinline__ void cp_async8(uint32_t dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];\n" ::"r"(bar) : "memory");
-}
-
 // E4M3 codes of four fp32 values (nearest, ties to even, saturating at 448),
 // x0 in the low byte.
 __device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x3) {
@@ -125,76 +125,68 @@ __device__ __forceinline__ uint32_t e4m3x4(float x0, float x1, float x2, float x
 struct MxqFmt {
   static constexpr int kPageBytes = mx4::kPageBytes;
   static constexpr int kStageDataBytes = mxq::kATileBytes + mxq::kScaleBytes;
-  static constexpr int kConsumers = 4;  // one warp per tensor-memory lane quarter
-  static constexpr int kStages = 3;
-  static constexpr int kFullCount = 1 + 32;  // the expect-tx arrival + each producer lane's copies
-  static constexpr int kEmptyCount = 1;      // the MMA group's commit (or a skip)
-  static constexpr int kExtraBytes = mxq::kRegionBytes;
+  static constexpr int kStageAlign = 1024;  // the A tile's 128-byte swizzle atoms
+  static constexpr int kConsumers = 4;      // one warp per tensor-memory lane quarter
+  static constexpr int kStages = 2;
+  static constexpr int kFullCount = 1;   // the producer's expect-tx arrival
+  static constexpr int kEmptyCount = 1;  // the MMA group's commit (or a skip)
+  static constexpr int kExtraBytes = (mxq::kRegionBytes + kStageAlign - 1) / kStageAlign * kStageAlign;
   static constexpr bool kWholePage = true;
-  // Three CTAs per SM (three producer warps): the 8-byte copies allocate in L1,
-  // and the misses an SM can keep in flight, not the stage count, set the rate
-  // (measured on the b256 workload: 1 CTA x 8 stages 123 us, 2 x 5 74 us, 3 x 3 62 us).
-  static constexpr int ctas_per_sm(int) { return 3; }
+  // Two stages and five CTAs an SM (as many as the shared memory holds): the page
+  // rate follows the CTAs working at once more than the stages each keeps in flight
+  // (measured on the b256 workload, stages x CTAs: 5 x 2 65 us, 3 x 3 53 us,
+  // 2 x 4 49 us, 2 x 5 47 us, 1 x 6 56 us).
+  static constexpr int ctas_per_sm(int) { return 5; }
 
-  // Producer warp: for each page of the CTA's range, once its stage is free, the
-  // page's 8-byte K-chunks go to their A-tile slots (instruction i of the 32 covers
-  // rows 8*(i/2) .. +7 and K-chunks 4*(i%2) .. +3: whole 32-byte sectors of the
-  // page), the scale row and the sequence's index-q rows by bulk copy.
+  // Producer warp: for each page of the CTA's range, once its stage is free, one
+  // tensor copy of the page's 128 data rows into the A tile (the pool's tensor map:
+  // 4-bit elements, 16 to a 16-byte slot, 128-byte swizzle), and bulk copies of the
+  // scale row and the sequence's index-q rows.  The tensor copy counts the 8192 bytes
+  // it reads in the barrier's transaction count.
   template <int Q>
   static __device__ void produce(const ScoreArgs& a, const StageRing& ring, const int* pref,
                                  int p0, int n, int lane) {
     constexpr int S = kStages;
     for (int base = 0; base < n; base += 32) {
       if (__any_sync(0xFFFFFFFFu, *ring.abort_flag != 0)) break;
-      PageRef pr{a.pages, -1, 0, 0, 0};
+      PageRef pr{a.pages, -1, 0, 0, 0, 0};
       if (base + lane < n) pr = resolve_page(a, pref, p0 + base + lane);
       const int cnt = min(32, n - base);
-      bool go = true;
-      for (int l = 0; l < cnt && go; ++l) {
-        const int kk = base + l, st = kk % S, round = kk / S;
-        const uint8_t* src = reinterpret_cast<const uint8_t*>(
-            __shfl_sync(0xFFFFFFFFu, reinterpret_cast<unsigned long long>(pr.src), l));
-        const int ok = __shfl_sync(0xFFFFFFFFu, pr.ok, l);
-        const int seq = __shfl_sync(0xFFFFFFFFu, pr.seq, l);
-        if (lane == 0) {
-          go = !*ring.abort_flag;
+      for (int l = 0; l < cnt; ++l) {
+        if (lane == l) {
+          const int kk = base + l, st = kk % S, round = kk / S;
+          bool go = !*ring.abort_flag;
           if (go && round > 0 && !mbar_wait(smem_addr(&ring.empty[st]), (round - 1) & 1)) {
             flag(a.status, MX4_STATUS_TIMEOUT);
             *ring.abort_flag = 1;
             go = false;
           }
-        }
-        go = __shfl_sync(0xFFFFFFFFu, go, 0);
-        if (!go) break;
-        if (lane == l) {
-          ring.seq[st] = pr.seq;
-          ring.page[st] = pr.page;
-          ring.len[st] = pr.len;
-          ring.ok[st] = pr.ok;
+          if (go) {
+            ring.seq[st] = pr.seq;
+            ring.page[st] = pr.page;
+            ring.len[st] = pr.len;
+            ring.ok[st] = pr.ok;
+            const uint32_t fb = smem_addr(&ring.full[st]);
+            const uint32_t d0 = smem_addr(ring.base + st * ring.stage_bytes);
+            if (pr.ok) {
+              mbar_arrive_expect_tx(fb, kRowDataBytes * kPageTokens + mxq::kScaleBytes +
+                                            Q * kHeadDim * 2);
+              asm volatile(
+                  "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::"
+                  "bytes [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(d0),
+                  "l"(reinterpret_cast<uint64_t>(&a.tmap)), "r"(0), "r"(0), "r"(pr.pid), "r"(fb)
+                  : "memory");
+              bulk_copy_g2s(d0 + mxq::kATileBytes, pr.src + kScaleOffset, mxq::kScaleBytes, fb);
+              bulk_copy_g2s(d0 + kStageDataBytes, a.iq + (int64_t)pr.seq * Q * kHeadDim,
+                            Q * kHeadDim * 2, fb);
+            } else {
+              mbar_arrive(fb);
+            }
+            *ring.issued = kk + 1;
+          }
         }
         __syncwarp();
-        const uint32_t fb = smem_addr(&ring.full[st]);
-        const uint32_t d0 = smem_addr(ring.base + st * ring.stage_bytes);
-        if (ok) {
-          if (lane == 0) {
-            mbar_arrive_expect_tx(fb, mxq::kScaleBytes + Q * kHeadDim * 2);
-            bulk_copy_g2s(d0 + mxq::kATileBytes, src + kScaleOffset, mxq::kScaleBytes, fb);
-            bulk_copy_g2s(d0 + kStageDataBytes, a.iq + (int64_t)seq * Q * kHeadDim,
-                          Q * kHeadDim * 2, fb);
-          }
-#pragma unroll 8
-          for (int i = 0; i < 32; ++i) {
-            const int r = (i >> 1) * 8 + (lane & 7), j = (i & 1) * 4 + (lane >> 3);
-            mxq::cp_async8(d0 + (r >> 3) * 1024 + j * 128 + (r & 7) * 16, src + r * 64 + j * 8);
-          }
-          mxq::cp_async_arrive(fb);
-        } else {
-          if (lane == 0) mbar_arrive(fb);
-          mbar_arrive(fb);
-        }
-        if (lane == 0) *ring.issued = kk + 1;
       }
-      if (!go) break;
     }
   }
 
@@ -351,7 +343,7 @@ struct MxqFmt {
           const uint32_t a_addr = smem_addr(stage);
 #pragma unroll
           for (uint32_t kb = 0; kb < 4; ++kb) {
-            const uint64_t ad = mxq::smem_desc(a_addr + kb * 256, 128, 1024);
+            const uint64_t ad = mxq::smem_desc_sw128(a_addr + kb * 32);
             const uint64_t bd = mxq::smem_desc(b_addr + kb * 256, 128, 1024);
             asm volatile(
                 "{\n .reg .pred p;\n setp.ne.b32 p, %6, 0;\n"
@@ -402,13 +394,44 @@ struct MxqFmt {
   }
 };
 
+// The pool's data rows as a 3-d tensor for the tensor copy: 128 4-bit elements a
+// row (64 bytes), 128 rows a page (64 bytes apart), num_pages pages (page_stride
+// apart); a box is one page.  The 4-bit type writes 16 elements to each 16-byte
+// slot.  Needs the pool 32-byte aligned and the page stride a multiple of 32.
+// The encoder is the driver's, found through the runtime (no link to the driver
+// library).
+static cudaError_t encode_pool(const uint8_t* pages, int64_t page_stride, int64_t num_pages,
+                               CUtensorMap* tm) {
+  static PFN_cuTensorMapEncodeTiled_v12000 enc = [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      fn = nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }();
+  if (!enc) return cudaErrorNotSupported;
+  const cuuint64_t dims[3] = {(cuuint64_t)2 * kRowDataBytes, (cuuint64_t)kPageTokens,
+                              (cuuint64_t)num_pages};
+  const cuuint64_t strides[2] = {(cuuint64_t)kRowDataBytes, (cuuint64_t)page_stride};
+  const cuuint32_t box[3] = {2 * kRowDataBytes, kPageTokens, 1};
+  const cuuint32_t elem_strides[3] = {1, 1, 1};
+  const CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3,
+                         const_cast<uint8_t*>(pages), dims, strides, box, elem_strides,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_index_score_mxq(const uint16_t* iq, int q, const uint8_t* idx_pages,
                                    int64_t idx_page_stride, int64_t num_pages,
                                    const int32_t* block_table, int B, int64_t bt_width,
                                    const int32_t* seq_lens, float* scores, int64_t ld,
                                    uint32_t* status, int num_sms, cudaStream_t stream) {
-  const ScoreArgs a{iq, idx_pages, idx_page_stride, num_pages, block_table, B, bt_width,
-                    seq_lens, scores, ld, status, 1.f};
+  ScoreArgs a{iq, idx_pages, idx_page_stride, num_pages, block_table, B, bt_width,
+              seq_lens, scores, ld, status, 1.f, {}};
+  if (cudaError_t e = encode_pool(idx_pages, idx_page_stride, num_pages, &a.tmap)) return e;
   switch (q) {
     case 1: return launch_score<MxqFmt, 1>(a, num_sms, stream);
     case 2: return launch_score<MxqFmt, 2>(a, num_sms, stream);

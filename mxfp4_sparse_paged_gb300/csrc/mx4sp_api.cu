@@ -269,6 +269,10 @@ int index_score_mxq(const uint16_t* iq, int64_t T, int q_per_seq, const uint8_t*
                     int64_t idx_page_stride, int64_t num_pages, const int32_t* block_table,
                     int64_t B, int64_t bt_width, const int32_t* seq_lens, float* scores,
                     int64_t ld_scores, void* stream) {
+  // the tensor copy of the pool wants it 32-byte aligned with a page stride of 32s
+  if (B > 0 && idx_pages && (!aligned(idx_pages, 32) || idx_page_stride % 32))
+    return fail(MX4_ERR_INVALID, "index_score_mxq: index pages not 32-byte aligned or page "
+                "stride not a multiple of 32");
   return score_entry("index_score_mxq", mx4::launch_index_score_mxq, iq, T, q_per_seq,
                      idx_pages, idx_page_stride, num_pages, block_table, B, bt_width, seq_lens,
                      scores, ld_scores, stream);

@@ -26,6 +26,10 @@
 // counts of its full and empty barriers.
 #pragma once
 
+#include <algorithm>
+
+#include <cuda.h>  // CUtensorMap (a type only: the map is encoded through the runtime)
+
 #include "common.cuh"
 
 namespace mx4 {
@@ -52,22 +56,28 @@ struct ScoreArgs {
   int64_t ld;
   uint32_t* status;
   float scale;                 // the fp8 cache's scale (1 for MXFP4)
+  CUtensorMap tmap;            // the pool as a tensor map, for a format that loads pages by one
 };
 
 // Shared-memory layout of the kernel, in bytes: format region | stages |
 // barriers | stage info | warp sums, flags | per-sequence page prefix [B].
 template <class F, int Q>
 struct ScoreLayout {
-  static constexpr int kStageBytes = F::kStageDataBytes + Q * kHeadDim * 2;
+  static constexpr int kStageBytes =
+      (F::kStageDataBytes + Q * kHeadDim * 2 + F::kStageAlign - 1) / F::kStageAlign * F::kStageAlign;
   static_assert(kStageBytes % 16 == 0, "bulk-copy alignment");
-  static_assert(F::kExtraBytes % 128 == 0, "format region alignment");
+  static_assert(F::kExtraBytes % 128 == 0 && F::kExtraBytes % F::kStageAlign == 0,
+                "format region alignment");
   static constexpr int kStagesOff = F::kExtraBytes;
   static constexpr int kBarOff = kStagesOff + F::kStages * kStageBytes;  // full[S], empty[S]
   static constexpr int kInfoOff = kBarOff + 2 * F::kStages * 8;
   static constexpr int kWarpSumOff = kInfoOff + 4 * F::kStages * 4;
   static constexpr int kFlagOff = kWarpSumOff + 32 * 4;  // abort, issued
   static constexpr int kPrefOff = (kFlagOff + 8 + 15) / 16 * 16;
-  static size_t bytes(int B) { return (size_t)kPrefOff + (size_t)B * 4; }
+  // (plus the slack that aligns the dynamic shared memory to a stage alignment above 128)
+  static size_t bytes(int B) {
+    return (size_t)kPrefOff + (size_t)B * 4 + (F::kStageAlign > 128 ? F::kStageAlign : 0);
+  }
 };
 
 // The stage ring as a whole-page format sees it: stage st holds a page (and the
@@ -92,6 +102,7 @@ struct StageRing {
 struct PageRef {
   const uint8_t* src;
   int seq, page, len, ok;
+  int pid;  // the page id (0 when not ok)
 };
 __device__ __forceinline__ PageRef resolve_page(const ScoreArgs& a, const int* pref, int P) {
   int lo = 0, hi = a.B - 1;
@@ -107,15 +118,21 @@ __device__ __forceinline__ PageRef resolve_page(const ScoreArgs& a, const int* p
   r.ok = (pid >= 0 && pid < a.num_pages) ? 1 : 0;
   if (!r.ok) flag(a.status, MX4_STATUS_BAD_PAGE);
   r.src = r.ok ? a.pages + (int64_t)pid * a.page_stride : a.pages;
+  r.pid = r.ok ? pid : 0;
   return r;
 }
 
 template <class F, int Q>
 __global__ void __launch_bounds__((F::kConsumers + 1) * 32, F::ctas_per_sm(Q))
-score_kernel(const ScoreArgs a) {
+score_kernel(const __grid_constant__ ScoreArgs a) {
   using Lay = ScoreLayout<F, Q>;
   constexpr int S = F::kStages, NC = F::kConsumers, NTHR = (NC + 1) * 32;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ __align__(128) uint8_t smem_dyn[];
+  uint8_t* const smem_raw =
+      F::kStageAlign > 128
+          ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_dyn) + F::kStageAlign - 1) &
+                                       ~static_cast<uintptr_t>(F::kStageAlign - 1))
+          : smem_dyn;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem_raw + Lay::kBarOff);
   uint64_t* empty = full + S;
   int* info_seq = reinterpret_cast<int*>(smem_raw + Lay::kInfoOff);
@@ -185,7 +202,7 @@ score_kernel(const ScoreArgs a) {
       for (int base = 0; base < n; base += 32) {
         if (__any_sync(0xFFFFFFFFu, *abort_flag != 0)) break;
         const int k = base + lane;
-        PageRef pr{a.pages, -1, 0, 0, 0};
+        PageRef pr{a.pages, -1, 0, 0, 0, 0};
         if (k < n) pr = resolve_page(a, pref, p0 + k);
         const int seqk = pr.seq, jk = pr.page, lenk = pr.len, okk = pr.ok;
         const uint8_t* src = pr.src;
@@ -284,6 +301,36 @@ score_kernel(const ScoreArgs a) {
   }
 }
 
+// CTAs of `kern` with `threads` threads and `smem` bytes of dynamic shared memory
+// that fit on one SM of the current device at once.
+inline cudaError_t resident_ctas(const void* kern, int threads, size_t smem, int* out) {
+  cudaFuncAttributes fa;
+  cudaError_t err = cudaFuncGetAttributes(&fa, kern);
+  if (err != cudaSuccess) return err;
+  int dev = 0, smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0, blocks_sm = 0;
+  if ((err = cudaGetDevice(&dev)) != cudaSuccess) return err;
+  if ((err = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                    dev)) != cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+          cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) !=
+          cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) !=
+          cudaSuccess ||
+      (err = cudaDeviceGetAttribute(&blocks_sm, cudaDevAttrMaxBlocksPerMultiprocessor, dev)) !=
+          cudaSuccess)
+    return err;
+  const size_t per_block = smem + fa.sharedSizeBytes + (size_t)reserved;
+  const int warps = (threads + 31) / 32;
+  const int regs_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated per warp, 256 at a time
+  int n = blocks_sm;
+  n = std::min(n, (int)((size_t)smem_sm / per_block));
+  n = std::min(n, regs_warp > 0 ? regs_sm / (regs_warp * warps) : n);
+  n = std::min(n, threads_sm / (warps * 32));
+  *out = n;
+  return cudaSuccess;
+}
+
 // Launch over batches of at most kScoreMaxBatch sequences (the prefix array).
 template <class F, int Q>
 cudaError_t launch_score(ScoreArgs a, int num_sms, cudaStream_t stream) {
@@ -294,7 +341,20 @@ cudaError_t launch_score(ScoreArgs a, int num_sms, cudaStream_t stream) {
   cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)Lay::bytes(kScoreMaxBatch));
   if (err != cudaSuccess) return err;
-  const int grid = num_sms * F::ctas_per_sm(Q);
+  // all of the SM's unified memory that can be shared memory (the stages are filled
+  // by bulk and tensor copies, not through L1)
+  err = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             cudaSharedmemCarveoutMaxShared);
+  if (err != cudaSuccess) return err;
+  // CTAs per SM: the format's figure, or fewer when this launch's shared memory
+  // (which grows with the batch) lets fewer reside, so the grid is one wave.  The
+  // residency is taken from the SM's shared memory, registers and threads and the
+  // kernel's own use of them.
+  int resident = 0;
+  err = resident_ctas(reinterpret_cast<const void*>(kern), (F::kConsumers + 1) * 32, smem,
+                      &resident);
+  if (err != cudaSuccess) return err;
+  const int grid = num_sms * max(1, min(F::ctas_per_sm(Q), resident));
   for (int b0 = 0; b0 < B; b0 += kScoreMaxBatch) {
     ScoreArgs c = a;
     c.B = min(kScoreMaxBatch, B - b0);
