@@ -273,11 +273,17 @@ struct MxqFmt {
     int p_seq = 0, p_pg = 0, p_len = 0;
     uint32_t p_buf = 0;
     bool failed = false;
+    bool bad = false;  // this thread saw a time-out (read back)
 
     // Wait for the pending group, read its accumulator and store its scores.
-    auto read_back = [&]() -> bool {
+    // Warp-local (tcgen05.ld is a warp's own): a time-out sets `bad`, which the next
+    // page's vote turns into a stop for all consumers.
+    auto read_back = [&]() {
       const bool done = mbar_wait(smem_addr(&mma_bar[p_buf]), (phases >> p_buf) & 1u);
-      if (!mxq::all_consumers(done)) return false;
+      if (!__all_sync(0xFFFFFFFFu, done)) {
+        bad = true;
+        return;
+      }
       phases ^= 1u << p_buf;
       running &= ~(1u << p_buf);
       pending = false;
@@ -300,7 +306,6 @@ struct MxqFmt {
         }
       }
       mxq::tc_fence_before();
-      return true;
     };
 
     for (int kk = 0; kk < n; ++kk) {
@@ -310,7 +315,7 @@ struct MxqFmt {
         landed = mbar_test(smem_addr(&ring.full[st]), round & 1);
         if (!landed && *ring.abort_flag) break;
       }
-      if (!mxq::all_consumers(landed)) {
+      if (!mxq::all_consumers(landed && !bad)) {
         failed = true;
         break;
       }
@@ -320,10 +325,7 @@ struct MxqFmt {
       const int seq = ring.seq[st], pg = ring.page[st], L = ring.len[st];
       const bool ok = ring.ok[st] != 0;
       const uint8_t* stage = ring.base + st * ring.stage_bytes;
-      if (ok && seq != cur_seq && pending && !read_back()) {  // the B tile is about to change
-        failed = true;
-        break;
-      }
+      if (ok && seq != cur_seq && pending) read_back();  // the B tile is about to change
       if (ok) {
         if (seq != cur_seq) {
           set_queries<Q>(reinterpret_cast<const uint16_t*>(stage + kStageDataBytes), region, tm,
@@ -361,10 +363,7 @@ struct MxqFmt {
       } else if (tid == 0) {
         mbar_arrive(smem_addr(&ring.empty[st]));
       }
-      if (pending && !read_back()) {
-        failed = true;
-        break;
-      }
+      if (pending) read_back();
       if (ok) {
         pending = true;
         p_seq = seq;
@@ -373,9 +372,9 @@ struct MxqFmt {
         p_buf = (groups - 1u) & 1u;
       }
     }
-    if (!failed && pending && !read_back()) failed = true;
-    if (failed) {
-      if (tid == 0) flag(a.status, MX4_STATUS_TIMEOUT);
+    if (!failed && pending) read_back();
+    if (failed || bad) {
+      flag(a.status, MX4_STATUS_TIMEOUT);
       *ring.abort_flag = 1;
     }
     // teardown (every consumer gets here): no MMA group may still run when the
