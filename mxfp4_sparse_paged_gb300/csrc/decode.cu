@@ -305,7 +305,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
   int ref[4] = {0, 0, 0, 0};  // largest valid V scale byte per 32-dim block so far
   float cQ = 0.f;
   int64_t cur_t = -1;
-  const int blo = tig >> 1, bhi = blo + 2;  // scale blocks of this lane's O columns
+  const int blo = tig >> 1;  // scale block of this lane's O columns j < 8 (blo + 2 for j >= 8)
 
   auto flush = [&](int64_t t) {
     float l0 = lsum[0], l1 = lsum[1];
