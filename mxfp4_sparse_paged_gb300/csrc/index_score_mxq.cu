@@ -279,6 +279,7 @@ struct MxqFmt {
     // Warp-local (tcgen05.ld is a warp's own): a time-out sets `bad`, which the next
     // page's vote turns into a stop for all consumers.
     auto read_back = [&]() {
+      if (bad) return;  // this warp already gave up: the teardown waits (bounded) once more
       const bool done = mbar_wait(smem_addr(&mma_bar[p_buf]), (phases >> p_buf) & 1u);
       if (!__all_sync(0xFFFFFFFFu, done)) {
         bad = true;

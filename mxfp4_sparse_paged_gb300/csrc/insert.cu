@@ -89,6 +89,11 @@ insert_kernel(const float* __restrict__ k, const float* __restrict__ v,
   const int64_t t = warp / rows_per_token;
   const int r = (int)(warp % rows_per_token);
 
+  // the row and the slot are independent loads: both in flight at once
+  const float* src = r < Hkv       ? k + (t * Hkv + r) * kHeadDim
+                     : r < 2 * Hkv ? v + (t * Hkv + (r - Hkv)) * kHeadDim
+                                   : idx_k + t * kHeadDim;
+  const float4 x = reinterpret_cast<const float4*>(src)[lane];
   const int64_t slot = slot_mapping[t];
   if (slot < 0) return;
   const int64_t page = slot / kPageTokens;
@@ -97,21 +102,11 @@ insert_kernel(const float* __restrict__ k, const float* __restrict__ v,
     if (lane == 0) flag(status, MX4_STATUS_BAD_SLOT);
     return;
   }
-
-  const float* src;
-  uint8_t* dst;
-  if (r < Hkv) {
-    src = k + (t * Hkv + r) * kHeadDim;
-    dst = k_pages + page * kv_page_stride + (int64_t)r * kv_head_stride;
-  } else if (r < 2 * Hkv) {
-    src = v + (t * Hkv + (r - Hkv)) * kHeadDim;
-    dst = v_pages + page * kv_page_stride + (int64_t)(r - Hkv) * kv_head_stride;
-  } else {
-    src = idx_k + t * kHeadDim;
-    dst = idx_pages + page * idx_page_stride;
-  }
-
-  quantize_store_row(reinterpret_cast<const float4*>(src)[lane], lane, dst, row, status);
+  uint8_t* const dst =
+      r < Hkv       ? k_pages + page * kv_page_stride + (int64_t)r * kv_head_stride
+      : r < 2 * Hkv ? v_pages + page * kv_page_stride + (int64_t)(r - Hkv) * kv_head_stride
+                    : idx_pages + page * idx_page_stride;
+  quantize_store_row(x, lane, dst, row, status);
 }
 
 cudaError_t launch_insert(const float* k, const float* v, const float* idx_k, int64_t T, int Hkv,
