@@ -181,7 +181,16 @@ norm_rope_insert_kernel(const float* __restrict__ q, const float* __restrict__ i
   if (warp >= T * rows_per_token) return;
   const int64_t t = warp / rows_per_token;
   const int r = (int)(warp % rows_per_token);
+  const int rk = r - H - 1;  // 0 .. 2 Hkv: K heads, V heads, index-k
+  // the row, the position and the slot are independent loads: all in flight at once
+  const float* src = r < H          ? q + (t * H + r) * kHeadDim
+                     : r == H       ? iq + t * kHeadDim
+                     : rk < Hkv     ? k + (t * Hkv + rk) * kHeadDim
+                     : rk < 2 * Hkv ? v + (t * Hkv + (rk - Hkv)) * kHeadDim
+                                    : idx_k + t * kHeadDim;
+  const float4 xr = reinterpret_cast<const float4*>(src)[lane];
   const int64_t pos = positions[t];
+  const int64_t slot = r > H ? slot_mapping[t] : 0;
   if (pos < 0 || pos >= max_pos) {
     if (lane == 0) flag(status, MX4_STATUS_BAD_INDEX);
     return;
@@ -190,17 +199,14 @@ norm_rope_insert_kernel(const float* __restrict__ q, const float* __restrict__ i
 
   if (r <= H) {  // q head r, or (r == H) the index-q head: bf16 out
     const bool isq = r < H;
-    const float* src = isq ? q + (t * H + r) * kHeadDim : iq + t * kHeadDim;
     uint16_t* dst = isq ? q_out + (t * H + r) * kHeadDim : iq_out + t * kHeadDim;
-    const float4 y = norm_rope_row(reinterpret_cast<const float4*>(src)[lane], lane,
-                                   isq ? g_q : g_iq, cs, eps, true);
+    const float4 y = norm_rope_row(xr, lane, isq ? g_q : g_iq, cs, eps, true);
     const __nv_bfloat162 lo = __floats2bfloat162_rn(y.x, y.y), hi = __floats2bfloat162_rn(y.z, y.w);
     reinterpret_cast<uint2*>(dst)[lane] =
         make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
     return;
   }
 
-  const int64_t slot = slot_mapping[t];
   if (slot < 0) return;
   const int64_t page = slot / kPageTokens;
   const int row = (int)(slot % kPageTokens);
@@ -208,19 +214,16 @@ norm_rope_insert_kernel(const float* __restrict__ q, const float* __restrict__ i
     if (lane == 0) flag(status, MX4_STATUS_BAD_SLOT);
     return;
   }
-  const int rk = r - H - 1;  // 0 .. 2 Hkv: K heads, V heads, index-k
   float4 x;
   uint8_t* dst;
   if (rk < Hkv) {
-    x = norm_rope_row(reinterpret_cast<const float4*>(k + (t * Hkv + rk) * kHeadDim)[lane], lane,
-                      g_k, cs, eps, true);
+    x = norm_rope_row(xr, lane, g_k, cs, eps, true);
     dst = k_pages + page * kv_page_stride + (int64_t)rk * kv_head_stride;
   } else if (rk < 2 * Hkv) {
-    x = reinterpret_cast<const float4*>(v + (t * Hkv + (rk - Hkv)) * kHeadDim)[lane];
+    x = xr;
     dst = v_pages + page * kv_page_stride + (int64_t)(rk - Hkv) * kv_head_stride;
   } else {
-    x = norm_rope_row(reinterpret_cast<const float4*>(idx_k + t * kHeadDim)[lane], lane, g_ik, cs,
-                      eps, true);
+    x = norm_rope_row(xr, lane, g_ik, cs, eps, true);
     dst = idx_pages + page * idx_page_stride;
   }
   quantize_store_row(x, lane, dst, row, status);
