@@ -58,7 +58,6 @@ static_assert(kTileBytes % 16 == 0, "16-byte aligned tiles");
 
 struct WarpSmem {
   uint8_t slot[kRing][kTileBytes];  // the ring of gathered tiles
-  uint4 qfrag[8][32];               // Q A fragments of the current token, per k16 slice and lane
   float4 kf[kTile];                 // K scale factors 2^(s_b - 127) * cQ of the tile computed
   uint16_t vm16[4][kTile];          // f16 V multipliers [block][entry] of that tile
   uint32_t okm[kRing];              // valid-entry mask (bit 2e) of each slot
@@ -138,12 +137,13 @@ struct DecodeArgs {
   float scale;
 };
 
-// Q of token t as f16 A fragments, into this warp's qfrag: bf16 scaled by 2^sigma
-// so the largest magnitude lands in [2^14, 2^15).  The conversion is exact for
-// every element whose exponent is at most 31 below the largest one's; smaller
-// elements round on the f16 subnormal grid (2^-24 after scaling).  Returns sigma.
+// Q of token t as this lane's f16 A fragments (qf[k16 slice]), held in registers for
+// the token's tiles: bf16 scaled by 2^sigma so the largest magnitude lands in
+// [2^14, 2^15).  The conversion is exact for every element whose exponent is at most
+// 31 below the largest one's; smaller elements round on the f16 subnormal grid
+// (2^-24 after scaling).  Returns sigma.
 __device__ __forceinline__ int load_q_fragments(const uint16_t* __restrict__ q, int64_t t,
-                                                WarpSmem& w, int lane) {
+                                                uint4 (&qf)[8], int lane) {
   const int g = lane >> 2, tig = lane & 3;
   uint4 qraw[2][4];
 #pragma unroll
@@ -177,7 +177,7 @@ __device__ __forceinline__ int load_q_fragments(const uint16_t* __restrict__ q, 
       // slice 2b+h: k = 2tig,2tig+1 <-> dims 32b+8tig+4h+{0,1}; k = 2tig+8,+9 <-> +{2,3}
       const uint32_t w0 = h ? qraw[0][b].z : qraw[0][b].x, w1 = h ? qraw[0][b].w : qraw[0][b].y;
       const uint32_t u0 = h ? qraw[1][b].z : qraw[1][b].x, u1 = h ? qraw[1][b].w : qraw[1][b].y;
-      w.qfrag[2 * b + h][lane] = make_uint4(
+      qf[2 * b + h] = make_uint4(
           pack_f16x2(bf16_bits_to_float(w0 & 0xFFFFu) * sc, bf16_bits_to_float(w0 >> 16) * sc),
           pack_f16x2(bf16_bits_to_float(u0 & 0xFFFFu) * sc, bf16_bits_to_float(u0 >> 16) * sc),
           pack_f16x2(bf16_bits_to_float(w1 & 0xFFFFu) * sc, bf16_bits_to_float(w1 >> 16) * sc),
@@ -305,6 +305,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
   int ref[4] = {0, 0, 0, 0};  // largest valid V scale byte per 32-dim block so far
   float cQ = 0.f;
   int64_t cur_t = -1;
+  uint4 qf[8];  // Q fragments of the current token
   const int blo = tig >> 1;  // scale block of this lane's O columns j < 8 (blo + 2 for j >= 8)
 
   auto flush = [&](int64_t t) {
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
       m_used[0] = m_used[1] = -INFINITY;
       lsum[0] = lsum[1] = 0.f;
       ref[0] = ref[1] = ref[2] = ref[3] = 0;
-      const int sigma = load_q_fragments(a.q, t, w, lane);
+      const int sigma = load_q_fragments(a.q, t, qf, lane);
       cQ = a.scale * kLog2e * pow2f(-sigma);  // logit (log2 units) = sum_b S_b 2^(s_b-127) cQ
     }
     cp_async_wait_pending<kRing - 1>();  // tile u has landed
@@ -403,7 +404,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
       float acc[2][4][4];
 #pragma unroll
       for (int b = 0; b < 4; ++b) {
-        const uint4 qa0 = w.qfrag[2 * b][lane], qa1 = w.qfrag[2 * b + 1][lane];
+        const uint4 qa0 = qf[2 * b], qa1 = qf[2 * b + 1];
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
           acc[nt][b][0] = acc[nt][b][1] = acc[nt][b][2] = acc[nt][b][3] = 0.f;
