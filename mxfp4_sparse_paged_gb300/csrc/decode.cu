@@ -26,7 +26,7 @@
 //   S = Q K^T with one accumulator per 32-dim scale block (K codes by the exact
 //   hardware e2m1 -> f16 conversion; the K scales applied in fp32);
 //   online softmax in log2 units with lazy rescaling (weights scaled by 2^7 so
-//   the f16 P stays normal); P split into f16 hi + lo parts so P V keeps about
+//   the f16 P stays normal; powers of two by the hardware's approximate exp2); P split into f16 hi + lo parts so P V keeps about
 //   22 bits; O += P V with V fragments built by zipping the nibbles of two
 //   entries, times exact f16 multipliers 2^(scale - reference), where the
 //   reference is the warp's running largest scale byte per 32-dim block (O is
@@ -184,6 +184,14 @@ __device__ __forceinline__ int load_q_fragments(const uint16_t* __restrict__ q, 
           pack_f16x2(bf16_bits_to_float(u1 & 0xFFFFu) * sc, bf16_bits_to_float(u1 >> 16) * sc));
     }
   return sigma;
+}
+
+// 2^x by the hardware's approximate base-2 exponential (PTX ex2.approx, flushing
+// subnormal results to zero); 2^-inf = +0.
+__device__ __forceinline__ float ex2_hw(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // 2^e as fp32 for e <= 127 (0 below the normal range).
@@ -449,7 +457,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
           const float nm = mx[rr] > m_used[rr] + kLazy ? mx[rr] : m_used[rr];
-          corr[rr] = (nm == m_used[rr]) ? 1.f : exp2f(m_used[rr] - nm);
+          corr[rr] = (nm == m_used[rr]) ? 1.f : ex2_hw(m_used[rr] - nm);
           m_used[rr] = nm;
           lsum[rr] *= corr[rr];
         }
@@ -467,10 +475,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_split_kernel(const Deco
       float pw[2][4];
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt) {
-        pw[nt][0] = exp2f(lg[nt][0] - mb0) * kPScale;
-        pw[nt][1] = exp2f(lg[nt][1] - mb0) * kPScale;
-        pw[nt][2] = exp2f(lg[nt][2] - mb1) * kPScale;
-        pw[nt][3] = exp2f(lg[nt][3] - mb1) * kPScale;
+        pw[nt][0] = ex2_hw(lg[nt][0] - mb0) * kPScale;
+        pw[nt][1] = ex2_hw(lg[nt][1] - mb0) * kPScale;
+        pw[nt][2] = ex2_hw(lg[nt][2] - mb1) * kPScale;
+        pw[nt][3] = ex2_hw(lg[nt][3] - mb1) * kPScale;
       }
       lsum[0] += (pw[0][0] + pw[0][1]) + (pw[1][0] + pw[1][1]);
       lsum[1] += (pw[0][2] + pw[0][3]) + (pw[1][2] + pw[1][3]);
